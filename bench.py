@@ -1,0 +1,531 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched-prefill projection over block-quantized weights.
+
+One step = one transformer layer's seven projections (q, k, v, o, gate, up,
+down) over one prompt, with the dequantization fused into each GEMM.  The
+default workload is the Qwen3-8B-shaped layer with Q2_K weights (Q6_K down
+projection) and an 8,192-token prompt; inputs are seeded synthetic tensors.
+The line printed reports whole-job TFLOP/s (and tok/s, % of the dense fp16
+tensor peak), the dominant kernel against its roofline, an end-to-end figure
+through the C ABI with host buffers, the CPU oracle timed on the host cores,
+and (rank 0 only) the remaining rows of the path: standalone dequant GB/s,
+the Qwen3-1.7B-shaped layer and the 31,258-token chunked prefill in fused and
+cached-f16 modes.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qp|reference]
+
+With N > 1 it runs under torch.distributed (one process per GPU): every rank
+processes its own prompt with the same weights (weak scaling, no collective
+on the data path); the step time is the max over ranks.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import workloads  # noqa: E402
+
+METRIC = "fused dequant-GEMM prefill TFLOP/s & tok/s (% dense-FP16 peak); dequant HBM GB/s"
+DEFAULT_WORKLOAD = "qwen3_8b_q2k_q6k_t8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of the dominant kernel per launch, from one ncu capture of the
+# kernel source whose hash is recorded; reported only while the source is
+# unchanged.  (bytes per launch of the Q2_K 4096x4096 projection at T=8192)
+NCU_TRAFFIC = {"source_sha": None, "bytes_per_launch": None, "what": None}
+KERNEL_SOURCES = ["block_quantized_weight_qp_gb300/csrc/qgemm.cu",
+                  "block_quantized_weight_qp_gb300/csrc/qp_ptx.cuh"]
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (the step time the job reports)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, world, device=None):
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_throughput(units_per_rank, world, max_ms):
+    """Units all ranks processed / the slowest rank's time (per second)."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
+# ------------------------------------------------------------------ peaks --
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (ctypes)
+    every few milliseconds while running.  Reads only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, index, period_s=0.005):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self.max_mhz = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            m = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _sample(self):
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(c)) != 0:
+            return
+        self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(r))
+        self.samples.append((c.value, r.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = [c for c, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------- GPU arm ----
+
+class Layer:
+    """Weights and inputs of one workload on the device."""
+
+    def __init__(self, wl, rank, device, need_f16=False):
+        import torch
+        self.wl = wl
+        self.T = wl["T"]
+        dims = workloads.input_dims(wl)
+        self.X_host = {k: synth.normal_f16((self.T, dims[k]), seed=wl["seed"] + 7919 * rank, tensor=1000 + i)
+                       for i, k in enumerate(("h", "o", "f"))}
+        self.X = {k: torch.from_numpy(v).to(device) for k, v in self.X_host.items()}
+        self.W_host = [synth.blocks(qt, out_f, in_f, seed=wl["seed"], tensor=i)
+                       for i, (_, out_f, in_f, _, qt) in enumerate(wl["projections"])]
+        self.W = [torch.from_numpy(w).to(device) for w in self.W_host]
+        self.Y = [torch.empty((self.T, out_f), dtype=torch.float32, device=device)
+                  for (_, out_f, _, _, _) in wl["projections"]]
+        self.W16 = None
+        if need_f16:
+            import block_quantized_weight_qp_gb300 as qp
+            self.W16 = []
+            for w, (_, out_f, in_f, _, qt) in zip(self.W, wl["projections"]):
+                h = torch.empty((out_f, in_f), dtype=torch.float16, device=device)
+                qp.qp_dequant_f16(qt, w, out_f, in_f, h)
+                self.W16.append(h)
+
+    def flops(self, T=None):
+        return workloads.flops(self.wl, T)
+
+
+def run_layer(qp, layer, stream, events=None, mode="fused", chunk=None, X=None, Y=None):
+    """Launch the seven projections; events[i] = (start, end) recorded around
+    projection i when given."""
+    for i, (_, out_f, in_f, src, qt) in enumerate(layer.wl["projections"]):
+        x = layer.X[src] if X is None else X[src]
+        y = layer.Y[i] if Y is None else Y[i]
+        if events is not None:
+            events[i][0].record(stream)
+        if chunk:
+            qp.qp_prefill_chunked(qt, layer.W[i], layer.W16[i] if layer.W16 else None, out_f, in_f, x, layer.T, y,
+                                  chunk, 0 if mode == "fused" else 1, stream)
+        elif mode == "fused":
+            qp.qp_prefill_gemm(qt, layer.W[i], out_f, in_f, x, layer.T, y, stream)
+        else:
+            qp.qp_prefill_gemm_f16w(layer.W16[i], out_f, in_f, x, layer.T, y, stream)
+        if events is not None:
+            events[i][1].record(stream)
+
+
+def time_layer(qp, layer, stream, steps, warmup, mode="fused", chunk=None):
+    """Mean ms per layer pass over `steps` passes (one timed region)."""
+    import torch
+    for _ in range(warmup):
+        run_layer(qp, layer, stream, mode=mode, chunk=chunk)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run_layer(qp, layer, stream, mode=mode, chunk=chunk)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    qp.qp_check(stream)
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_dequant(qp, stream, device, iters=20):
+    """Standalone dequant GB/s (quantized bytes read + output bytes written),
+    L2 flushed before every timed launch; median of `iters`."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    cases = [("Q4_K", qp.Q4_K, 4096, 4096, 12), ("Q8_0", qp.Q8_0, 4096, 4096, 13),
+             ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15)]
+    out = {}
+    for name, qt, rows, cols, tid in cases:
+        w = torch.from_numpy(synth.blocks(qt, rows, cols, seed=1, tensor=tid)).to(device)
+        in_bytes = w.numel()
+        for f16 in (False, True):
+            y = torch.empty((rows, cols), dtype=torch.float16 if f16 else torch.float32, device=device)
+            fn = qp.qp_dequant_f16 if f16 else qp.qp_dequant_f32
+            for _ in range(3):
+                fn(qt, w, rows, cols, y, stream)
+            times = []
+            for _ in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(qt, w, rows, cols, y, stream)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            nbytes = in_bytes + y.numel() * y.element_size()
+            out["%s_%dx%d_%s" % (name, rows, cols, "f16" if f16 else "f32")] = {
+                "gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2), "bytes": nbytes}
+    qp.qp_check(stream)
+    return out
+
+
+def cpu_oracle_sample(wl, seconds=10.0, rows_max=4096):
+    """The CPU oracle as it stands on a bounded sample of the workload: it
+    dequantizes all seven weights to f32 and computes the fp64 projection for
+    a sample of token rows; the time is extrapolated linearly in rows to the
+    full prompt.  Returns the cpu_baseline object."""
+    import oracle
+    t0 = time.perf_counter()
+    Ws = [oracle.dequant_f32(qt, synth.blocks(qt, out_f, in_f, seed=wl["seed"], tensor=i), out_f, in_f)
+          for i, (_, out_f, in_f, _, qt) in enumerate(wl["projections"])]
+    t_deq = time.perf_counter() - t0
+    dims = workloads.input_dims(wl)
+    X = {k: synth.normal_f16((64, dims[k]), seed=wl["seed"], tensor=1000 + i) for i, k in enumerate(("h", "o", "f"))}
+
+    def gemm_rows(n):
+        rows = np.arange(n, dtype=np.int64)
+        t = time.perf_counter()
+        for W, (_, _, _, src, _) in zip(Ws, wl["projections"]):
+            Xs = X[src] if n <= 64 else np.resize(X[src], (n, X[src].shape[1]))
+            oracle.gemm_f64(Xs, W, rows)
+        return time.perf_counter() - t
+
+    probe = 4
+    t_probe = gemm_rows(probe)
+    n = int(min(rows_max, max(probe, (seconds - t_deq) / max(t_probe / probe, 1e-9))))
+    t_rows = gemm_rows(n) if n > probe else t_probe
+    per_row = t_rows / n
+    T = wl["T"]
+    t_full = t_deq + per_row * T
+    flops = workloads.flops(wl)
+    return {"value": round(flops / t_full / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "scalar-C oracle: f32 dequant of all 7 weights (%.2f s) + fp64 GEMM of %d token rows "
+                      "(%.2f s), extrapolated linearly to T=%d" % (t_deq, n, t_rows, T)}
+
+
+def main_qp(args):
+    import torch
+
+    import block_quantized_weight_qp_gb300 as qp
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    qp.load()
+    peaks, peak_src = load_peaks()
+    wl = workloads.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(device)
+    layer = Layer(wl, rank, device)
+    T = layer.T
+    flops = layer.flops()
+    nproj = len(wl["projections"])
+
+    # ---- timed region: K steps, per-projection events on the launch stream
+    for _ in range(args.warmup):
+        run_layer(qp, layer, stream)
+    torch.cuda.synchronize()
+    qp.qp_check(stream)
+    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nproj)]
+              for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for s in range(args.steps):
+            run_layer(qp, layer, stream, events=events[s])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    qp.qp_check(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    max_ms = max_over_ranks(ms, world, device)
+    value = job_throughput(flops, world, max_ms) / 1e12
+    tok_s = job_throughput(T, world, max_ms)
+    per_proj = []
+    for i, (name, out_f, in_f, _, qt) in enumerate(wl["projections"]):
+        t_ms = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
+        f = 2.0 * T * out_f * in_f
+        per_proj.append({"proj": name, "type": synth.NAMES[qt], "out": out_f, "in": in_f,
+                         "ms": round(statistics.mean(t_ms), 4),
+                         "tflops": round(f / (statistics.mean(t_ms) / 1e3) / 1e12, 1)})
+    # dominant kernel: the fused GEMM instantiation with the most time
+    by_type = {}
+    for p in per_proj:
+        d = by_type.setdefault(p["type"], [0.0, 0.0, 0])
+        d[0] += 2.0 * T * p["out"] * p["in"]
+        d[1] += p["ms"]
+        d[2] += 1
+    dom = max(by_type, key=lambda k: by_type[k][1])
+    achieved = by_type[dom][0] / (by_type[dom][1] / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = None
+    if NCU_TRAFFIC["source_sha"] and NCU_TRAFFIC["source_sha"] == kernel_source_sha():
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "prefill_gemm_kernel<%s> (fused dequant, tcgen05)" % dom,
+                "peak_source": "%s dense bf16 burst (fp16 runs at the bf16 rate)" % peak_src}
+
+    # ---- end to end through the C ABI with host buffers
+    Xh = {k: torch.from_numpy(v).pin_memory() for k, v in layer.X_host.items()}
+    Yh = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in layer.Y]
+    Xd = {k: torch.empty_like(v) for k, v in layer.X.items()}
+    h2d = sum(v.numel() * v.element_size() for v in Xh.values())
+    d2h = sum(y.numel() * y.element_size() for y in Yh)
+
+    def e2e_step():
+        for k in Xh:
+            Xd[k].copy_(Xh[k], non_blocking=True)
+        run_layer(qp, layer, stream, X=Xd)
+        for y_h, y_d in zip(Yh, layer.Y):
+            y_h.copy_(y_d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    qp.qp_check(stream)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
+    e2e = {"value": round(job_throughput(flops, world, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+           "tok_per_s": round(job_throughput(T, world, e2e_ms), 1)}
+    del Xh, Yh, Xd
+
+    rows = None
+    cpu = None
+    if rank == 0 and world == 1:
+        if not args.no_rows:
+            rows = {"dequant": bench_dequant(qp, stream, device)}
+            l17 = Layer(workloads.WORKLOADS["qwen3_1p7b_q4k_t2048"], rank, device)
+            ms17 = time_layer(qp, l17, stream, max(5, args.steps), 3)
+            rows["qwen3_1p7b_q4k_t2048"] = {"ms": round(ms17, 4), "tflops": round(l17.flops() / ms17 / 1e9, 1),
+                                            "tok_per_s": round(l17.T / ms17 * 1e3, 1)}
+            del l17
+            wl5 = workloads.WORKLOADS["qwen3_8b_q4k_t31258_chunk4864"]
+            l5 = Layer(wl5, rank, device, need_f16=True)
+            ms_f = time_layer(qp, l5, stream, 3, 1, mode="fused", chunk=wl5["chunk"])
+            ms_c = time_layer(qp, l5, stream, 3, 1, mode="cached", chunk=wl5["chunk"])
+            rows["qwen3_8b_q4k_t31258_chunk4864"] = {
+                "fused": {"ms": round(ms_f, 3), "tok_per_s": round(l5.T / ms_f * 1e3, 1),
+                          "tflops": round(l5.flops() / ms_f / 1e9, 1)},
+                "cached_f16": {"ms": round(ms_c, 3), "tok_per_s": round(l5.T / ms_c * 1e3, 1),
+                               "tflops": round(l5.flops() / ms_c / 1e9, 1),
+                               "note": "excludes the one-time f16 weight build"}}
+            del l5
+        if not args.no_cpu_baseline:
+            cpu = cpu_oracle_sample(wl, seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded; weights and activations drawn as the workload states)",
+            "config": {"workload": args.workload, "T": T, "tokens_per_rank": T,
+                       "projections": "q,k,v,o,gate,up (Q2_K) + down (Q6_K); hidden 4096, kv 1024, ffn 12288",
+                       "accumulate": "f32", "parallelism": "replicas x%d (weak scaling, no collective)" % world,
+                       "l2": "inputs larger than L2: each step streams %.2f GB of X, W and Y" % (
+                           (sum(v.numel() * 2 for v in layer.X.values()) + sum(w.numel() for w in layer.W)
+                            + sum(y.numel() * 4 for y in layer.Y)) / 1e9)},
+            "tok_per_s": round(tok_s, 1),
+            "pct_dense_fp16_peak": round(100.0 * value / (peak * world), 2),
+            "per_projection": per_proj,
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": args.steps * nproj,
+            "clocks": sampler.summary(),
+            "cpu_baseline": cpu,
+            "rows": rows,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------- reference arm ----
+
+def main_reference(args):
+    """The CPU oracle timed on this host's cores on the same workload and
+    metric; each step dequantizes all seven weights (f32) and computes the
+    fp64 projection for a bounded sample of token rows."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = workloads.WORKLOADS[args.workload]
+    dims = workloads.input_dims(wl)
+    n_rows = args.reference_rows
+    X = {k: synth.normal_f16((n_rows, dims[k]), seed=wl["seed"], tensor=1000 + i)
+         for i, k in enumerate(("h", "o", "f"))}
+    W_q = [synth.blocks(qt, out_f, in_f, seed=wl["seed"], tensor=i)
+           for i, (_, out_f, in_f, _, qt) in enumerate(wl["projections"])]
+    rows = np.arange(n_rows, dtype=np.int64)
+
+    def step():
+        for w, (_, out_f, in_f, src, qt) in zip(W_q, wl["projections"]):
+            W = oracle.dequant_f32(qt, w, out_f, in_f)
+            oracle.gemm_f64(X[src], W, rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = workloads.flops(wl, n_rows)
+    value = flops / dt / 1e12
+    sample = ("each step: f32 dequant of all 7 weights + fp64 GEMM of %d of the %d token rows" % (n_rows, wl["T"]))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": args.workload, "T": n_rows,
+                                                     "tokens_per_rank": n_rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["qp", "reference"], default="qp")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--no-rows", action="store_true", help="skip the other rows of the path")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--reference-rows", type=int, default=8)
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_qp(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,43 @@
+// qp_internal.h — declarations shared by the library's translation units
+// (kernel launchers called from the C-ABI layer in api.cu).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace qp {
+
+// GGUF type ids.
+constexpr int kQ8_0 = 8;
+constexpr int kQ2_K = 10;
+constexpr int kQ4_K = 12;
+constexpr int kQ6_K = 14;
+
+// Device error word bits (OR-ed by kernels, read and cleared by qp_check).
+constexpr uint32_t kErrTimeoutProducer = 1u << 0;
+constexpr uint32_t kErrTimeoutMma = 1u << 1;
+constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
+constexpr uint32_t kErrTimeoutDequant = 1u << 3;
+
+cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
+                               cudaStream_t stream, int num_sms);
+cudaError_t launch_dequant_f16(int type, const void *blocks, int64_t rows, int64_t cols, uint16_t *out,
+                               cudaStream_t stream, int num_sms);
+
+// Everything a GEMM launch needs, prepared on the host by api.cu.
+struct GemmArgs {
+    int type;              // block type, or 0 for the cached f16 weight
+    int64_t out_f, in_f, T;
+    const void *W;         // quantized blocks or fp16 weight
+    const uint16_t *X;
+    float *Y;
+    int num_sms;
+    uint32_t *err;         // device error word
+    uint64_t wait_limit_ns;
+    int inject_stall;      // test hook: >= 0 makes the producer drop that load
+};
+
+// Builds the tensor maps and launches; `encode` is cuTensorMapEncodeTiled.
+cudaError_t launch_prefill_gemm(const GemmArgs &a, void *encode_fn, cudaStream_t stream);
+
+}  // namespace qp
