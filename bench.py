@@ -177,9 +177,10 @@ class ClockSampler:
 class Layer:
     """Weights and inputs of one workload on the device."""
 
-    def __init__(self, wl, rank, device, need_f16=False):
+    def __init__(self, wl, rank, device, need_f16=False, only=None):
         import torch
         self.wl = wl
+        self.only = only
         self.T = wl["T"]
         dims = workloads.input_dims(wl)
         self.X_host = {k: synth.normal_f16((self.T, dims[k]), seed=wl["seed"] + 7919 * rank, tensor=1000 + i)
@@ -200,13 +201,17 @@ class Layer:
                 self.W16.append(h)
 
     def flops(self, T=None):
-        return workloads.flops(self.wl, T)
+        T = self.T if T is None else T
+        return sum(2 * T * out_f * in_f for name, out_f, in_f, _, _ in self.wl["projections"]
+                   if not self.only or name == self.only)
 
 
 def run_layer(qp, layer, stream, events=None, mode="fused", chunk=None, X=None, Y=None):
-    """Launch the seven projections; events[i] = (start, end) recorded around
-    projection i when given."""
-    for i, (_, out_f, in_f, src, qt) in enumerate(layer.wl["projections"]):
+    """Launch the seven projections (or the one named by layer.only);
+    events[i] = (start, end) recorded around projection i when given."""
+    for i, (name, out_f, in_f, src, qt) in enumerate(layer.wl["projections"]):
+        if layer.only and name != layer.only:
+            continue
         x = layer.X[src] if X is None else X[src]
         y = layer.Y[i] if Y is None else Y[i]
         if events is not None:
@@ -320,10 +325,11 @@ def main_qp(args):
     peaks, peak_src = load_peaks()
     wl = workloads.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(device)
-    layer = Layer(wl, rank, device)
+    layer = Layer(wl, rank, device, only=args.only_proj)
     T = layer.T
     flops = layer.flops()
     nproj = len(wl["projections"])
+    nlaunch = 1 if args.only_proj else nproj
 
     # ---- timed region: K steps, per-projection events on the launch stream
     for _ in range(args.warmup):
@@ -350,6 +356,8 @@ def main_qp(args):
     tok_s = job_throughput(T, world, max_ms)
     per_proj = []
     for i, (name, out_f, in_f, _, qt) in enumerate(wl["projections"]):
+        if args.only_proj and name != args.only_proj:
+            continue
         t_ms = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
         f = 2.0 * T * out_f * in_f
         per_proj.append({"proj": name, "type": synth.NAMES[qt], "out": out_f, "in": in_f,
@@ -387,22 +395,24 @@ def main_qp(args):
         for y_h, y_d in zip(Yh, layer.Y):
             y_h.copy_(y_d, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    qp.qp_check(stream)
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
-    e2e = {"value": round(job_throughput(flops, world, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-           "tok_per_s": round(job_throughput(T, world, e2e_ms), 1)}
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        qp.qp_check(stream)
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
+        e2e = {"value": round(job_throughput(flops, world, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+               "tok_per_s": round(job_throughput(T, world, e2e_ms), 1)}
     del Xh, Yh, Xd
 
     rows = None
@@ -446,7 +456,7 @@ def main_qp(args):
             "per_projection": per_proj,
             "roofline": roofline,
             "e2e": e2e,
-            "gpu_launches": args.steps * nproj,
+            "gpu_launches": args.steps * nlaunch,
             "clocks": sampler.summary(),
             "cpu_baseline": cpu,
             "rows": rows,
@@ -493,8 +503,8 @@ def main_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": args.workload, "T": n_rows,
-                                                     "tokens_per_rank": n_rows},
+            "data": "synthetic (seeded)", "config": {"workload": args.workload, "T": wl["T"],
+                                                     "sampled_rows_per_step": n_rows},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -511,6 +521,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--no-rows", action="store_true", help="skip the other rows of the path")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    p.add_argument("--only-proj", default=None, help="time only this projection (profiling runs)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-rows", type=int, default=8)
     a = p.parse_args(argv)
