@@ -243,35 +243,39 @@ def time_layer(qp, layer, stream, steps, warmup, mode="fused", chunk=None):
     return e0.elapsed_time(e1) / steps
 
 
-def bench_dequant(qp, stream, device, iters=20):
-    """Standalone dequant GB/s (quantized bytes read + output bytes written),
-    L2 flushed before every timed launch; median of `iters`."""
+def bench_dequant(qp, stream, device, launches=64):
+    """Standalone dequant throughput: GB/s of quantized bytes read + output
+    bytes written.  Launches run back to back over rotating input/output
+    buffer sets whose total is at least 4x the L2 size, so every launch finds
+    its data in HBM; one CUDA-event pair brackets `launches` launches."""
     import torch
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     cases = [("Q4_K", qp.Q4_K, 4096, 4096, 12), ("Q8_0", qp.Q8_0, 4096, 4096, 13),
              ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15)]
     out = {}
     for name, qt, rows, cols, tid in cases:
-        w = torch.from_numpy(synth.blocks(qt, rows, cols, seed=1, tensor=tid)).to(device)
-        in_bytes = w.numel()
+        w0 = torch.from_numpy(synth.blocks(qt, rows, cols, seed=1, tensor=tid)).to(device)
         for f16 in (False, True):
-            y = torch.empty((rows, cols), dtype=torch.float16 if f16 else torch.float32, device=device)
+            esize = 2 if f16 else 4
+            nbytes = w0.numel() + rows * cols * esize
+            nsets = max(2, -(-4 * l2 // nbytes))
+            ws = [w0.clone() for _ in range(nsets)]
+            ys = [torch.empty((rows, cols), dtype=torch.float16 if f16 else torch.float32, device=device)
+                  for _ in range(nsets)]
             fn = qp.qp_dequant_f16 if f16 else qp.qp_dequant_f32
-            for _ in range(3):
-                fn(qt, w, rows, cols, y, stream)
-            times = []
-            for _ in range(iters):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn(qt, w, rows, cols, y, stream)
-                e1.record(stream)
-                e1.synchronize()
-                times.append(e0.elapsed_time(e1))
-            ms = statistics.median(times)
-            nbytes = in_bytes + y.numel() * y.element_size()
+            for i in range(nsets):
+                fn(qt, ws[i], rows, cols, ys[i], stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(launches):
+                fn(qt, ws[i % nsets], rows, cols, ys[i % nsets], stream)
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / launches
             out["%s_%dx%d_%s" % (name, rows, cols, "f16" if f16 else "f32")] = {
-                "gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2), "bytes": nbytes}
+                "gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2), "bytes": nbytes,
+                "buffer_sets": nsets}
+            del ws, ys
     qp.qp_check(stream)
     return out
 

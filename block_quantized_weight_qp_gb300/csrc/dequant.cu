@@ -65,6 +65,21 @@ struct LaneOut {
     int64_t col0;
 };
 
+// (row, block-in-row) of flat block index g: 32-bit division when the block
+// count fits (the host picks), 64-bit otherwise.
+template <bool WIDE>
+__device__ __forceinline__ void split(int64_t g, int64_t nb, int64_t &row, int64_t &kb) {
+    if constexpr (WIDE) {
+        row = g / nb;
+        kb = g - row * nb;
+    } else {
+        const uint32_t q = static_cast<uint32_t>(g) / static_cast<uint32_t>(nb);
+        row = q;
+        kb = static_cast<uint32_t>(g) - q * static_cast<uint32_t>(nb);
+    }
+}
+
+template <bool WIDE>
 __device__ __forceinline__ LaneOut lane_q4_k(const uint8_t *blocks, int64_t group, int64_t nb, int lane,
                                              float (&y)[8]) {
     const uint8_t *b = blocks + group * 144;
@@ -91,9 +106,12 @@ __device__ __forceinline__ LaneOut lane_q4_k(const uint8_t *blocks, int64_t grou
         const uint32_t q = (byte_of(qv.x, qv.y, i) >> (high ? 4 : 0)) & 15u;
         y[i] = __fsub_rn(__fmul_rn(dl, static_cast<float>(q)), ml);
     }
-    return {group / nb, (group % nb) * 256 + 8 * lane};
+    int64_t row, kb;
+    split<WIDE>(group, nb, row, kb);
+    return {row, kb * 256 + 8 * lane};
 }
 
+template <bool WIDE>
 __device__ __forceinline__ LaneOut lane_q2_k(const uint8_t *blocks, int64_t group, int64_t nb, int lane,
                                              float (&y)[8]) {
     const uint8_t *b = blocks + group * 84;                        // 4-byte aligned
@@ -110,9 +128,12 @@ __device__ __forceinline__ LaneOut lane_q2_k(const uint8_t *blocks, int64_t grou
         const uint32_t q = (byte_of(q0, q1, i) >> (2 * j)) & 3u;
         y[i] = __fsub_rn(__fmul_rn(dl, static_cast<float>(q)), ml);
     }
-    return {group / nb, (group % nb) * 256 + 8 * lane};
+    int64_t row, kb;
+    split<WIDE>(group, nb, row, kb);
+    return {row, kb * 256 + 8 * lane};
 }
 
+template <bool WIDE>
 __device__ __forceinline__ LaneOut lane_q6_k(const uint8_t *blocks, int64_t group, int64_t nb, int lane,
                                              float (&y)[8]) {
     const uint8_t *b = blocks + group * 210;                       // 2-byte aligned
@@ -131,11 +152,14 @@ __device__ __forceinline__ LaneOut lane_q6_k(const uint8_t *blocks, int64_t grou
         const int32_t q = static_cast<int32_t>(lo | (hi << 4)) - 32;
         y[i] = __fmul_rn(dl, static_cast<float>(q));
     }
-    return {group / nb, (group % nb) * 256 + 8 * lane};
+    int64_t row, kb;
+    split<WIDE>(group, nb, row, kb);
+    return {row, kb * 256 + 8 * lane};
 }
 
 // Q8_0 groups hold eight consecutive blocks of the flat block array; lane l
 // takes values 8(l%4)..+7 of block 8*group + l/4.
+template <bool WIDE>
 __device__ __forceinline__ LaneOut lane_q8_0(const uint8_t *blocks, int64_t group, int64_t nb, int64_t nblocks,
                                              int lane, float (&y)[8]) {
     const int64_t blk = group * 8 + (lane >> 2);
@@ -150,7 +174,9 @@ __device__ __forceinline__ LaneOut lane_q8_0(const uint8_t *blocks, int64_t grou
         const int32_t q = static_cast<int8_t>(byte_of(q_lo, q_hi, i));
         y[i] = __fmul_rn(d, static_cast<float>(q));
     }
-    return {blk / nb, (blk % nb) * 32 + v0};
+    int64_t row, kb;
+    split<WIDE>(blk, nb, row, kb);
+    return {row, kb * 32 + v0};
 }
 
 // ------------------------------------------------------------------ store --
@@ -188,21 +214,35 @@ __device__ __forceinline__ void store8(uint16_t *out, int64_t cols, LaneOut o, c
 
 // ----------------------------------------------------------------- kernel --
 
-template <int TYPE, typename OutT>
+template <int TYPE, bool WIDE>
+__device__ __forceinline__ LaneOut decode_group(const uint8_t *blocks, int64_t g, int64_t nb, int64_t nblocks,
+                                                int lane, float (&y)[8]) {
+    if constexpr (TYPE == kQ4_K) return lane_q4_k<WIDE>(blocks, g, nb, lane, y);
+    else if constexpr (TYPE == kQ2_K) return lane_q2_k<WIDE>(blocks, g, nb, lane, y);
+    else if constexpr (TYPE == kQ6_K) return lane_q6_k<WIDE>(blocks, g, nb, lane, y);
+    else return lane_q8_0<WIDE>(blocks, g, nb, nblocks, lane, y);
+}
+
+// Grid-stride over groups, two groups per warp per iteration so that the
+// loads of both are in flight before either is stored.
+template <int TYPE, bool WIDE, typename OutT>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t rows, int64_t cols,
                                                       int64_t nb, OutT *__restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int64_t nblocks = rows * nb;
     const int64_t ngroups = TYPE == kQ8_0 ? (nblocks + 7) / 8 : nblocks;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); g < ngroups;
-         g += warps) {
+    int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (; g + warps < ngroups; g += 2 * warps) {
+        float y0[8], y1[8];
+        const LaneOut o0 = decode_group<TYPE, WIDE>(blocks, g, nb, nblocks, lane, y0);
+        const LaneOut o1 = decode_group<TYPE, WIDE>(blocks, g + warps, nb, nblocks, lane, y1);
+        store8(out, cols, o0, y0);
+        store8(out, cols, o1, y1);
+    }
+    if (g < ngroups) {
         float y[8];
-        LaneOut o;
-        if constexpr (TYPE == kQ4_K) o = lane_q4_k(blocks, g, nb, lane, y);
-        else if constexpr (TYPE == kQ2_K) o = lane_q2_k(blocks, g, nb, lane, y);
-        else if constexpr (TYPE == kQ6_K) o = lane_q6_k(blocks, g, nb, lane, y);
-        else o = lane_q8_0(blocks, g, nb, nblocks, lane, y);
+        const LaneOut o = decode_group<TYPE, WIDE>(blocks, g, nb, nblocks, lane, y);
         store8(out, cols, o, y);
     }
 }
@@ -215,8 +255,12 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
     const int64_t want = (ngroups + 7) / 8;                         // 8 warps per block
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;          // 8 blocks of 256 threads per SM
     const int grid = static_cast<int>(want < cap ? want : cap);
-    dequant_kernel<TYPE, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), rows, cols, nb,
-                                                           out);
+    if (rows * nb + 8 < (int64_t(1) << 32))
+        dequant_kernel<TYPE, false, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), rows, cols,
+                                                                    nb, out);
+    else
+        dequant_kernel<TYPE, true, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), rows, cols,
+                                                                   nb, out);
     return cudaGetLastError();
 }
 

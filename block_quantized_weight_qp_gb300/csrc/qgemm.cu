@@ -7,9 +7,9 @@
 //
 // Two modes share one persistent, warp-specialized kernel:
 //   FUSED  W is block-quantized.  TMA stages one superblock-wide slice of 128
-//          weight rows (raw bytes) into shared memory; four dequant warps
-//          decode it row by row into fp16, written straight into the
-//          128-byte-swizzled K-major layout the tensor cores read.
+//          weight rows (raw bytes) into shared memory; eight dequant warps
+//          decode it into fp16, written straight into the 128-byte-swizzled
+//          K-major layout the tensor cores read.
 //   F16W   W is a dense fp16 weight (the cached mode), staged by TMA.
 // Roles (one CTA per SM, tiles 128 weight rows x 256 tokens, K step 64):
 //   warp 0      TMA producer (X tiles; quantized slices or fp16 W tiles)
@@ -18,7 +18,9 @@
 //               in TMEM, double buffered (2 x 256 columns)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, fp32 stores of Y
 //               (each warp owns the 32 TMEM lanes its warp index selects)
-//   warps 6-9   dequant (FUSED only), thread i owns weight row i of the tile
+//   warps 6-13  dequant (FUSED only): warps 6-9 write the first 32 values of
+//               every 64-value K step, warps 10-13 the last 32; thread i of
+//               each group owns weight row i of the tile
 //
 // Exactness of the fused decode: every field is widened exactly, the int ->
 // float step is the exponent-bias trick (OR the integer into the mantissa of
@@ -53,20 +55,22 @@ constexpr int QSTAGES = 2;                    // quantized slices in flight
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 // Geometry of one quantized slice: SB_BYTES bytes of one row cover 256
-// values; the TMA box (BOX bytes wide, a multiple of 16) starts at the slice
+// values; the TMA box (BOX bytes wide, an odd multiple of 16 so that 16-byte
+// loads from eight consecutive rows never share a bank) starts at the slice
 // start rounded down to 16 bytes, so the slice begins REM = start % 16 bytes
 // into each smem row.
 template <int TYPE> struct QFmt;
 template <> struct QFmt<kQ4_K> { static constexpr int SB_BYTES = 144, BOX = 144; };
-template <> struct QFmt<kQ2_K> { static constexpr int SB_BYTES = 84, BOX = 96; };
-template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 224; };
+template <> struct QFmt<kQ2_K> { static constexpr int SB_BYTES = 84, BOX = 112; };
+template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 240; };
 template <> struct QFmt<kQ8_0> { static constexpr int SB_BYTES = 272, BOX = 272; };  // 8 blocks
 template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };            // fp16 weight
 
 template <int TYPE> struct Cfg {
     static constexpr bool FUSED = TYPE != 0;
     static constexpr int STAGES = FUSED ? 3 : 4;
-    static constexpr int THREADS = FUSED ? 320 : 192;
+    static constexpr int DQ_WARPS = FUSED ? 8 : 0;      // two per SM sub-partition
+    static constexpr int THREADS = (6 + DQ_WARPS) * 32;
     static constexpr int Q_SLOT_BYTES = FUSED ? BM * QFmt<TYPE>::BOX : 0;
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W = OFF_X + STAGES * X_STAGE_BYTES;
@@ -119,79 +123,158 @@ __device__ __forceinline__ void advance(int &stage, uint32_t &phase, int n) {
 }
 
 // --------------------------------------------------------- fused decoding --
+//
+// Each dequant thread owns one weight row of the tile and one half of every
+// 64-value K step ("atom"): half H produces output chunks 4H..4H+3 (values
+// 32H..32H+31 of the atom), 8 fp16 values = one 16-byte chunk at a time.
+// Quantized bytes are read from the staged slice with 16-byte shared loads
+// (row pitches are odd multiples of 16 bytes, so eight consecutive rows hit
+// eight different bank groups); misaligned fields are realigned in registers
+// with compile-time word offsets (and, for Q6_K, a run-time half-word shift).
 
 // fp16 bits (low half of h) -> f32, exact.
 __device__ __forceinline__ float h2f(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu)));
 }
 
-// Four small unsigned integers held in the bytes of u (each < 2^8) -> the
-// floats 2^23 + byte, exactly: the byte is placed in the low mantissa bits of
-// 2^23 (0x4B000000).
-__device__ __forceinline__ void bias_floats(uint32_t u, float &f0, float &f1, float &f2, float &f3) {
-    f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440));
-    f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441));
-    f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442));
-    f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443));
+// A pair of f32 values processed together: packed f32x2 instructions
+// (sm_100+) by default, plain scalar f32 operations with QP_SCALAR_PAIRS.
+// Either way every operation is an individually rounded IEEE f32 op.
+#ifndef QP_SCALAR_PAIRS
+using pair_t = uint64_t;
+
+__device__ __forceinline__ pair_t pk2(float lo, float hi) {
+    pair_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) {
+    pair_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) {
+    pair_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
+    pair_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Round a packed float pair to a packed half pair (round to nearest even).
+__device__ __forceinline__ uint32_t f2h2(pair_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
+#else
+struct pair_t {
+    float x, y;
+};
 
-// y = dl*q - ml for the 8 quant values held in the bytes of (u0, u1), packed
-// to 4 x half2.  dl*q is exact, so the fma rounds once.
-__device__ __forceinline__ uint4 chunk_affine(uint32_t u0, uint32_t u1, float dl, float ml) {
-    float f[8];
-    bias_floats(u0, f[0], f[1], f[2], f[3]);
-    bias_floats(u1, f[4], f[5], f[6], f[7]);
-    float y[8];
+__device__ __forceinline__ pair_t pk2(float lo, float hi) { return {lo, hi}; }
+__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) { return {__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)}; }
+__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) { return {__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)}; }
+__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
+    return {__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y)};
+}
+__device__ __forceinline__ uint32_t f2h2(pair_t v) {
+    const __half2 h = __floats2half2_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+#endif
+
+// Byte i (< 2^8) of u -> the float 2^23 + byte, exactly: the byte becomes the
+// low mantissa bits of 2^23 (0x4B000000).
+template <int I>
+__device__ __forceinline__ float bias_float(uint32_t u) {
+    return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440 + I));
+}
+
+// Four small integers (the bytes of u) -> four fp16 weights.
+// Two variants, both exact in f32 before the one rounding to fp16 (each call
+// handles the four values of one 32-bit word, two at a time in f32x2 form):
+//   affine: y = fma(dl, byte, -ml)          (dl*byte exact)
+//   scaled: y = dl * (byte - off)           (product exact)
+__device__ __forceinline__ uint2 word_affine(uint32_t u, pair_t dl2, pair_t nml2) {
+    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+    const pair_t b01 = pk2(bias_float<0>(u), bias_float<1>(u));
+    const pair_t b23 = pk2(bias_float<2>(u), bias_float<3>(u));
+    const pair_t q01 = fadd2(b01, nbias);                          // - 2^23, exact
+    const pair_t q23 = fadd2(b23, nbias);
+    return make_uint2(f2h2(ffma2(dl2, q01, nml2)), f2h2(ffma2(dl2, q23, nml2)));
+}
+
+__device__ __forceinline__ uint2 word_scaled(uint32_t u, pair_t dl2, pair_t nbias2) {
+    const pair_t b01 = pk2(bias_float<0>(u), bias_float<1>(u));
+    const pair_t b23 = pk2(bias_float<2>(u), bias_float<3>(u));
+    return make_uint2(f2h2(fmul2(dl2, fadd2(b01, nbias2))), f2h2(fmul2(dl2, fadd2(b23, nbias2))));
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// NW consecutive 32-bit words starting at byte OFF (+2 when hs16 == 16) of a
+// 16-byte aligned smem row, read with 16-byte loads.  OFF % 4 == 0.
+template <int OFF, int NW, bool HALF>
+__device__ __forceinline__ void row_words(const uint8_t *row, uint32_t hs16, uint32_t (&w)[NW]) {
+    static_assert(OFF % 4 == 0, "word aligned");
+    constexpr int LO = OFF & ~15;
+    constexpr int HI = (OFF + 4 * NW + (HALF ? 4 : 0) + 15) & ~15;
+    constexpr int NC = (HI - LO) / 16;
+    uint32_t c[4 * NC];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fmaf_rn(dl, __fsub_rn(f[i], 8388608.0f), -ml);
-    return make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]), pack_half2(y[4], y[5]),
-                      pack_half2(y[6], y[7]));
-}
-
-// y = dl*(byte - off) for the 8 bytes of (u0, u1); the product is exact.
-__device__ __forceinline__ uint4 chunk_scaled(uint32_t u0, uint32_t u1, float dl, float bias) {
-    float f[8];
-    bias_floats(u0, f[0], f[1], f[2], f[3]);
-    bias_floats(u1, f[4], f[5], f[6], f[7]);
-    float y[8];
+    for (int i = 0; i < NC; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + LO + 16 * i);
+        c[4 * i] = v.x;
+        c[4 * i + 1] = v.y;
+        c[4 * i + 2] = v.z;
+        c[4 * i + 3] = v.w;
+    }
+    constexpr int B = (OFF - LO) / 4;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(dl, __fsub_rn(f[i], bias));
-    return make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]), pack_half2(y[4], y[5]),
-                      pack_half2(y[6], y[7]));
+    for (int k = 0; k < NW; ++k) {
+        if constexpr (HALF) w[k] = __funnelshift_r(c[B + k], c[B + k + 1], hs16);
+        else w[k] = c[B + k];
+    }
 }
 
-// Store 16-byte chunk c (k = 8c..8c+7) of row `row` into a 128-B swizzled
-// K-major tile: physical chunk = c XOR (row mod 8).
-__device__ __forceinline__ void st_chunk(uint8_t *tile, int row, int c, uint4 v) {
-    *reinterpret_cast<uint4 *>(tile + row * 128 + ((c ^ (row & 7)) << 4)) = v;
-}
+// Output chunk addresses of this thread's row in a stage's W tile: chunk c
+// (k = 8c..8c+7) sits at row*128 + ((c ^ (row & 7)) << 4) (128-byte swizzle).
+struct ChunkAddr {
+    uint32_t off[8];
+    __device__ __forceinline__ explicit ChunkAddr(int row) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) off[c] = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+    }
+};
 
-// Word k (4 bytes at byte offset rem + 4k) of a row whose aligned start is
-// `base`; `rem` is even and uniform across the CTA for a given slice.
-__device__ __forceinline__ uint32_t ld_word_at(const uint32_t *base, int rem, int k) {
-    const int w = (rem >> 2) + k;
-    if ((rem & 3) == 0) return base[w];
-    return __funnelshift_r(base[w], base[w + 1], 16);
-}
+// Per-type decoders.  slice(): per-superblock state of this thread's row and
+// half; atom<A>(): writes chunks 4H..4H+3 of K step A (values 64A + 32H ..).
+template <int TYPE, int H, int WO> struct Dec;
 
-// Per-superblock state of one dequant thread (decoded scales).
-template <int TYPE> struct SbState;
-
-template <> struct SbState<kQ4_K> {
-    float dl[8], ml[8];
-    __device__ __forceinline__ void load(const uint8_t *row, int /*rem*/) {
+// Q4_K: sub-block 2A+H holds values 64A+32H..; they are the low (H=0) or
+// high (H=1) nibbles of qs[32A .. 32A+31].
+template <int H, int WO> struct Dec<kQ4_K, H, WO> {
+    pair_t dl2[4], nml2[4];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t) {
         const uint4 h = *reinterpret_cast<const uint4 *>(row);
         const float d = h2f(h.x), dmin = h2f(h.x >> 16);
         const uint32_t sw[3] = {h.y, h.z, h.w};
+        auto byte = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xffu; };
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
+        for (int a = 0; a < 4; ++a) {
+            const int s = 2 * a + H;
             uint32_t sc, m;
-            auto byte = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xffu; };
             if (s < 4) {
                 sc = byte(s) & 63u;
                 m = byte(s + 4) & 63u;
@@ -199,129 +282,216 @@ template <> struct SbState<kQ4_K> {
                 sc = (byte(s + 4) & 15u) | ((byte(s - 4) >> 6) << 4);
                 m = (byte(s + 4) >> 4) | ((byte(s) >> 6) << 4);
             }
-            dl[s] = __fmul_rn(d, static_cast<float>(sc));
-            ml[s] = __fmul_rn(dmin, static_cast<float>(m));
+            const float dl = __fmul_rn(d, static_cast<float>(sc));
+            const float nml = -__fmul_rn(dmin, static_cast<float>(m));
+            dl2[a] = pk2(dl, dl);
+            nml2[a] = pk2(nml, nml);
         }
     }
-    // Values 64a..64a+63: chunk c < 4 = low nibbles of qs[32a + 8c ..], sub-block 2a;
-    // chunk c >= 4 = high nibbles of qs[32a + 8(c-4) ..], sub-block 2a+1.
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, int /*rem*/, uint8_t *tile, int r) const {
-        const uint4 q0 = *reinterpret_cast<const uint4 *>(row + 16 + 32 * A);
-        const uint4 q1 = *reinterpret_cast<const uint4 *>(row + 16 + 32 * A + 16);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            st_chunk(tile, r, c,
-                     chunk_affine(w[2 * c] & 0x0F0F0F0Fu, w[2 * c + 1] & 0x0F0F0F0Fu, dl[2 * A], ml[2 * A]));
-            st_chunk(tile, r, c + 4,
-                     chunk_affine((w[2 * c] >> 4) & 0x0F0F0F0Fu, (w[2 * c + 1] >> 4) & 0x0F0F0F0Fu, dl[2 * A + 1],
-                                  ml[2 * A + 1]));
-        }
-    }
-};
-
-template <> struct SbState<kQ2_K> {
-    float d, dmin;
-    __device__ __forceinline__ void load(const uint8_t *row, int rem) {
-        const uint32_t dd = *reinterpret_cast<const uint32_t *>(row + rem + 80);
-        d = h2f(dd);
-        dmin = h2f(dd >> 16);
-    }
-    // Values 64a..: q of value 128n + 32j + l is bits 2j..2j+1 of qs[32n + l];
-    // sub-block of 16 values s = v/16 with scale byte scales[s] (sc low nibble,
-    // m high nibble).  Chunk c: j = 2(a%2) + c/4, l = 8(c%4).., s = 4a + c/2.
-    template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, int rem, uint8_t *tile, int r) const {
-        const uint32_t *rw = reinterpret_cast<const uint32_t *>(row + rem);
-        const uint32_t sw = rw[A];                             // scales[4a .. 4a+3]
-        float dl[4], ml[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t b = (sw >> (8 * k)) & 0xffu;
-            dl[k] = __fmul_rn(d, static_cast<float>(b & 15u));
-            ml[k] = __fmul_rn(dmin, static_cast<float>(b >> 4));
-        }
-        constexpr int n = A / 2;
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
         uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = rw[4 + 8 * n + k];  // qs[32n .. 32n+31]
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int j = 2 * (A % 2) + c / 4;
-            const int wl = 2 * (c % 4);
-            st_chunk(tile, r, c,
-                     chunk_affine((w[wl] >> (2 * j)) & 0x03030303u, (w[wl + 1] >> (2 * j)) & 0x03030303u,
-                                  dl[c / 2], ml[c / 2]));
-        }
-    }
-};
-
-template <> struct SbState<kQ6_K> {
-    float d;
-    __device__ __forceinline__ void load(const uint8_t *row, int rem) {
-        const uint32_t *base = reinterpret_cast<const uint32_t *>(row);
-        d = h2f(ld_word_at(base, rem, 52));                     // bytes 208..209
-    }
-    // Value 128n + 32j + l: low 4 bits = nibble (low for j < 2, high for j >= 2)
-    // of ql[64n + l + 32(j&1)], high 2 bits = bits 2j..2j+1 of qh[32n + l];
-    // sub-block s = v/16 with int8 scale.  Atom a: n = a/2, j = 2(a%2) for
-    // chunks 0-3 and 2(a%2)+1 for chunks 4-7.
-    template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, int rem, uint8_t *tile, int r) const {
-        const uint32_t *base = reinterpret_cast<const uint32_t *>(row);
-        constexpr int n = A / 2;
-        const uint32_t sw = ld_word_at(base, rem, 48 + A);     // scales[4a .. 4a+3]
-        float dl[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            dl[k] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>((sw >> (8 * k)) & 0xffu)));
-        uint32_t ql[16], qh[8];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) ql[k] = ld_word_at(base, rem, 16 * n + k);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qh[k] = ld_word_at(base, rem, 32 + 8 * n + k);
-        constexpr int nsh = (A % 2) ? 4 : 0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int j = 2 * (A % 2) + c / 4;
-            const int lw = (c / 4) * 8 + 2 * (c % 4);          // ql word: 32(j&1) + 8(c%4) bytes
-            const int hw = 2 * (c % 4);
-            const uint32_t u0 = ((ql[lw] >> nsh) & 0x0F0F0F0Fu) | (((qh[hw] >> (2 * j)) & 0x03030303u) << 4);
-            const uint32_t u1 =
-                ((ql[lw + 1] >> nsh) & 0x0F0F0F0Fu) | (((qh[hw + 1] >> (2 * j)) & 0x03030303u) << 4);
-            st_chunk(tile, r, c, chunk_scaled(u0, u1, dl[c / 2], 8388640.0f));  // 2^23 + 32
-        }
-    }
-};
-
-template <> struct SbState<kQ8_0> {
-    __device__ __forceinline__ void load(const uint8_t *, int) {}
-    // Atom a = blocks 2a and 2a+1 of the eight in the slice: bytes 68a .. 68a+67
-    // hold d0, q0[32], d1, q1[32].  q + 128 = byte ^ 0x80.
-    template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, int /*rem*/, uint8_t *tile, int r) const {
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(row) + 17 * A;
-        uint32_t v[17];
-#pragma unroll
-        for (int k = 0; k < 17; ++k) v[k] = w[k];
-        const float d0 = h2f(v[0]), d1 = h2f(v[8] >> 16);
+        row_words<16 + 32 * A, 8, false>(row, 0, w);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint32_t a0 = __funnelshift_r(v[2 * c], v[2 * c + 1], 16) ^ 0x80808080u;
-            const uint32_t a1 = __funnelshift_r(v[2 * c + 1], v[2 * c + 2], 16) ^ 0x80808080u;
-            st_chunk(tile, r, c, chunk_scaled(a0, a1, d0, 8388736.0f));          // 2^23 + 128
-            st_chunk(tile, r, c + 4,
-                     chunk_scaled(v[9 + 2 * c] ^ 0x80808080u, v[10 + 2 * c] ^ 0x80808080u, d1, 8388736.0f));
+            const uint2 lo = word_affine((w[2 * c] >> (4 * H)) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            const uint2 hi = word_affine((w[2 * c + 1] >> (4 * H)) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
         }
     }
 };
 
-template <> struct SbState<0> {
-    __device__ __forceinline__ void load(const uint8_t *, int) {}
+// Q2_K (slice starts 4*WO bytes into the staged row): value 128n + 32j + l
+// takes bits 2j..2j+1 of qs[32n + l]; sub-block s = v/16 has scale byte
+// scales[s] (sc low nibble, m high nibble).  A 4-bit sc/m pair gives each
+// sub-block only four distinct values, f16(dl*q - ml) for q = 0..3: they are
+// computed exactly once per sub-block and then selected per value with byte
+// permutes (a lookup stored as a low-byte plane and a high-byte plane).
+template <int H, int WO> struct Dec<kQ2_K, H, WO> {
+    float d, dmin;
+    uint32_t sc[4];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t) {
+        uint32_t dd[1];
+        row_words<80 + 4 * WO, 1, false>(row, 0, dd);
+        d = h2f(dd[0]);
+        dmin = h2f(dd[0] >> 16);
+        row_words<4 * WO, 4, false>(row, 0, sc);
+    }
+    // byte-planar lookup for the sub-block with scale byte b
+    __device__ __forceinline__ void lut(uint32_t b, uint32_t &plo, uint32_t &phi) const {
+        const float dl = __fmul_rn(d, static_cast<float>(b & 15u));
+        const float nml = -__fmul_rn(dmin, static_cast<float>(b >> 4));
+        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
+        const uint32_t h01 = f2h2(ffma2(dl2, pk2(0.0f, 1.0f), nml2));
+        const uint32_t h23 = f2h2(ffma2(dl2, pk2(2.0f, 3.0f), nml2));
+        plo = __byte_perm(h01, h23, 0x6420);
+        phi = __byte_perm(h01, h23, 0x7531);
+    }
+    // 4 crumb values in the bytes of u -> 2 half2
+    __device__ __forceinline__ static uint2 pick(uint32_t u, uint32_t plo, uint32_t phi) {
+        const uint32_t sel = u * 0x11u + 0x40404040u;     // byte q -> nibbles (q, q + 4)
+        return make_uint2(__byte_perm(plo, phi, sel), __byte_perm(plo, phi, sel >> 16));
+    }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *, int, uint8_t *, int) const {}
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
+        constexpr int n = A / 2, j = 2 * (A % 2) + H;
+        uint32_t w[8];
+        row_words<16 + 32 * n + 4 * WO, 8, false>(row, 0, w);
+        const uint32_t sw = sc[A];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {           // two sub-blocks of 16 values
+            uint32_t plo, phi;
+            lut((sw >> (8 * (2 * H + half))) & 0xffu, plo, phi);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
+                const uint2 lo = pick((w[2 * c] >> (2 * j)) & 0x03030303u, plo, phi);
+                const uint2 hi = pick((w[2 * c + 1] >> (2 * j)) & 0x03030303u, plo, phi);
+                sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+    }
 };
+
+// Q6_K (slice starts 4*WO + 2*(hs16/16) bytes into the staged row): value
+// 128n + 32j + l has low four bits = a nibble (low for j < 2, high for j >= 2)
+// of ql[64n + l + 32(j&1)] and high two bits = bits 2j..2j+1 of qh[32n + l];
+// sub-block s = v/16 has an int8 scale.  y = d*s*(q - 32), an exact product.
+template <int H, int WO> struct Dec<kQ6_K, H, WO> {
+    float d;
+    uint32_t sc[4];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16) {
+        uint32_t dd[1];
+        row_words<208 + 4 * WO, 1, true>(row, hs16, dd);
+        d = h2f(dd[0]);
+        row_words<192 + 4 * WO, 4, true>(row, hs16, sc);
+    }
+    template <int A>
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t hs16, uint32_t tile,
+                                         const ChunkAddr &ca) const {
+        constexpr int n = A / 2, j = 2 * (A % 2) + H;
+        constexpr int nsh = (A % 2) ? 4 : 0;             // j >= 2: high nibble
+        uint32_t ql[8], qh[8];
+        row_words<64 * n + 32 * H + 4 * WO, 8, true>(row, hs16, ql);
+        row_words<128 + 32 * n + 4 * WO, 8, true>(row, hs16, qh);
+        const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);     // -(2^23 + 32)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int8_t s = static_cast<int8_t>((sc[A] >> (8 * (2 * H + half))) & 0xffu);
+            const float dl = __fmul_rn(d, static_cast<float>(s));
+            const pair_t dl2 = pk2(dl, dl);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
+                uint32_t u[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t hbits = (j <= 2 ? (qh[2 * c + k] << (4 - 2 * j)) : (qh[2 * c + k] >> 2)) &
+                                           0x30303030u;
+                    u[k] = ((ql[2 * c + k] >> nsh) & 0x0F0F0F0Fu) | hbits;
+                }
+                const uint2 lo = word_scaled(u[0], dl2, nbias2);
+                const uint2 hi = word_scaled(u[1], dl2, nbias2);
+                sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+    }
+};
+
+// Q8_0: the slice holds eight 34-byte blocks; K step A = blocks 2A (H = 0)
+// and 2A+1 (H = 1), i.e. bytes 68A .. 68A+67 = d0, q0[32], d1, q1[32].
+// q + 128 = byte XOR 0x80.
+template <int H, int WO> struct Dec<kQ8_0, H, WO> {
+    __device__ __forceinline__ void slice(const uint8_t *, uint32_t) {}
+    template <int A>
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
+        uint32_t w[9];
+        row_words<68 * A + 32 * H, 9, false>(row, 0, w);
+        uint32_t q[8];
+        float dv;
+        if constexpr (H == 0) {              // d0 = bytes 0-1, q0 = bytes 2..33
+            dv = h2f(w[0]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[k], w[k + 1], 16);
+        } else {                             // d1 = bytes 34-35, q1 = bytes 36..67
+            dv = h2f(w[0] >> 16);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = w[k + 1];
+        }
+        const pair_t d2 = pk2(dv, dv);
+        const pair_t nbias2 = pk2(-8388736.0f, -8388736.0f);     // -(2^23 + 128)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 lo = word_scaled(q[2 * c] ^ 0x80808080u, d2, nbias2);
+            const uint2 hi = word_scaled(q[2 * c + 1] ^ 0x80808080u, d2, nbias2);
+            sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+        }
+    }
+};
+
+// One superblock slice of one half-row: four K steps, each waiting for its
+// W stage to be free, decoding into it and signalling the MMA.
+#ifdef QP_NOINLINE_SLICE
+#define QP_SLICE_INLINE __noinline__
+#else
+#define QP_SLICE_INLINE __forceinline__
+#endif
+template <int TYPE, int H, int WO>
+__device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, uint32_t ws_addr,
+                                              const ChunkAddr &ca, int lane, int &stage, uint32_t &phase,
+                                              uint64_t limit_ns, uint32_t *err) {
+    constexpr int S = Cfg<TYPE>::STAGES;
+    Dec<TYPE, H, WO> dec;
+    dec.slice(row, hs16);
+#define QP_DEQUANT_ATOM(A)                                                                                     \
+    {                                                                                                          \
+        if (!wait_phase_warp(&sh.empty[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
+            return false;                                                                                      \
+        dec.template atom<A>(row, hs16, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);            \
+        fence_proxy_async_smem();                                                                              \
+        __syncwarp();                                                                                          \
+        if (lane == 0) mbar_arrive(&sh.full[stage]);                                                           \
+        advance(stage, phase, S);                                                                              \
+    }
+    QP_DEQUANT_ATOM(0)
+    QP_DEQUANT_ATOM(1)
+    QP_DEQUANT_ATOM(2)
+    QP_DEQUANT_ATOM(3)
+#undef QP_DEQUANT_ATOM
+    return true;
+}
+
+template <int TYPE, int H>
+__device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_addr, int r,
+                                             int lane, int num_tiles, int nk, uint64_t limit_ns, uint32_t *err) {
+    using C = Cfg<TYPE>;
+    const ChunkAddr ca(r);
+    int stage = 0, qs = 0;
+    uint32_t phase = 0, qphase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb) {
+            if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) return;
+            const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
+            const int rem = (kb * QFmt<TYPE>::SB_BYTES) & 15;
+            const uint32_t hs16 = (rem & 2) ? 16u : 0u;
+            bool ok;
+            if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
+                switch (rem >> 2) {
+                case 0: ok = dequant_slice<TYPE, H, 0>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, H, 1>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, H, 2>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, H, 3>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                }
+            } else {
+                ok = dequant_slice<TYPE, H, 0>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err);
+            }
+            if (!ok) return;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.qempty[qs]);
+            advance(qs, qphase, QSTAGES);
+        }
+    }
+}
 
 // ----------------------------------------------------------------- kernel --
 
@@ -350,12 +520,14 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&sh.full[s], C::FUSED ? 1 + 4 : 1);  // TMA arrive (+ 4 dequant warps)
+            mbar_init(&sh.full[s], 1 + C::DQ_WARPS);       // TMA arrive (+ each dequant warp)
             mbar_init(&sh.empty[s], 1);                    // MMA commit
         }
-        for (int s = 0; s < QSTAGES; ++s) {
-            mbar_init(&sh.qfull[s], 1);
-            mbar_init(&sh.qempty[s], 4);
+        if constexpr (C::FUSED) {                        // quantized-slice ring (fused mode only)
+            for (int s = 0; s < QSTAGES; ++s) {
+                mbar_init(&sh.qfull[s], 1);
+                mbar_init(&sh.qempty[s], C::DQ_WARPS);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.accfull[a], 1);
@@ -484,38 +656,10 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         }
     } else if constexpr (C::FUSED) {
         // ------------------------------------------------------- dequant --
-        const int r = (warp - 6) * 32 + lane;              // weight row within the tile
-        int stage = 0, qs = 0;
-        uint32_t phase = 0, qphase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            for (int kb = 0; kb < nk; ++kb) {
-                if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant))
-                    goto dequant_done;
-                const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
-                const int rem = (kb * QFmt<TYPE>::SB_BYTES) & 15;
-                SbState<TYPE> st;
-                st.load(row, rem);
-#define QP_DEQUANT_ATOM(A)                                                                                 \
-    {                                                                                                      \
-        if (!wait_phase_warp(&sh.empty[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
-            goto dequant_done;                                                                             \
-        st.template atom<A>(row, rem, ws + stage * W_STAGE_BYTES, r);                                      \
-        fence_proxy_async_smem();                                                                          \
-        __syncwarp();                                                                                      \
-        if (lane == 0) mbar_arrive(&sh.full[stage]);                                                       \
-        advance(stage, phase, S);                                                                          \
-    }
-                QP_DEQUANT_ATOM(0)
-                QP_DEQUANT_ATOM(1)
-                QP_DEQUANT_ATOM(2)
-                QP_DEQUANT_ATOM(3)
-#undef QP_DEQUANT_ATOM
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.qempty[qs]);
-                advance(qs, qphase, QSTAGES);
-            }
-        }
-    dequant_done:;
+        const int dw = warp - 6;
+        const int r = (dw & 3) * 32 + lane;                // weight row within the tile
+        if (dw < 4) dequant_role<TYPE, 0>(sh, qslots, smem_u32(ws), r, lane, num_tiles, nk, limit_ns, err);
+        else dequant_role<TYPE, 1>(sh, qslots, smem_u32(ws), r, lane, num_tiles, nk, limit_ns, err);
     }
 
     __syncthreads();
