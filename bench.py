@@ -243,7 +243,7 @@ def time_layer(qp, layer, stream, steps, warmup, mode="fused", chunk=None):
     return e0.elapsed_time(e1) / steps
 
 
-def bench_dequant(qp, stream, device, launches=64):
+def bench_dequant(qp, stream, device, launches=64, only=None):
     """Standalone dequant throughput: GB/s of quantized bytes read + output
     bytes written.  Launches run back to back over rotating input/output
     buffer sets whose total is at least 4x the L2 size, so every launch finds
@@ -254,8 +254,12 @@ def bench_dequant(qp, stream, device, launches=64):
              ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15)]
     out = {}
     for name, qt, rows, cols, tid in cases:
+        if only and not any(o.startswith(name) for o in only):
+            continue
         w0 = torch.from_numpy(synth.blocks(qt, rows, cols, seed=1, tensor=tid)).to(device)
         for f16 in (False, True):
+            if only and "%s_%s" % (name, "f16" if f16 else "f32") not in only:
+                continue
             esize = 2 if f16 else 4
             nbytes = w0.numel() + rows * cols * esize
             nsets = max(2, -(-4 * l2 // nbytes))
@@ -315,10 +319,26 @@ def cpu_oracle_sample(wl, seconds=10.0, rows_max=4096):
                       "(%.2f s), extrapolated linearly to T=%d" % (t_deq, n, t_rows, T)}
 
 
+def main_dequant_only(args):
+    """Standalone dequant rows only (profiling runs)."""
+    import torch
+
+    import block_quantized_weight_qp_gb300 as qp
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    qp.load()
+    stream = torch.cuda.current_stream(device)
+    only = args.dequant_cases.split(",") if args.dequant_cases else None
+    rows = bench_dequant(qp, stream, device, launches=args.steps, only=only)
+    print(json.dumps({"dequant": rows}))
+
+
 def main_qp(args):
     import torch
 
     import block_quantized_weight_qp_gb300 as qp
+    if args.dequant_only:
+        return main_dequant_only(args)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -527,6 +547,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--only-proj", default=None, help="time only this projection (profiling runs)")
+    p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")
+    p.add_argument("--dequant-cases", default=None, help="e.g. Q4_K_f16,Q2_K_f32 (with --dequant-only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-rows", type=int, default=8)
     a = p.parse_args(argv)
