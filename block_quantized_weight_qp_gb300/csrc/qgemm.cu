@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "qp_decode.cuh"
 #include "qp_internal.h"
 #include "qp_ptx.cuh"
 
@@ -132,92 +133,6 @@ __device__ __forceinline__ void advance(int &stage, uint32_t &phase, int n) {
 // eight different bank groups); misaligned fields are realigned in registers
 // with compile-time word offsets (and, for Q6_K, a run-time half-word shift).
 
-// fp16 bits (low half of h) -> f32, exact.
-__device__ __forceinline__ float h2f(uint32_t h) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu)));
-}
-
-// A pair of f32 values processed together: packed f32x2 instructions
-// (sm_100+) by default, plain scalar f32 operations with QP_SCALAR_PAIRS.
-// Either way every operation is an individually rounded IEEE f32 op.
-#ifndef QP_SCALAR_PAIRS
-using pair_t = uint64_t;
-
-__device__ __forceinline__ pair_t pk2(float lo, float hi) {
-    pair_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) {
-    pair_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) {
-    pair_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
-    pair_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-// Round a packed float pair to a packed half pair (round to nearest even).
-__device__ __forceinline__ uint32_t f2h2(pair_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-#else
-struct pair_t {
-    float x, y;
-};
-
-__device__ __forceinline__ pair_t pk2(float lo, float hi) { return {lo, hi}; }
-__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) { return {__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)}; }
-__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) { return {__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)}; }
-__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
-    return {__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y)};
-}
-__device__ __forceinline__ uint32_t f2h2(pair_t v) {
-    const __half2 h = __floats2half2_rn(v.x, v.y);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-#endif
-
-// Byte i (< 2^8) of u -> the float 2^23 + byte, exactly: the byte becomes the
-// low mantissa bits of 2^23 (0x4B000000).
-template <int I>
-__device__ __forceinline__ float bias_float(uint32_t u) {
-    return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440 + I));
-}
-
-// Four small integers (the bytes of u) -> four fp16 weights.
-// Two variants, both exact in f32 before the one rounding to fp16 (each call
-// handles the four values of one 32-bit word, two at a time in f32x2 form):
-//   affine: y = fma(dl, byte, -ml)          (dl*byte exact)
-//   scaled: y = dl * (byte - off)           (product exact)
-__device__ __forceinline__ uint2 word_affine(uint32_t u, pair_t dl2, pair_t nml2) {
-    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
-    const pair_t b01 = pk2(bias_float<0>(u), bias_float<1>(u));
-    const pair_t b23 = pk2(bias_float<2>(u), bias_float<3>(u));
-    const pair_t q01 = fadd2(b01, nbias);                          // - 2^23, exact
-    const pair_t q23 = fadd2(b23, nbias);
-    return make_uint2(f2h2(ffma2(dl2, q01, nml2)), f2h2(ffma2(dl2, q23, nml2)));
-}
-
-__device__ __forceinline__ uint2 word_scaled(uint32_t u, pair_t dl2, pair_t nbias2) {
-    const pair_t b01 = pk2(bias_float<0>(u), bias_float<1>(u));
-    const pair_t b23 = pk2(bias_float<2>(u), bias_float<3>(u));
-    return make_uint2(f2h2(fmul2(dl2, fadd2(b01, nbias2))), f2h2(fmul2(dl2, fadd2(b23, nbias2))));
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -248,39 +163,43 @@ __device__ __forceinline__ void row_words(const uint8_t *row, uint32_t hs16, uin
     }
 }
 
-// Output chunk addresses of this thread's row in a stage's W tile: chunk c
-// (k = 8c..8c+7) sits at row*128 + ((c ^ (row & 7)) << 4) (128-byte swizzle).
+// Output chunk addresses of this thread's row and half in a stage's W tile:
+// chunk 4h + c (k = 32h + 8c ..) sits at row*128 + (((4h + c) ^ (row & 7)) << 4)
+// (128-byte swizzle).
 struct ChunkAddr {
-    uint32_t off[8];
-    __device__ __forceinline__ explicit ChunkAddr(int row) {
+    uint32_t off[4];
+    __device__ __forceinline__ ChunkAddr(int row, int h) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) off[c] = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+        for (int c = 0; c < 4; ++c) off[c] = static_cast<uint32_t>(row * 128 + (((4 * h + c) ^ (row & 7)) << 4));
     }
 };
 
 // Per-type decoders.  slice(): per-superblock state of this thread's row and
-// half; atom<A>(): writes chunks 4H..4H+3 of K step A (values 64A + 32H ..).
-template <int TYPE, int H, int WO> struct Dec;
+// half h; atom<A>(): writes the thread's four chunks of K step A (values
+// 64A + 32h .. 64A + 32h + 31 of the superblock).  WO = (slice start % 16)/4,
+// the slice's word offset in the staged row (Q2_K, Q6_K); hs16 = 16 when the
+// start is 2 bytes past a word (Q6_K), else 0.
+template <int TYPE, int WO> struct Dec;
 
-// Q4_K: sub-block 2A+H holds values 64A+32H..; they are the low (H=0) or
-// high (H=1) nibbles of qs[32A .. 32A+31].
-template <int H, int WO> struct Dec<kQ4_K, H, WO> {
+// Q4_K: sub-block 2A+h holds values 64A+32h..; they are the low (h=0) or
+// high (h=1) nibbles of qs[32A .. 32A+31].
+template <int WO> struct Dec<kQ4_K, WO> {
     pair_t dl2[4], nml2[4];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t) {
-        const uint4 h = *reinterpret_cast<const uint4 *>(row);
-        const float d = h2f(h.x), dmin = h2f(h.x >> 16);
-        const uint32_t sw[3] = {h.y, h.z, h.w};
-        auto byte = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xffu; };
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int h) {
+        const uint4 hd = *reinterpret_cast<const uint4 *>(row);   // d, dmin, scales[0..11]
+        const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int s = 2 * a + H;
             uint32_t sc, m;
-            if (s < 4) {
-                sc = byte(s) & 63u;
-                m = byte(s + 4) & 63u;
-            } else {
-                sc = (byte(s + 4) & 15u) | ((byte(s - 4) >> 6) << 4);
-                m = (byte(s + 4) >> 4) | ((byte(s) >> 6) << 4);
+            if (a < 2) {                                 // s = 2a + h < 4: bytes s, s + 4
+                const int sh = 8 * (2 * a + h);
+                sc = (hd.y >> sh) & 63u;
+                m = (hd.z >> sh) & 63u;
+            } else {                                     // s >= 4, t = s - 4: bytes t + 8, t, t + 4
+                const int sh = 8 * (2 * (a - 2) + h);
+                const uint32_t lo = hd.w >> sh;
+                sc = (lo & 15u) | (((hd.y >> sh) >> 6 & 3u) << 4);
+                m = ((lo >> 4) & 15u) | (((hd.z >> sh) >> 6 & 3u) << 4);
             }
             const float dl = __fmul_rn(d, static_cast<float>(sc));
             const float nml = -__fmul_rn(dmin, static_cast<float>(m));
@@ -289,33 +208,37 @@ template <int H, int WO> struct Dec<kQ4_K, H, WO> {
         }
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
+                                         const ChunkAddr &ca) const {
         uint32_t w[8];
         row_words<16 + 32 * A, 8, false>(row, 0, w);
+        const int sh = 4 * h;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint2 lo = word_affine((w[2 * c] >> (4 * H)) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-            const uint2 hi = word_affine((w[2 * c + 1] >> (4 * H)) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-            sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+            const uint2 lo = word_affine((w[2 * c] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            const uint2 hi = word_affine((w[2 * c + 1] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
         }
     }
 };
 
-// Q2_K (slice starts 4*WO bytes into the staged row): value 128n + 32j + l
-// takes bits 2j..2j+1 of qs[32n + l]; sub-block s = v/16 has scale byte
-// scales[s] (sc low nibble, m high nibble).  A 4-bit sc/m pair gives each
-// sub-block only four distinct values, f16(dl*q - ml) for q = 0..3: they are
-// computed exactly once per sub-block and then selected per value with byte
-// permutes (a lookup stored as a low-byte plane and a high-byte plane).
-template <int H, int WO> struct Dec<kQ2_K, H, WO> {
+// Q2_K: value 128n + 32j + l takes bits 2j..2j+1 of qs[32n + l]; sub-block
+// s = v/16 has scale byte scales[s] (sc low nibble, m high nibble).  A 4-bit
+// sc/m pair gives each sub-block only four distinct values, f16(dl*q - ml)
+// for q = 0..3: they are computed exactly once per sub-block and then
+// selected per value with byte permutes (a lookup stored as a low-byte plane
+// and a high-byte plane).  The thread keeps the slice's 64 qs bytes in
+// registers: K steps 2n and 2n+1 read the same bytes with different j.
+template <int WO> struct Dec<kQ2_K, WO> {
     float d, dmin;
-    uint32_t sc[4];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t) {
+    uint32_t sc[4], qs[16];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int) {
         uint32_t dd[1];
         row_words<80 + 4 * WO, 1, false>(row, 0, dd);
         d = h2f(dd[0]);
         dmin = h2f(dd[0] >> 16);
         row_words<4 * WO, 4, false>(row, 0, sc);
+        row_words<16 + 4 * WO, 16, false>(row, 0, qs);
     }
     // byte-planar lookup for the sub-block with scale byte b
     __device__ __forceinline__ void lut(uint32_t b, uint32_t &plo, uint32_t &phi) const {
@@ -333,51 +256,53 @@ template <int H, int WO> struct Dec<kQ2_K, H, WO> {
         return make_uint2(__byte_perm(plo, phi, sel), __byte_perm(plo, phi, sel >> 16));
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
-        constexpr int n = A / 2, j = 2 * (A % 2) + H;
-        uint32_t w[8];
-        row_words<16 + 32 * n + 4 * WO, 8, false>(row, 0, w);
-        const uint32_t sw = sc[A];
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
+                                         const ChunkAddr &ca) const {
+        constexpr int n = A / 2;
+        const int sh = 2 * (2 * (A % 2) + h);            // 2j
+        const uint32_t sw = sc[A] >> (16 * h);           // scale bytes of sub-blocks 4A+2h, 4A+2h+1
 #pragma unroll
         for (int half = 0; half < 2; ++half) {           // two sub-blocks of 16 values
             uint32_t plo, phi;
-            lut((sw >> (8 * (2 * H + half))) & 0xffu, plo, phi);
+            lut((sw >> (8 * half)) & 0xffu, plo, phi);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * half + cc;
-                const uint2 lo = pick((w[2 * c] >> (2 * j)) & 0x03030303u, plo, phi);
-                const uint2 hi = pick((w[2 * c + 1] >> (2 * j)) & 0x03030303u, plo, phi);
-                sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+                const uint2 lo = pick((qs[8 * n + 2 * c] >> sh) & 0x03030303u, plo, phi);
+                const uint2 hi = pick((qs[8 * n + 2 * c + 1] >> sh) & 0x03030303u, plo, phi);
+                sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
             }
         }
     }
 };
 
-// Q6_K (slice starts 4*WO + 2*(hs16/16) bytes into the staged row): value
-// 128n + 32j + l has low four bits = a nibble (low for j < 2, high for j >= 2)
-// of ql[64n + l + 32(j&1)] and high two bits = bits 2j..2j+1 of qh[32n + l];
-// sub-block s = v/16 has an int8 scale.  y = d*s*(q - 32), an exact product.
-template <int H, int WO> struct Dec<kQ6_K, H, WO> {
+// Q6_K: value 128n + 32j + l has low four bits = a nibble (low for j < 2,
+// high for j >= 2) of ql[64n + l + 32(j&1)] and high two bits = bits
+// 2j..2j+1 of qh[32n + l]; sub-block s = v/16 has an int8 scale.
+// y = d*s*(q - 32), an exact product.
+template <int WO> struct Dec<kQ6_K, WO> {
     float d;
     uint32_t sc[4];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16) {
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int) {
         uint32_t dd[1];
         row_words<208 + 4 * WO, 1, true>(row, hs16, dd);
         d = h2f(dd[0]);
         row_words<192 + 4 * WO, 4, true>(row, hs16, sc);
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t hs16, uint32_t tile,
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t hs16, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
-        constexpr int n = A / 2, j = 2 * (A % 2) + H;
+        constexpr int n = A / 2;
         constexpr int nsh = (A % 2) ? 4 : 0;             // j >= 2: high nibble
+        const int sh = 2 * (2 * (A % 2) + h);            // 2j
         uint32_t ql[8], qh[8];
-        row_words<64 * n + 32 * H + 4 * WO, 8, true>(row, hs16, ql);
+        row_words<64 * n + 4 * WO, 8, true>(row + 32 * h, hs16, ql);   // ql[64n + 32h ..]
         row_words<128 + 32 * n + 4 * WO, 8, true>(row, hs16, qh);
         const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);     // -(2^23 + 32)
+        const uint32_t sw = sc[A] >> (16 * h);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            const int8_t s = static_cast<int8_t>((sc[A] >> (8 * (2 * H + half))) & 0xffu);
+            const int8_t s = static_cast<int8_t>((sw >> (8 * half)) & 0xffu);
             const float dl = __fmul_rn(d, static_cast<float>(s));
             const pair_t dl2 = pk2(dl, dl);
 #pragma unroll
@@ -385,46 +310,37 @@ template <int H, int WO> struct Dec<kQ6_K, H, WO> {
                 const int c = 2 * half + cc;
                 uint32_t u[2];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const uint32_t hbits = (j <= 2 ? (qh[2 * c + k] << (4 - 2 * j)) : (qh[2 * c + k] >> 2)) &
-                                           0x30303030u;
-                    u[k] = ((ql[2 * c + k] >> nsh) & 0x0F0F0F0Fu) | hbits;
-                }
+                for (int k = 0; k < 2; ++k)
+                    u[k] = ((ql[2 * c + k] >> nsh) & 0x0F0F0F0Fu) | (((qh[2 * c + k] >> sh) << 4) & 0x30303030u);
                 const uint2 lo = word_scaled(u[0], dl2, nbias2);
                 const uint2 hi = word_scaled(u[1], dl2, nbias2);
-                sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+                sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
             }
         }
     }
 };
 
-// Q8_0: the slice holds eight 34-byte blocks; K step A = blocks 2A (H = 0)
-// and 2A+1 (H = 1), i.e. bytes 68A .. 68A+67 = d0, q0[32], d1, q1[32].
+// Q8_0: the slice holds eight 34-byte blocks; K step A = blocks 2A (h = 0)
+// and 2A+1 (h = 1), i.e. bytes 68A .. 68A+67 = d0, q0[32], d1, q1[32].
 // q + 128 = byte XOR 0x80.
-template <int H, int WO> struct Dec<kQ8_0, H, WO> {
-    __device__ __forceinline__ void slice(const uint8_t *, uint32_t) {}
+template <int WO> struct Dec<kQ8_0, WO> {
+    __device__ __forceinline__ void slice(const uint8_t *, uint32_t, int) {}
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, uint32_t tile, const ChunkAddr &ca) const {
-        uint32_t w[9];
-        row_words<68 * A + 32 * H, 9, false>(row, 0, w);
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
+                                         const ChunkAddr &ca) const {
+        uint32_t w[17];
+        row_words<68 * A, 17, false>(row, 0, w);
+        const float dv = h2f(h ? (w[8] >> 16) : w[0]);
         uint32_t q[8];
-        float dv;
-        if constexpr (H == 0) {              // d0 = bytes 0-1, q0 = bytes 2..33
-            dv = h2f(w[0]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[k], w[k + 1], 16);
-        } else {                             // d1 = bytes 34-35, q1 = bytes 36..67
-            dv = h2f(w[0] >> 16);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) q[k] = w[k + 1];
-        }
+        for (int k = 0; k < 8; ++k) q[k] = h ? w[k + 9] : __funnelshift_r(w[k], w[k + 1], 16);
         const pair_t d2 = pk2(dv, dv);
         const pair_t nbias2 = pk2(-8388736.0f, -8388736.0f);     // -(2^23 + 128)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint2 lo = word_scaled(q[2 * c] ^ 0x80808080u, d2, nbias2);
             const uint2 hi = word_scaled(q[2 * c + 1] ^ 0x80808080u, d2, nbias2);
-            sts128(tile + ca.off[4 * H + c], lo.x, lo.y, hi.x, hi.y);
+            sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
         }
     }
 };
@@ -436,18 +352,18 @@ template <int H, int WO> struct Dec<kQ8_0, H, WO> {
 #else
 #define QP_SLICE_INLINE __forceinline__
 #endif
-template <int TYPE, int H, int WO>
-__device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, uint32_t ws_addr,
-                                              const ChunkAddr &ca, int lane, int &stage, uint32_t &phase,
-                                              uint64_t limit_ns, uint32_t *err) {
+template <int TYPE, int WO>
+__device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int h,
+                                              uint32_t ws_addr, const ChunkAddr &ca, int lane, int &stage,
+                                              uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
     constexpr int S = Cfg<TYPE>::STAGES;
-    Dec<TYPE, H, WO> dec;
-    dec.slice(row, hs16);
+    Dec<TYPE, WO> dec;
+    dec.slice(row, hs16, h);
 #define QP_DEQUANT_ATOM(A)                                                                                     \
     {                                                                                                          \
         if (!wait_phase_warp(&sh.empty[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
             return false;                                                                                      \
-        dec.template atom<A>(row, hs16, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);            \
+        dec.template atom<A>(row, hs16, h, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
         fence_proxy_async_smem();                                                                              \
         __syncwarp();                                                                                          \
         if (lane == 0) mbar_arrive(&sh.full[stage]);                                                           \
@@ -461,11 +377,12 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
     return true;
 }
 
-template <int TYPE, int H>
+template <int TYPE>
 __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_addr, int r,
-                                             int lane, int num_tiles, int nk, uint64_t limit_ns, uint32_t *err) {
+                                             int h, int lane, int num_tiles, int nk, uint64_t limit_ns,
+                                             uint32_t *err) {
     using C = Cfg<TYPE>;
-    const ChunkAddr ca(r);
+    const ChunkAddr ca(r, h);
     int stage = 0, qs = 0;
     uint32_t phase = 0, qphase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -477,13 +394,13 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qs
             bool ok;
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = dequant_slice<TYPE, H, 0>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 1: ok = dequant_slice<TYPE, H, 1>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 2: ok = dequant_slice<TYPE, H, 2>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                default: ok = dequant_slice<TYPE, H, 3>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = dequant_slice<TYPE, H, 0>(sh, row, hs16, ws_addr, ca, lane, stage, phase, limit_ns, err);
+                ok = dequant_slice<TYPE, 0>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err);
             }
             if (!ok) return;
             __syncwarp();
@@ -658,8 +575,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         // ------------------------------------------------------- dequant --
         const int dw = warp - 6;
         const int r = (dw & 3) * 32 + lane;                // weight row within the tile
-        if (dw < 4) dequant_role<TYPE, 0>(sh, qslots, smem_u32(ws), r, lane, num_tiles, nk, limit_ns, err);
-        else dequant_role<TYPE, 1>(sh, qslots, smem_u32(ws), r, lane, num_tiles, nk, limit_ns, err);
+        dequant_role<TYPE>(sh, qslots, smem_u32(ws), r, dw >> 2, lane, num_tiles, nk, limit_ns, err);
     }
 
     __syncthreads();

@@ -1,0 +1,129 @@
+// qp_decode.cuh — exact per-value arithmetic shared by the dequant kernels
+// and the fused GEMM's decode warps.
+//
+// A quantized field q (a small unsigned integer held in one byte of a 32-bit
+// word) becomes the float 2^23 + q by placing the byte in the low mantissa
+// bits of 2^23 (0x4B000000) with one byte permute; subtracting 2^23 (or
+// 2^23 + offset) is exact.  The weight is then one fma / mul whose product is
+// exact for these formats (at most 24 significant bits), so each value is
+// rounded once in f32, as the value formula evaluated with separately rounded
+// f32 operations would be.  f16 results are round-to-nearest-even of that f32.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace qp {
+
+// fp16 bits (low half of h) -> f32, exact.
+__device__ __forceinline__ float h2f(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu)));
+}
+
+// A pair of f32 values processed together: packed f32x2 instructions
+// (sm_100+) by default, plain scalar f32 operations with QP_SCALAR_PAIRS.
+// Either way every operation is an individually rounded IEEE f32 op.
+#ifndef QP_SCALAR_PAIRS
+using pair_t = uint64_t;
+
+__device__ __forceinline__ pair_t pk2(float lo, float hi) {
+    pair_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) {
+    pair_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) {
+    pair_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
+    pair_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Round a packed float pair to a packed half pair (round to nearest even).
+__device__ __forceinline__ uint32_t f2h2(pair_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+#else
+struct pair_t {
+    float x, y;
+};
+
+__device__ __forceinline__ pair_t pk2(float lo, float hi) { return {lo, hi}; }
+__device__ __forceinline__ pair_t fadd2(pair_t a, pair_t b) { return {__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)}; }
+__device__ __forceinline__ pair_t fmul2(pair_t a, pair_t b) { return {__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)}; }
+__device__ __forceinline__ pair_t ffma2(pair_t a, pair_t b, pair_t c) {
+    return {__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y)};
+}
+__device__ __forceinline__ uint32_t f2h2(pair_t v) {
+    const __half2 h = __floats2half2_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+#endif
+
+// Byte i (< 2^8) of u -> the float 2^23 + byte, exactly: the byte becomes the
+// low mantissa bits of 2^23 (0x4B000000).
+template <int I>
+__device__ __forceinline__ float bias_float(uint32_t u) {
+    return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440 + I));
+}
+
+// Unpack a pair into two floats.
+#ifndef QP_SCALAR_PAIRS
+__device__ __forceinline__ void unpk2(pair_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+#else
+__device__ __forceinline__ void unpk2(pair_t v, float &lo, float &hi) {
+    lo = v.x;
+    hi = v.y;
+}
+#endif
+
+// Four small integers (the bytes of u) -> four weights, as two f32 pairs.
+//   affine: y = fma(dl, byte, -ml)      (dl*byte exact)
+//   scaled: y = dl * (byte + nbias)     (nbias = -(2^23 + offset); product exact)
+__device__ __forceinline__ void affine4(uint32_t u, pair_t dl2, pair_t nml2, pair_t &y01, pair_t &y23) {
+    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+    const pair_t q01 = fadd2(pk2(bias_float<0>(u), bias_float<1>(u)), nbias);   // exact
+    const pair_t q23 = fadd2(pk2(bias_float<2>(u), bias_float<3>(u)), nbias);
+    y01 = ffma2(dl2, q01, nml2);
+    y23 = ffma2(dl2, q23, nml2);
+}
+
+__device__ __forceinline__ void scaled4(uint32_t u, pair_t dl2, pair_t nbias2, pair_t &y01, pair_t &y23) {
+    y01 = fmul2(dl2, fadd2(pk2(bias_float<0>(u), bias_float<1>(u)), nbias2));
+    y23 = fmul2(dl2, fadd2(pk2(bias_float<2>(u), bias_float<3>(u)), nbias2));
+}
+
+// The same, rounded to four fp16 (two half2 words).
+__device__ __forceinline__ uint2 word_affine(uint32_t u, pair_t dl2, pair_t nml2) {
+    pair_t a, b;
+    affine4(u, dl2, nml2, a, b);
+    return make_uint2(f2h2(a), f2h2(b));
+}
+
+__device__ __forceinline__ uint2 word_scaled(uint32_t u, pair_t dl2, pair_t nbias2) {
+    pair_t a, b;
+    scaled4(u, dl2, nbias2, a, b);
+    return make_uint2(f2h2(a), f2h2(b));
+}
+
+// Small integer (< 2^23) -> float, exactly.
+__device__ __forceinline__ float u2f_exact(uint32_t v) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | v), 8388608.0f);
+}
+
+}  // namespace qp
