@@ -412,12 +412,32 @@ def main_qp(args):
     h2d = sum(v.numel() * v.element_size() for v in Xh.values())
     d2h = sum(y.numel() * y.element_size() for y in Yh)
 
+    # Host->device copies of X run on one copy stream and the device->host read
+    # of each projection's Y on another as soon as that projection is done,
+    # so both directions overlap the GEMMs; steps do not overlap each other.
+    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
     def e2e_step():
-        for k in Xh:
-            Xd[k].copy_(Xh[k], non_blocking=True)
-        run_layer(qp, layer, stream, X=Xd)
-        for y_h, y_d in zip(Yh, layer.Y):
-            y_h.copy_(y_d, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(stream)
+        h2d_s.wait_event(start)
+        ready = {}
+        with torch.cuda.stream(h2d_s):
+            for k in ("h", "o", "f"):
+                Xd[k].copy_(Xh[k], non_blocking=True)
+                ready[k] = torch.cuda.Event()
+                ready[k].record(h2d_s)
+        for i, (name, out_f, in_f, src, qt) in enumerate(wl["projections"]):
+            if args.only_proj and name != args.only_proj:
+                continue
+            stream.wait_event(ready[src])
+            qp.qp_prefill_gemm(qt, layer.W[i], out_f, in_f, Xd[src], T, layer.Y[i], stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h_s.wait_event(done)
+            with torch.cuda.stream(d2h_s):
+                Yh[i].copy_(layer.Y[i], non_blocking=True)
+        stream.wait_stream(d2h_s)
 
     e2e = None
     if not args.no_e2e:
