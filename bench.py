@@ -349,7 +349,7 @@ def main_qp(args):
     peaks, peak_src = load_peaks()
     wl = workloads.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(device)
-    layer = Layer(wl, rank, device, only=args.only_proj)
+    layer = Layer(wl, rank, device, need_f16=args.mode == "cached", only=args.only_proj)
     T = layer.T
     flops = layer.flops()
     nproj = len(wl["projections"])
@@ -357,7 +357,7 @@ def main_qp(args):
 
     # ---- timed region: K steps, per-projection events on the launch stream
     for _ in range(args.warmup):
-        run_layer(qp, layer, stream)
+        run_layer(qp, layer, stream, mode=args.mode)
     torch.cuda.synchronize()
     qp.qp_check(stream)
     events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nproj)]
@@ -369,7 +369,7 @@ def main_qp(args):
     with sampler:
         e0.record(stream)
         for s in range(args.steps):
-            run_layer(qp, layer, stream, events=events[s])
+            run_layer(qp, layer, stream, events=events[s], mode=args.mode)
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -402,7 +402,8 @@ def main_qp(args):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "prefill_gemm_kernel<%s> (fused dequant, tcgen05)" % dom,
+                "kernel": ("prefill_gemm_kernel<%s> (fused dequant, tcgen05)" % dom if args.mode == "fused"
+                           else "prefill_gemm_kernel<f16 weight> (cached mode, tcgen05)"),
                 "peak_source": "%s dense bf16 burst (fp16 runs at the bf16 rate)" % peak_src}
 
     # ---- end to end through the C ABI with host buffers
@@ -440,7 +441,7 @@ def main_qp(args):
         stream.wait_stream(d2h_s)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.mode == "fused":
         e2e_steps = max(3, min(args.steps, 10))
         for _ in range(2):
             e2e_step()
@@ -489,7 +490,7 @@ def main_qp(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded; weights and activations drawn as the workload states)",
-            "config": {"workload": args.workload, "T": T, "tokens_per_rank": T,
+            "config": {"workload": args.workload, "T": T, "tokens_per_rank": T, "mode": args.mode,
                        "projections": "q,k,v,o,gate,up (Q2_K) + down (Q6_K); hidden 4096, kv 1024, ffn 12288",
                        "accumulate": "f32", "parallelism": "replicas x%d (weak scaling, no collective)" % world,
                        "l2": "inputs larger than L2: each step streams %.2f GB of X, W and Y" % (
@@ -567,6 +568,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--only-proj", default=None, help="time only this projection (profiling runs)")
+    p.add_argument("--mode", choices=["fused", "cached"], default="fused",
+                   help="cached: the same step over f16 weights made once by qp_dequant_f16")
     p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")
     p.add_argument("--dequant-cases", default=None, help="e.g. Q4_K_f16,Q2_K_f32 (with --dequant-only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -40,10 +40,11 @@ class QPError(RuntimeError):
 
 
 def load():
-    """Build (if stale) and load libqp.so; raises if it cannot."""
+    """Build (if stale) and load libqp.so; raises if it cannot.  QP_LIBRARY
+    names another build of the same sources to load instead."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = os.environ.get("QP_LIBRARY") or _build.build()
         lib = ctypes.CDLL(path)
         i, i64, u64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
         lib.qp_status_str.argtypes = [i]
@@ -70,7 +71,7 @@ def load():
 
 
 def library_path():
-    return _build.LIB
+    return os.environ.get("QP_LIBRARY") or _build.LIB
 
 
 def _ptr(x):

@@ -18,9 +18,10 @@
 //               in TMEM, double buffered (2 x 256 columns)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, fp32 stores of Y
 //               (each warp owns the 32 TMEM lanes its warp index selects)
-//   warps 6-13  dequant (FUSED only): warps 6-9 write the first 32 values of
-//               every 64-value K step, warps 10-13 the last 32; thread i of
-//               each group owns weight row i of the tile
+//   warps 6-15  dequant (FUSED only; 9 and 13 idle, so no decode work shares
+//               the MMA thread's SM sub-partition): unit u = 0..7 decodes
+//               weight rows 32(u%4)..+31, values 32(u/4)..+31 of every
+//               64-value K step
 //
 // Exactness of the fused decode: every field is widened exactly, the int ->
 // float step is the exponent-bias trick (OR the integer into the mantissa of
@@ -67,25 +68,41 @@ template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 240;
 template <> struct QFmt<kQ8_0> { static constexpr int SB_BYTES = 272, BOX = 272; };  // 8 blocks
 template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };            // fp16 weight
 
+// Pipeline depths.  X tiles (TMA) and fp16 W tiles (written by the dequant
+// warps in fused mode) have rings of their own, so X can be prefetched deeper
+// than the decode runs ahead; the cached mode stages X and W together.
+// Shared memory: XST * 32 KiB + WST * 16 KiB + 2 quantized slices, <= 227 KiB.
+template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3; };   // Q4_K, Q2_K
+template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 2; };
+template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3; };
+template <> struct Depth<0> { static constexpr int XST = 4, WST = 4; };
+
 template <int TYPE> struct Cfg {
     static constexpr bool FUSED = TYPE != 0;
-    static constexpr int STAGES = FUSED ? 3 : 4;
-    static constexpr int DQ_WARPS = FUSED ? 8 : 0;      // two per SM sub-partition
-    static constexpr int THREADS = (6 + DQ_WARPS) * 32;
+    static constexpr int XST = Depth<TYPE>::XST;
+    static constexpr int WST = Depth<TYPE>::WST;
+    // Dequant warps sit only on SM sub-partitions 0, 2 and 3 (warp w runs on
+    // sub-partition w % 4): sub-partition 1 keeps its issue slots for the
+    // single MMA-issuing thread of warp 1.  Warps 6..15 minus 9 and 13.
+    static constexpr int DQ_WARPS = FUSED ? 8 : 0;
+    static constexpr int THREADS = FUSED ? 16 * 32 : 6 * 32;
     static constexpr int Q_SLOT_BYTES = FUSED ? BM * QFmt<TYPE>::BOX : 0;
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_W = OFF_X + STAGES * X_STAGE_BYTES;
-    static constexpr int OFF_Q = OFF_W + STAGES * W_STAGE_BYTES;
+    static constexpr int OFF_W = OFF_X + XST * X_STAGE_BYTES;
+    static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_Q + (FUSED ? QSTAGES * Q_SLOT_BYTES : 0);
-    // barriers: full[S], empty[S], qfull[Q], qempty[Q], accfull[2], accempty[2], done
-    static constexpr int NBAR = 2 * STAGES + 2 * QSTAGES + 5;
+    // barriers: fullx[XST], emptyx[XST], fullw[WST], emptyw[WST], qfull[Q], qempty[Q],
+    //           accfull[2], accempty[2], done
+    static constexpr int NBAR = 2 * XST + 2 * WST + 2 * QSTAGES + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
     static_assert(OFF_Q % 1024 == 0 && Q_SLOT_BYTES % 16 == 0, "alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(FUSED || XST == WST, "the cached mode stages X and W together");
 };
 
 struct Shared {
-    uint64_t *full, *empty, *qfull, *qempty, *accfull, *accempty, *done;
+    uint64_t *fullx, *emptyx, *fullw, *emptyw, *qfull, *qempty, *accfull, *accempty, *done;
     uint32_t *tmem_base;
     volatile uint32_t *abort_flag;
 };
@@ -106,6 +123,29 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
                 return false;
             }
         }
+    }
+}
+
+// The same for waits that are not on the critical path (the epilogue waiting
+// for a whole tile's mainloop, the producer running ahead of the MMA): back
+// off with nanosleep between polls so the waiting warp does not take issue
+// slots from the decode warps sharing its SM sub-partition.
+__device__ __forceinline__ bool wait_phase_sleepy(uint64_t *bar, uint32_t parity, uint32_t max_sleep_ns,
+                                                  uint64_t limit_ns, volatile uint32_t *abort_flag, uint32_t *err,
+                                                  uint32_t errbit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t sleep_ns = 32;
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1u;
+            atomicOr(err, errbit);
+            return false;
+        }
+        if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
     }
 }
 
@@ -353,20 +393,20 @@ template <int WO> struct Dec<kQ8_0, WO> {
 #define QP_SLICE_INLINE __forceinline__
 #endif
 template <int TYPE, int WO>
-__device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int h,
+__device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int p,
                                               uint32_t ws_addr, const ChunkAddr &ca, int lane, int &stage,
                                               uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
-    constexpr int S = Cfg<TYPE>::STAGES;
+    constexpr int S = Cfg<TYPE>::WST;
     Dec<TYPE, WO> dec;
-    dec.slice(row, hs16, h);
+    dec.slice(row, hs16, p);
 #define QP_DEQUANT_ATOM(A)                                                                                     \
     {                                                                                                          \
-        if (!wait_phase_warp(&sh.empty[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
+        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
             return false;                                                                                      \
-        dec.template atom<A>(row, hs16, h, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
+        dec.template atom<A>(row, hs16, p, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
         fence_proxy_async_smem();                                                                              \
         __syncwarp();                                                                                          \
-        if (lane == 0) mbar_arrive(&sh.full[stage]);                                                           \
+        if (lane == 0) mbar_arrive(&sh.fullw[stage]);                                                          \
         advance(stage, phase, S);                                                                              \
     }
     QP_DEQUANT_ATOM(0)
@@ -379,10 +419,10 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
 
 template <int TYPE>
 __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_addr, int r,
-                                             int h, int lane, int num_tiles, int nk, uint64_t limit_ns,
+                                             int p, int lane, int num_tiles, int nk, uint64_t limit_ns,
                                              uint32_t *err) {
     using C = Cfg<TYPE>;
-    const ChunkAddr ca(r, h);
+    const ChunkAddr ca(r, p);
     int stage = 0, qs = 0;
     uint32_t phase = 0, qphase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -394,13 +434,13 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qs
             bool ok;
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = dequant_slice<TYPE, 0>(sh, row, hs16, h, ws_addr, ca, lane, stage, phase, limit_ns, err);
+                ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err);
             }
             if (!ok) return;
             __syncwarp();
@@ -418,16 +458,18 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         float *__restrict__ Y, int out_f, int T, int nk, int m_tiles, int num_tiles,
                         uint32_t *err, uint64_t limit_ns, int inject_stall) {
     using C = Cfg<TYPE>;
-    constexpr int S = C::STAGES;
+    constexpr int XS = C::XST, WS = C::WST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     Shared sh;
-    sh.full = bars;
-    sh.empty = bars + S;
-    sh.qfull = bars + 2 * S;
-    sh.qempty = bars + 2 * S + QSTAGES;
-    sh.accfull = bars + 2 * S + 2 * QSTAGES;
+    sh.fullx = bars;
+    sh.emptyx = bars + XS;
+    sh.fullw = bars + 2 * XS;
+    sh.emptyw = bars + 2 * XS + WS;
+    sh.qfull = bars + 2 * XS + 2 * WS;
+    sh.qempty = sh.qfull + QSTAGES;
+    sh.accfull = sh.qempty + QSTAGES;
     sh.accempty = sh.accfull + 2;
     sh.done = sh.accfull + 4;
     sh.tmem_base = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -436,11 +478,15 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&sh.full[s], 1 + C::DQ_WARPS);       // TMA arrive (+ each dequant warp)
-            mbar_init(&sh.empty[s], 1);                    // MMA commit
+        for (int s = 0; s < XS; ++s) {
+            mbar_init(&sh.fullx[s], 1);                    // TMA arrive with the byte count
+            mbar_init(&sh.emptyx[s], 1);                   // MMA commit
         }
-        if constexpr (C::FUSED) {                        // quantized-slice ring (fused mode only)
+        if constexpr (C::FUSED) {                        // W16 and quantized-slice rings (fused mode only)
+            for (int s = 0; s < WS; ++s) {
+                mbar_init(&sh.fullw[s], C::DQ_WARPS);      // each dequant warp
+                mbar_init(&sh.emptyw[s], 1);               // MMA commit
+            }
             for (int s = 0; s < QSTAGES; ++s) {
                 mbar_init(&sh.qfull[s], 1);
                 mbar_init(&sh.qempty[s], C::DQ_WARPS);
@@ -478,8 +524,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                 const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if constexpr (C::FUSED) {
-                        if (!wait_phase(&sh.qempty[qs], qphase ^ 1u, limit_ns, sh.abort_flag, err,
-                                        kErrTimeoutProducer))
+                        if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
+                                               kErrTimeoutProducer))
                             goto producer_done;
                         const int start = kb * QFmt<TYPE>::SB_BYTES;
                         mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
@@ -488,19 +534,19 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                     }
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
-                        if (!wait_phase(&sh.empty[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,
-                                        kErrTimeoutProducer))
+                        if (!wait_phase_sleepy(&sh.emptyx[stage], phase ^ 1u, 256, limit_ns, sh.abort_flag, err,
+                                               kErrTimeoutProducer))
                             goto producer_done;
                         const int k0 = kb * SB + a * BK;
-                        mbar_arrive_expect_tx(&sh.full[stage],
+                        mbar_arrive_expect_tx(&sh.fullx[stage],
                                               C::FUSED ? X_STAGE_BYTES : X_STAGE_BYTES + W_STAGE_BYTES);
                         if (loads != inject_stall) {
-                            tma_load_2d(xs + stage * X_STAGE_BYTES, &tmX, &sh.full[stage], k0, n0);
+                            tma_load_2d(xs + stage * X_STAGE_BYTES, &tmX, &sh.fullx[stage], k0, n0);
                             if constexpr (!C::FUSED)
-                                tma_load_2d(ws + stage * W_STAGE_BYTES, &tmW, &sh.full[stage], k0, m0);
+                                tma_load_2d(ws + stage * W_STAGE_BYTES, &tmW, &sh.fullx[stage], k0, m0);
                         }
                         ++loads;
-                        advance(stage, phase, S);
+                        advance(stage, phase, XS);
                     }
                 }
             }
@@ -510,8 +556,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA --
         if (lane == 0) {
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, wstage = 0, acc = 0;
+            uint32_t phase = 0, wphase = 0, acc_phase = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                     goto mma_done;
@@ -520,16 +566,25 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                 for (int kb = 0; kb < nk; ++kb) {
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
-                        if (!wait_phase(&sh.full[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                        if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                             goto mma_done;
+                        if constexpr (C::FUSED) {
+                            if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                                goto mma_done;
+                        }
                         tc_fence_after();
-                        const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + stage * W_STAGE_BYTES));
+                        const int wt = C::FUSED ? wstage : stage;
+                        const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wt * W_STAGE_BYTES));
                         const uint64_t bdesc = desc_sw128_kmajor(smem_u32(xs + stage * X_STAGE_BYTES));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)  // advance 16 fp16 = 32 B inside the swizzle row
                             mma_f16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | a | k) != 0);
-                        mma_commit(&sh.empty[stage]);      // frees the stage when these MMAs finish
-                        advance(stage, phase, S);
+                        mma_commit(&sh.emptyx[stage]);     // frees the stages when these MMAs finish
+                        advance(stage, phase, XS);
+                        if constexpr (C::FUSED) {
+                            mma_commit(&sh.emptyw[wstage]);
+                            advance(wstage, wphase, WS);
+                        }
                     }
                 }
                 mma_commit(&sh.accfull[acc]);              // accumulator ready for the epilogue
@@ -548,7 +603,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-            if (!wait_phase_warp(&sh.accfull[acc], acc_phase, limit_ns, sh.abort_flag, err, kErrTimeoutEpilogue))
+            if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 2048, limit_ns,
+                                                           sh.abort_flag, err, kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const int o = m0 + quarter * 32 + lane;
@@ -573,9 +629,12 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         }
     } else if constexpr (C::FUSED) {
         // ------------------------------------------------------- dequant --
-        const int dw = warp - 6;
-        const int r = (dw & 3) * 32 + lane;                // weight row within the tile
-        dequant_role<TYPE>(sh, qslots, smem_u32(ws), r, dw >> 2, lane, num_tiles, nk, limit_ns, err);
+        // unit u = 0..7 <- warps 6, 7, 8, 10, 11, 12, 14, 15 (none on sub-partition 1)
+        const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
+        if (warp != 9 && warp != 13) {
+            const int r = (u & 3) * 32 + lane;             // weight row within the tile
+            dequant_role<TYPE>(sh, qslots, smem_u32(ws), r, u >> 2, lane, num_tiles, nk, limit_ns, err);
+        }
     }
 
     __syncthreads();
