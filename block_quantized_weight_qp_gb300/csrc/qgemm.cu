@@ -319,25 +319,31 @@ template <int WO> struct Dec<kQ2_K, WO> {
 // Q6_K: value 128n + 32j + l has low four bits = a nibble (low for j < 2,
 // high for j >= 2) of ql[64n + l + 32(j&1)] and high two bits = bits
 // 2j..2j+1 of qh[32n + l]; sub-block s = v/16 has an int8 scale.
-// y = d*s*(q - 32), an exact product.
+// y = d*s*(q - 32), an exact product.  Half h of K step A has j = 2(A%2) + h,
+// so over a slice the thread reads ql[64n + 32h ..+31] and qh[32n ..+31] for
+// n = 0, 1: 32 words, realigned once per slice and kept in registers.
 template <int WO> struct Dec<kQ6_K, WO> {
     float d;
-    uint32_t sc[4];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int) {
+    uint32_t sc[4], ql[16], qh[16];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int h) {
         uint32_t dd[1];
         row_words<208 + 4 * WO, 1, true>(row, hs16, dd);
         d = h2f(dd[0]);
         row_words<192 + 4 * WO, 4, true>(row, hs16, sc);
+        uint32_t t[8];
+        row_words<4 * WO, 8, true>(row + 32 * h, hs16, t);          // ql[32h ..]
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ql[k] = t[k];
+        row_words<64 + 4 * WO, 8, true>(row + 32 * h, hs16, t);     // ql[64 + 32h ..]
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ql[8 + k] = t[k];
+        row_words<128 + 4 * WO, 16, true>(row, hs16, qh);           // qh[0 .. 63]
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t hs16, int h, uint32_t tile,
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
         constexpr int n = A / 2;
         constexpr int nsh = (A % 2) ? 4 : 0;             // j >= 2: high nibble
-        const int sh = 2 * (2 * (A % 2) + h);            // 2j
-        uint32_t ql[8], qh[8];
-        row_words<64 * n + 4 * WO, 8, true>(row + 32 * h, hs16, ql);   // ql[64n + 32h ..]
-        row_words<128 + 32 * n + 4 * WO, 8, true>(row, hs16, qh);
         const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);     // -(2^23 + 32)
         const uint32_t sw = sc[A] >> (16 * h);
 #pragma unroll
@@ -350,8 +356,12 @@ template <int WO> struct Dec<kQ6_K, WO> {
                 const int c = 2 * half + cc;
                 uint32_t u[2];
 #pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    u[k] = ((ql[2 * c + k] >> nsh) & 0x0F0F0F0Fu) | (((qh[2 * c + k] >> sh) << 4) & 0x30303030u);
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t qhw = qh[8 * n + 2 * c + k];
+                    // bits 2j..2j+1 of each qh byte moved to bits 4..5: j = 2(A%2) + h
+                    const uint32_t hb = ((A % 2) ? (qhw >> (2 * h)) : (qhw << (4 - 2 * h))) & 0x30303030u;
+                    u[k] = ((ql[8 * n + 2 * c + k] >> nsh) & 0x0F0F0F0Fu) | hb;
+                }
                 const uint2 lo = word_scaled(u[0], dl2, nbias2);
                 const uint2 hi = word_scaled(u[1], dl2, nbias2);
                 sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
@@ -534,8 +544,12 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                     }
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
-                        if (!wait_phase_sleepy(&sh.emptyx[stage], phase ^ 1u, 256, limit_ns, sh.abort_flag, err,
-                                               kErrTimeoutProducer))
+                        // fused: the decode warps share this sub-partition, so poll gently;
+                        // cached: the producer feeds the MMA directly, so poll hot
+                        if (!(C::FUSED ? wait_phase_sleepy(&sh.emptyx[stage], phase ^ 1u, 256, limit_ns,
+                                                           sh.abort_flag, err, kErrTimeoutProducer)
+                                       : wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,
+                                                    kErrTimeoutProducer)))
                             goto producer_done;
                         const int k0 = kb * SB + a * BK;
                         mbar_arrive_expect_tx(&sh.fullx[stage],
@@ -603,7 +617,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-            if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 2048, limit_ns,
+            if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
                                                            sh.abort_flag, err, kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
