@@ -276,10 +276,23 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
             e1.record(stream)
             e1.synchronize()
             ms = e0.elapsed_time(e1) / launches
+            # reference: a device-to-device copy moving the same bytes (half read,
+            # half written) over the same rotating buffers
+            srcs = [y.view(torch.uint8).view(-1)[: nbytes // 2] for y in ys]
+            dsts = [torch.empty(nbytes // 2, dtype=torch.uint8, device=device) for _ in range(nsets)]
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for i in range(nsets):
+                dsts[i][: nbytes // 2].copy_(srcs[(i + 1) % nsets])
+            c0.record(stream)
+            for i in range(launches):
+                dsts[i % nsets][: nbytes // 2].copy_(srcs[(i + 1) % nsets])
+            c1.record(stream)
+            c1.synchronize()
+            copy_gbs = round(nbytes / (c0.elapsed_time(c1) / launches / 1e3) / 1e9, 1)
             out["%s_%dx%d_%s" % (name, rows, cols, "f16" if f16 else "f32")] = {
                 "gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2), "bytes": nbytes,
-                "buffer_sets": nsets}
-            del ws, ys
+                "buffer_sets": nsets, "same_bytes_copy_gbs": copy_gbs}
+            del ws, ys, srcs, dsts
     qp.qp_check(stream)
     return out
 

@@ -2,16 +2,16 @@
 // dequantize-to-f32 step of "Qwen3.5 batched prefill has no f32 dequant for
 // IQ2_XXS, IQ3_S, IQ3_XXS, Q2_K", §Cause; the f16 copy built from it).
 //
-// HBM-bound.  One warp decodes one 256-value group (one K-quant superblock, or
-// eight Q8_0 blocks) per step of a grid-stride loop, two groups per loop
-// iteration so that both groups' loads are in flight together; lane l owns
-// values 8l..8l+7 of the group, so a warp writes 1 KiB (f32) or 512 B (f16)
-// of one output row with two / one 16-byte stores per lane.  Block fields are
-// read straight from global memory with loads no wider than the block's
-// alignment (Q4_K blocks are 16-byte aligned, Q2_K 4-byte, Q6_K and Q8_0
-// 2-byte; 2-byte aligned runs are assembled from aligned words).  The
-// (row, block) position of a warp's group is divided out once and then
-// stepped.
+// HBM-bound.  Each lane decodes one run of 32 consecutive values per step of
+// a grid-stride loop: a whole 32-value sub-block of Q4_K, two 16-value
+// sub-blocks of Q2_K / Q6_K, or one Q8_0 block, so the per-run work (scale
+// unpacking, addresses, loop control) is paid once per 32 values.  A warp
+// covers four K-quant superblocks (or 32 Q8_0 blocks) per step and writes each
+// lane's run with 16-byte stores.  Block fields are read straight from
+// global memory with loads no wider than the block's alignment (Q4_K blocks
+// are 16-byte aligned, Q2_K 4-byte, Q6_K and Q8_0 2-byte; 2-byte aligned runs
+// are assembled from aligned words).  The (row, block) position of a lane's
+// run is divided out once and then stepped.
 //
 // Arithmetic (qp_decode.cuh): every field is widened exactly and each value
 // is one fma / mul with an exact product, i.e. one f32 rounding — the same
@@ -38,124 +38,145 @@ __device__ __forceinline__ uint32_t ldg32(const uint8_t *p) {
     return __ldg(reinterpret_cast<const unsigned int *>(p));
 }
 
-// 8 bytes starting at a 2-byte aligned address, as two little-endian words;
-// every load stays inside those 8 bytes or the 2 bytes just before them.
-__device__ __forceinline__ void ld8_a2(const uint8_t *p, uint32_t &lo, uint32_t &hi) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    if ((a & 2u) == 0) {
-        lo = ldg32(p);
-        hi = ldg32(p + 4);
-    } else {
-        const uint32_t w0 = ldg32(p - 2), w1 = ldg32(p + 2), t = ldg16(p + 6);
-        lo = __funnelshift_r(w0, w1, 16);
-        hi = __funnelshift_r(w1, t, 16);
-    }
-}
-
-// ---------------------------------------------------------- per-type lanes --
-// Values 8l..8l+7 of the group whose first (or only) block starts at b, as
-// four f32 pairs.
-
-// Q4_K: sub-block s = l/4; the lane's 8 quants are the low (l%8 < 4) or high
-// nibbles of qs[32(l/8) + 8(l%4) ..]; 6-bit scale/min of s unpacked from the
-// 12 scale bytes (s < 4: low 6 bits of bytes s and s+4; s >= 4: nibbles of
-// byte s+4 plus the top two bits of bytes s-4 and s).
-__device__ __forceinline__ void lane_q4_k(const uint8_t *b, int lane, pair_t (&y)[4]) {
-    const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(b));   // d, dmin, scales[0..11]
-    const uint2 q = __ldg(reinterpret_cast<const uint2 *>(b + 16 + 32 * (lane >> 3) + 8 * (lane & 3)));
-    const int s = lane >> 2;
-    const int sh = 8 * (s & 3);
-    const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
-    const uint32_t sc = s < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
-    const uint32_t m = s < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
-    const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
-    const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
-    const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-    const int nsh = (lane & 4) ? 4 : 0;
-    affine4((q.x >> nsh) & 0x0F0F0F0Fu, dl2, nml2, y[0], y[1]);
-    affine4((q.y >> nsh) & 0x0F0F0F0Fu, dl2, nml2, y[2], y[3]);
-}
-
-// Q2_K: value 128n + 32j + l' takes bits 2j..2j+1 of qs[32n + l']; lane l has
-// n = l/16, j = (l/4)%4, l' = 8(l%4).., sub-block s = l/2 with scale byte
-// scales[s] (sc low nibble, m high nibble).
-__device__ __forceinline__ void lane_q2_k(const uint8_t *b, int lane, pair_t (&y)[4]) {
-    const int n = lane >> 4, j = (lane >> 2) & 3, s = lane >> 1;
-    const uint32_t q0 = ldg32(b + 16 + 32 * n + 8 * (lane & 3));
-    const uint32_t q1 = ldg32(b + 20 + 32 * n + 8 * (lane & 3));
-    const uint32_t scb = (ldg32(b + 4 * (s >> 2)) >> (8 * (s & 3))) & 0xffu;
-    const uint32_t dd = ldg32(b + 80);                                // d | dmin << 16
-    const float dl = __fmul_rn(h2f(dd), u2f_exact(scb & 15u));
-    const float nml = -__fmul_rn(h2f(dd >> 16), u2f_exact(scb >> 4));
-    const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-    affine4((q0 >> (2 * j)) & 0x03030303u, dl2, nml2, y[0], y[1]);
-    affine4((q1 >> (2 * j)) & 0x03030303u, dl2, nml2, y[2], y[3]);
-}
-
-// Q6_K: value 128n + 32j + l' has low four bits = a nibble (low for j < 2,
-// high for j >= 2) of ql[64n + l' + 32(j&1)] and high two bits = bits
-// 2j..2j+1 of qh[32n + l']; sub-block s = l/2 has an int8 scale.
-__device__ __forceinline__ void lane_q6_k(const uint8_t *b, int lane, pair_t (&y)[4]) {
-    const int n = lane >> 4, j = (lane >> 2) & 3, l0 = 8 * (lane & 3), s = lane >> 1;
-    uint32_t l_lo, l_hi, h_lo, h_hi;
-    ld8_a2(b + 64 * n + l0 + 32 * (j & 1), l_lo, l_hi);
-    ld8_a2(b + 128 + 32 * n + l0, h_lo, h_hi);
-    const uint32_t sb = __ldg(b + 192 + s);                              // int8 scale, as a byte
-    const float sf = __fsub_rn(u2f_exact(sb ^ 0x80u), 128.0f);           // exact int8 value
-    const float dl = __fmul_rn(h2f(ldg16(b + 208)), sf);
-    const pair_t dl2 = pk2(dl, dl), nbias2 = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
-    const int nsh = j >= 2 ? 4 : 0;
-    const uint32_t u0 = ((l_lo >> nsh) & 0x0F0F0F0Fu) | (((h_lo >> (2 * j)) << 4) & 0x30303030u);
-    const uint32_t u1 = ((l_hi >> nsh) & 0x0F0F0F0Fu) | (((h_hi >> (2 * j)) << 4) & 0x30303030u);
-    scaled4(u0, dl2, nbias2, y[0], y[1]);
-    scaled4(u1, dl2, nbias2, y[2], y[3]);
-}
-
-// Q8_0: lane l takes values 8(l%4)..+7 of the block at b; q + 128 = byte ^ 0x80.
-__device__ __forceinline__ void lane_q8_0(const uint8_t *b, int lane, pair_t (&y)[4]) {
-    uint32_t q0, q1;
-    ld8_a2(b + 2 + 8 * (lane & 3), q0, q1);
-    const float d = h2f(ldg16(b));
-    const pair_t d2 = pk2(d, d), nbias2 = pk2(-8388736.0f, -8388736.0f);     // -(2^23 + 128)
-    scaled4(q0 ^ 0x80808080u, d2, nbias2, y[0], y[1]);
-    scaled4(q1 ^ 0x80808080u, d2, nbias2, y[2], y[3]);
-}
-
-// ------------------------------------------------------------------ store --
-
-__device__ __forceinline__ void store8(float *out, int64_t cols, int64_t row, int64_t col0, const pair_t (&y)[4]) {
-    float v[8];
+// Raw bytes of one lane's run, loaded one loop step ahead of their decode.
+// Two-byte aligned runs (Q6_K, Q8_0) are fetched as aligned words starting
+// up to 2 bytes early (never before the block array, which is 16-byte
+// aligned) and realigned when decoded; every load stays inside
+// [run start - 2, run end).
+struct Span32 {
+    uint32_t a[9];
+    uint32_t sh;                                          // 0 or 16: realignment shift
+    __device__ __forceinline__ void load(const uint8_t *p) {
+        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p) & 2u);
+        const uint8_t *q = p - mis;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) unpk2(y[i], v[2 * i], v[2 * i + 1]);
-    float *p = out + row * cols + col0;
-    if (col0 + 8 <= cols && (cols & 3) == 0) {
-        __stcs(reinterpret_cast<float4 *>(p), make_float4(v[0], v[1], v[2], v[3]));
-        __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (col0 + i < cols) p[i] = v[i];
+        for (int k = 0; k < 8; ++k) a[k] = ldg32(q + 4 * k);
+        a[8] = mis ? ldg16(p + 30) : 0u;
+        sh = mis ? 16u : 0u;
     }
-}
+    __device__ __forceinline__ uint32_t word(int k) const { return __funnelshift_r(a[k], a[k + 1], sh); }
+};
 
-__device__ __forceinline__ void store8(uint16_t *out, int64_t cols, int64_t row, int64_t col0,
-                                       const pair_t (&y)[4]) {
-    uint16_t *p = out + row * cols + col0;
-    const uint32_t h0 = f2h2(y[0]), h1 = f2h2(y[1]), h2 = f2h2(y[2]), h3 = f2h2(y[3]);
-    if (col0 + 8 <= cols && (cols & 7) == 0) {
-        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(h0, h1, h2, h3));
-    } else {
-        const uint32_t h[4] = {h0, h1, h2, h3};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (col0 + i < cols) p[i] = static_cast<uint16_t>(h[i >> 1] >> (16 * (i & 1)));
+// ---------------------------------------------------------- per-type runs --
+// Run t (0..7) of the superblock at b: values 32t..32t+31, decoded to 16 f32
+// pairs.
+
+// Q4_K: run t is sub-block t: the low (t even) or high nibbles of
+// qs[32(t/2) .. +31]; its 6-bit scale/min are unpacked from the 12 scale
+// bytes (t < 4: low 6 bits of bytes t and t+4; t >= 4: nibbles of byte t+4
+// plus the top two bits of bytes t-4 and t).
+struct RawQ4K {
+    uint4 hd, q0, q1;
+    __device__ __forceinline__ void load(const uint8_t *b, int t) {
+        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
+        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 16 + 32 * (t >> 1)));
+        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 32 + 32 * (t >> 1)));
     }
-}
+    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
+        const int sh = 8 * (t & 3);
+        const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
+        const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
+        const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
+        const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
+        const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
+        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
+        const int nsh = 4 * (t & 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) affine4((w[k] >> nsh) & 0x0F0F0F0Fu, dl2, nml2, y[2 * k], y[2 * k + 1]);
+    }
+};
+
+// Q2_K: value 128n + 32j + l takes bits 2j..2j+1 of qs[32n + l]; run t has
+// n = t/4, j = t%4, sub-blocks 2t (l < 16) and 2t+1, scale bytes scales[2t],
+// scales[2t+1] (sc low nibble, m high nibble).
+struct RawQ2K {
+    uint32_t w[8], sb, dd;
+    __device__ __forceinline__ void load(const uint8_t *b, int t) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = ldg32(b + 16 + 32 * (t >> 2) + 4 * k);
+        sb = ldg32(b + 4 * (t >> 1));
+        dd = ldg32(b + 80);                                // d | dmin << 16
+    }
+    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
+        const uint32_t sbt = sb >> (16 * (t & 1));         // scales[2t] | scales[2t+1] << 8
+        const float d = h2f(dd), dmin = h2f(dd >> 16);
+        const int sh = 2 * (t & 3);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t s = (sbt >> (8 * half)) & 0xffu;
+            const float dl = __fmul_rn(d, u2f_exact(s & 15u));
+            const float nml = -__fmul_rn(dmin, u2f_exact(s >> 4));
+            const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = 4 * half + k;
+                affine4((w[i] >> sh) & 0x03030303u, dl2, nml2, y[2 * i], y[2 * i + 1]);
+            }
+        }
+    }
+};
+
+// Q6_K: value 128n + 32j + l has low four bits = a nibble (low for j < 2,
+// high for j >= 2) of ql[64n + l + 32(j&1)] and high two bits = bits
+// 2j..2j+1 of qh[32n + l]; run t has n = t/4, j = t%4, sub-blocks 2t and
+// 2t+1 with int8 scales.  y = d*s*(q - 32), an exact product.
+struct RawQ6K {
+    Span32 ql, qh;
+    uint32_t sb, db;
+    __device__ __forceinline__ void load(const uint8_t *b, int t) {
+        ql.load(b + 64 * (t >> 2) + 32 * (t & 1));
+        qh.load(b + 128 + 32 * (t >> 2));
+        sb = ldg16(b + 192 + 2 * t);                       // two int8 scales
+        db = ldg16(b + 208);
+    }
+    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
+        const int j = t & 3;
+        const float d = h2f(db);
+        const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
+        const int nsh = j >= 2 ? 4 : 0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t s = (sb >> (8 * half)) & 0xffu;
+            const float dl = __fmul_rn(d, __fsub_rn(u2f_exact(s ^ 0x80u), 128.0f));   // exact int8 value
+            const pair_t dl2 = pk2(dl, dl);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = 4 * half + k;
+                const uint32_t u =
+                    ((ql.word(i) >> nsh) & 0x0F0F0F0Fu) | (((qh.word(i) >> (2 * j)) << 4) & 0x30303030u);
+                scaled4(u, dl2, nbias2, y[2 * i], y[2 * i + 1]);
+            }
+        }
+    }
+};
+
+// Q8_0: one block = one run of 32 values; q + 128 = byte ^ 0x80.
+struct RawQ80 {
+    Span32 q;
+    uint32_t db;
+    __device__ __forceinline__ void load(const uint8_t *b, int) {
+        q.load(b + 2);
+        db = ldg16(b);
+    }
+    __device__ __forceinline__ void decode(int, pair_t (&y)[16]) const {
+        const float d = h2f(db);
+        const pair_t d2 = pk2(d, d), nbias2 = pk2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) scaled4(q.word(k) ^ 0x80808080u, d2, nbias2, y[2 * k], y[2 * k + 1]);
+    }
+};
+
+template <int TYPE> struct RawOf;
+template <> struct RawOf<kQ4_K> { using T = RawQ4K; };
+template <> struct RawOf<kQ2_K> { using T = RawQ2K; };
+template <> struct RawOf<kQ6_K> { using T = RawQ6K; };
+template <> struct RawOf<kQ8_0> { using T = RawQ80; };
 
 // ----------------------------------------------------------------- kernel --
 
-// Position of a lane's values: block index, its (row, block-in-row), stepped
-// by a grid stride whose (rows, blocks) split was divided out on the host.
+// Position of a lane's run: block index, its (row, block-in-row), stepped by
+// a grid stride whose (rows, blocks) split was divided out on the host.
 struct Cursor {
     int64_t blk, row, kb;
     __device__ __forceinline__ void step(int64_t dblk, int64_t drow, int64_t dkb, int64_t nb) {
@@ -169,42 +190,128 @@ struct Cursor {
     }
 };
 
-template <int TYPE>
-__device__ __forceinline__ void decode_lane(const uint8_t *p, int lane, pair_t (&y)[4]) {
-    if constexpr (TYPE == kQ4_K) lane_q4_k(p, lane, y);
-    else if constexpr (TYPE == kQ2_K) lane_q2_k(p, lane, y);
-    else if constexpr (TYPE == kQ6_K) lane_q6_k(p, lane, y);
-    else lane_q8_0(p, lane, y);
+// Blocks a warp covers per grid-stride step: four superblocks (8 runs each),
+// or 32 Q8_0 blocks (one run each) -- 1024 values either way.
+template <int TYPE> __host__ __device__ constexpr int blocks_per_warp() { return TYPE == kQ8_0 ? 32 : 4; }
+
+constexpr int WARPS = 8;                                       // per 256-thread block
+
+// Per-warp staging area: 32 runs, each run's bytes padded by 16 so that 16-byte
+// accesses of eight consecutive runs fall in eight different bank groups.
+template <typename OutT> struct Stage {
+    static constexpr int RUN = 32 * static_cast<int>(sizeof(OutT));   // bytes per run
+    static constexpr int PITCH = RUN + 16;
+    static constexpr int CHUNKS = 32 * RUN / 16;                      // 16-byte chunks per warp step
+    static constexpr int PER_RUN = RUN / 16;
+};
+
+template <typename OutT>
+__device__ __forceinline__ void put_run(uint8_t *stage, int lane, const pair_t (&y)[16]);
+
+template <>
+__device__ __forceinline__ void put_run<float>(uint8_t *stage, int lane, const pair_t (&y)[16]) {
+    uint8_t *p = stage + lane * Stage<float>::PITCH;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        float a, b, c, d;
+        unpk2(y[2 * k], a, b);
+        unpk2(y[2 * k + 1], c, d);
+        *reinterpret_cast<float4 *>(p + 16 * k) = make_float4(a, b, c, d);
+    }
+}
+
+template <>
+__device__ __forceinline__ void put_run<uint16_t>(uint8_t *stage, int lane, const pair_t (&y)[16]) {
+    uint8_t *p = stage + lane * Stage<uint16_t>::PITCH;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4 *>(p + 16 * k) =
+            make_uint4(f2h2(y[4 * k]), f2h2(y[4 * k + 1]), f2h2(y[4 * k + 2]), f2h2(y[4 * k + 3]));
 }
 
 template <int TYPE, typename OutT>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
                                                       int64_t nblocks, int64_t drow, int64_t dkb,
                                                       OutT *__restrict__ out) {
+    using S = Stage<OutT>;
+    using Raw = typename RawOf<TYPE>::T;
     constexpr int QK = TYPE == kQ8_0 ? 32 : 256;
     constexpr int BB = TYPE == kQ8_0 ? 34 : (TYPE == kQ4_K ? 144 : (TYPE == kQ2_K ? 84 : 210));
-    constexpr int BPG = TYPE == kQ8_0 ? 8 : 1;                // blocks per group
+    constexpr int BPW = blocks_per_warp<TYPE>();
+    constexpr int RUNS_PER_BLOCK = 32 / BPW;                  // 8 (K-quants) or 1 (Q8_0)
+    __shared__ __align__(16) uint8_t stage_all[WARPS * 32 * S::PITCH];
     const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t dblk = warps * BPG;                         // blocks per grid stride
-    // the lane's block: the group's block, or (Q8_0) block l/4 of the group
-    Cursor a;
-    a.blk = g0 * BPG + (TYPE == kQ8_0 ? (lane >> 2) : 0);
-    a.row = a.blk / nb;
-    a.kb = a.blk - a.row * nb;
-    const int v0 = TYPE == kQ8_0 ? 8 * (lane & 3) : 8 * lane;
-    while (__any_sync(0xffffffffu, a.blk < nblocks)) {
-        Cursor b = a;
-        b.step(dblk, drow, dkb, nb);
-        const bool a_ok = a.blk < nblocks, b_ok = b.blk < nblocks;
-        pair_t ya[4], yb[4];
-        if (a_ok) decode_lane<TYPE>(blocks + a.blk * BB, lane, ya);
-        if (b_ok) decode_lane<TYPE>(blocks + b.blk * BB, lane, yb);
-        if (a_ok && a.kb * QK + v0 < cols) store8(out, cols, a.row, a.kb * QK + v0, ya);
-        if (b_ok && b.kb * QK + v0 < cols) store8(out, cols, b.row, b.kb * QK + v0, yb);
-        a = b;
-        a.step(dblk, drow, dkb, nb);
+    uint8_t *stage = stage_all + (threadIdx.x >> 5) * 32 * S::PITCH;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * WARPS;
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+    const int t = TYPE == kQ8_0 ? 0 : (lane & 7);             // run within the superblock
+    Cursor c;
+    c.blk = w0 * BPW + lane / RUNS_PER_BLOCK;
+    c.row = c.blk / nb;
+    c.kb = c.blk - c.row * nb;
+    const int64_t dblk = warps * BPW;
+    const bool vec_ok = (cols & (16 / sizeof(OutT) - 1)) == 0;  // output rows keep 16-byte alignment
+    Raw raw;
+    if (c.blk < nblocks) raw.load(blocks + c.blk * BB, t);
+    while (__any_sync(0xffffffffu, c.blk < nblocks)) {
+        Cursor n = c;
+        n.step(dblk, drow, dkb, nb);
+        Raw next;
+        if (n.blk < nblocks) next.load(blocks + n.blk * BB, t);   // in flight while this step decodes
+        const bool valid = c.blk < nblocks;
+        pair_t y[16];
+        if (valid) raw.decode(t, y);
+        const int64_t col0 = c.kb * QK + 32 * t;
+        // Coalesced path: every run of the warp is whole and inside its row, and
+        // the runs of each 512-byte output piece are contiguous in memory.
+        bool whole = valid && vec_ok && col0 + 32 <= cols;
+        if constexpr (TYPE == kQ8_0) {
+            // every lane takes part in the shuffle (it must not sit behind a
+            // short-circuit): all 32 blocks in one row, consecutive
+            const int64_t kb_first = __shfl_sync(0xffffffffu, c.kb, 0);
+            whole = whole && (c.kb - lane == kb_first);
+        }
+        if (__all_sync(0xffffffffu, whole)) {
+            put_run<OutT>(stage, lane, y);
+            __syncwarp();
+            // piece k of the warp step: 32 chunks = 512 bytes, all from one block
+            // run group (K-quants: superblock (k*32)/(8*PER_RUN); Q8_0: one row)
+#pragma unroll
+            for (int k = 0; k < S::CHUNKS / 32; ++k) {
+                const int chunk = 32 * k + lane;
+                const int run = chunk / S::PER_RUN;
+                const int within = chunk % S::PER_RUN;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + run * S::PITCH + 16 * within);
+                const int src = TYPE == kQ8_0 ? 0 : (run & ~7);    // a lane holding that run's block cursor
+                const int64_t row = __shfl_sync(0xffffffffu, c.row, src);
+                const int64_t kb0 = __shfl_sync(0xffffffffu, c.kb, src);
+                const int64_t col = kb0 * QK + (TYPE == kQ8_0 ? 32 * run : 32 * (run & 7));
+                __stcs(reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out + row * cols + col) + 16 * within),
+                       v);
+            }
+            __syncwarp();
+        } else if (valid && col0 < cols) {
+            // Guarded per-lane path (partial blocks, unaligned rows, row ends).
+            OutT *p = out + c.row * cols + col0;
+            if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float a, b;
+                    unpk2(y[k], a, b);
+                    if (col0 + 2 * k < cols) p[2 * k] = a;
+                    if (col0 + 2 * k + 1 < cols) p[2 * k + 1] = b;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t h = f2h2(y[k]);
+                    if (col0 + 2 * k < cols) p[2 * k] = static_cast<uint16_t>(h);
+                    if (col0 + 2 * k + 1 < cols) p[2 * k + 1] = static_cast<uint16_t>(h >> 16);
+                }
+            }
+        }
+        raw = next;
+        c = n;
     }
 }
 
@@ -213,8 +320,8 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
     const int64_t qk = TYPE == kQ8_0 ? 32 : 256;
     const int64_t nb = (cols + qk - 1) / qk;
     const int64_t nblocks = rows * nb;
-    const int64_t ngroups = TYPE == kQ8_0 ? (nblocks + 7) / 8 : nblocks;
-    // one resident wave of 256-thread blocks, at least two groups per warp
+    const int64_t nwarps = (nblocks + blocks_per_warp<TYPE>() - 1) / blocks_per_warp<TYPE>();
+    // one resident wave of 256-thread blocks at most
     static int per_sm = 0;
     if (per_sm == 0) {
         int n = 0;
@@ -223,10 +330,10 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
             n = 1;
         per_sm = n;
     }
-    const int64_t want = (ngroups + 15) / 16;
+    const int64_t want = (nwarps + WARPS - 1) / WARPS;
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    const int64_t dblk = static_cast<int64_t>(grid) * 8 * (TYPE == kQ8_0 ? 8 : 1);
+    const int64_t dblk = static_cast<int64_t>(grid) * WARPS * blocks_per_warp<TYPE>();
     dequant_kernel<TYPE, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), cols, nb, nblocks,
                                                          dblk / nb, dblk % nb, out);
     return cudaGetLastError();
