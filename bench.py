@@ -429,7 +429,8 @@ def main_qp(args):
     # Host->device copies of X run on one copy stream and the device->host read
     # of each projection's Y on another as soon as that projection is done,
     # so both directions overlap the GEMMs; steps do not overlap each other.
-    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    h2d_s = torch.cuda.Stream(device)
+    d2h_streams = [torch.cuda.Stream(device) for _ in range(max(1, args.d2h_streams))]
 
     def e2e_step():
         start = torch.cuda.Event()
@@ -448,10 +449,15 @@ def main_qp(args):
             qp.qp_prefill_gemm(qt, layer.W[i], out_f, in_f, Xd[src], T, layer.Y[i], stream)
             done = torch.cuda.Event()
             done.record(stream)
-            d2h_s.wait_event(done)
-            with torch.cuda.stream(d2h_s):
-                Yh[i].copy_(layer.Y[i], non_blocking=True)
-        stream.wait_stream(d2h_s)
+            # the read-back of Y is split row-wise over the copy streams
+            parts = len(d2h_streams)
+            rows = -(-T // parts)
+            for j, ds in enumerate(d2h_streams):
+                ds.wait_event(done)
+                with torch.cuda.stream(ds):
+                    Yh[i][j * rows:(j + 1) * rows].copy_(layer.Y[i][j * rows:(j + 1) * rows], non_blocking=True)
+        for ds in d2h_streams:
+            stream.wait_stream(ds)
 
     e2e = None
     if not args.no_e2e and args.mode == "fused":
@@ -469,6 +475,7 @@ def main_qp(args):
         qp.qp_check(stream)
         e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
         e2e = {"value": round(job_throughput(flops, world, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
+               "d2h_streams": len(d2h_streams),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                "tok_per_s": round(job_throughput(T, world, e2e_ms), 1)}
     del Xh, Yh, Xd
@@ -581,6 +588,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--only-proj", default=None, help="time only this projection (profiling runs)")
+    p.add_argument("--d2h-streams", type=int, default=1, help="copy streams for the e2e read-back of Y")
     p.add_argument("--mode", choices=["fused", "cached"], default="fused",
                    help="cached: the same step over f16 weights made once by qp_dequant_f16")
     p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")
