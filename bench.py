@@ -41,10 +41,12 @@ METRIC = "fused dequant-GEMM prefill TFLOP/s & tok/s (% dense-FP16 peak); dequan
 DEFAULT_WORKLOAD = "qwen3_8b_q2k_q6k_t8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of the dominant kernel per launch, from one ncu capture of the
-# kernel source whose hash is recorded; reported only while the source is
-# unchanged.  (bytes per launch of the Q2_K 4096x4096 projection at T=8192)
-NCU_TRAFFIC = {"source_sha": None, "bytes_per_launch": None, "what": None}
+# DRAM traffic of the dominant kernel per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum), from one ncu capture of the kernel source whose hash
+# is recorded; reported only while the source is unchanged.
+NCU_TRAFFIC = {"source_sha": "44eaa4d9ebba9388", "bytes_per_launch": 427236608,
+               "what": "fused Q2_K gate projection 12288x4096, T=8192 (read 84.19 MB + write 343.05 MB); "
+                       "algorithmic 486.3 MB (W 16.5 + X 67.1 + Y 402.7), part of Y still in L2 at kernel end"}
 KERNEL_SOURCES = ["block_quantized_weight_qp_gb300/csrc/qgemm.cu",
                   "block_quantized_weight_qp_gb300/csrc/qp_ptx.cuh"]
 
@@ -415,6 +417,7 @@ def main_qp(args):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
+                "traffic_what": NCU_TRAFFIC["what"] if traffic else None,
                 "kernel": ("prefill_gemm_kernel<%s> (fused dequant, tcgen05)" % dom if args.mode == "fused"
                            else "prefill_gemm_kernel<f16 weight> (cached mode, tcgen05)"),
                 "peak_source": "%s dense bf16 burst (fp16 runs at the bf16 rate)" % peak_src}
