@@ -6,16 +6,11 @@
 // mode works from an f16 copy of them).
 //
 // Two modes share one persistent, warp-specialized kernel:
-//   FUSED  W is block-quantized.  The kernel runs as clusters of two CTAs
-//          (a pair) that work on the same 128 weight rows and on two adjacent
-//          256-token tiles.  Each CTA stages a superblock-wide slice of 64 of
-//          those rows (raw bytes, TMA) and its eight dequant warps decode them
-//          into fp16, written straight into the 128-byte-swizzled K-major
-//          layout the tensor cores read -- into its own W stage and, through
-//          distributed shared memory, into the peer's.  Each weight is thus
-//          decoded once for 512 tokens.
-//   F16W   W is a dense fp16 weight (the cached mode), staged by TMA; one CTA
-//          per weight tile.
+//   FUSED  W is block-quantized.  TMA stages one superblock-wide slice of 128
+//          weight rows (raw bytes) into shared memory; eight dequant warps
+//          decode it into fp16, written straight into the 128-byte-swizzled
+//          K-major layout the tensor cores read.
+//   F16W   W is a dense fp16 weight (the cached mode), staged by TMA.
 // Roles (one CTA per SM, tiles 128 weight rows x 256 tokens, K step 64):
 //   warp 0      TMA producer (X tiles; quantized slices or fp16 W tiles)
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
@@ -25,11 +20,8 @@
 //               (each warp owns the 32 TMEM lanes its warp index selects)
 //   warps 6-15  dequant (FUSED only; 9 and 13 idle, so no decode work shares
 //               the MMA thread's SM sub-partition): unit u = 0..7 decodes
-//               slice rows 32(u%2)..+31, values 16(u/2)..+15 of every
+//               weight rows 32(u%4)..+31, values 32(u/4)..+31 of every
 //               64-value K step
-// A W stage is full when the decode warps of both CTAs have arrived on it,
-// and free when both CTAs' MMAs have finished reading their copies (the MMA
-// commit is multicast to the pair).
 //
 // Exactness of the fused decode: every field is widened exactly, the int ->
 // float step is the exponent-bias trick (OR the integer into the mantissa of
@@ -79,8 +71,10 @@ template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };     
 // Pipeline depths.  X tiles (TMA) and fp16 W tiles (written by the dequant
 // warps in fused mode) have rings of their own, so X can be prefetched deeper
 // than the decode runs ahead; the cached mode stages X and W together.
-// Shared memory: XST * 32 KiB + WST * 16 KiB + 2 quantized 64-row slices, <= 227 KiB.
-template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3; };   // fused types
+// Shared memory: XST * 32 KiB + WST * 16 KiB + 2 quantized slices, <= 227 KiB.
+template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3; };   // Q4_K, Q2_K
+template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 2; };
+template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3; };
 template <> struct Depth<0> { static constexpr int XST = 4, WST = 4; };
 
 template <int TYPE> struct Cfg {
@@ -92,11 +86,7 @@ template <int TYPE> struct Cfg {
     // single MMA-issuing thread of warp 1.  Warps 6..15 minus 9 and 13.
     static constexpr int DQ_WARPS = FUSED ? 8 : 0;
     static constexpr int THREADS = FUSED ? 16 * 32 : 6 * 32;
-    // fused mode runs as a pair of CTAs (a cluster of 2) on one weight tile;
-    // each stages and decodes half of its rows
-    static constexpr int PAIR = FUSED ? 2 : 1;
-    static constexpr int Q_ROWS = BM / PAIR;
-    static constexpr int Q_SLOT_BYTES = FUSED ? Q_ROWS * QFmt<TYPE>::BOX : 0;
+    static constexpr int Q_SLOT_BYTES = FUSED ? BM * QFmt<TYPE>::BOX : 0;
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W = OFF_X + XST * X_STAGE_BYTES;
     static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
@@ -119,16 +109,12 @@ struct Shared {
 
 // Bounded wait on a barrier phase.  Returns false (and stops every role of
 // this CTA) when the limit passes or another role already gave up.
-// CLUSTER: acquire at cluster scope (the phase is completed by arrivals from
-// the peer CTA of the pair).
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                            volatile uint32_t *abort_flag, uint32_t *err, uint32_t errbit) {
-    auto poll = [&] { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (poll()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (poll()) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 63u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
@@ -164,10 +150,9 @@ __device__ __forceinline__ bool wait_phase_sleepy(uint64_t *bar, uint32_t parity
 }
 
 // Warp-uniform form for roles whose every lane reads the guarded data.
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_phase_warp(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                                 volatile uint32_t *abort_flag, uint32_t *err, uint32_t errbit) {
-    const bool ok = wait_phase<CLUSTER>(bar, parity, limit_ns, abort_flag, err, errbit);
+    const bool ok = wait_phase(bar, parity, limit_ns, abort_flag, err, errbit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -218,51 +203,31 @@ __device__ __forceinline__ void row_words(const uint8_t *row, uint32_t hs16, uin
     }
 }
 
-// The 8 decode warps of a CTA cover 64 of the tile's 128 weight rows (the
-// other 64 are decoded by the peer CTA of the cluster) and split every
-// 64-value K step of a row into PARTS parts of 16 values (two 16-byte output
-// chunks): part p writes chunks 2p and 2p+1.  All lanes of a warp share p,
-// so branches on p are uniform.  Every chunk is stored twice: into this
-// CTA's W stage and into the peer's (shared::cluster), at the same offset.
-constexpr int PARTS = 4;
-
-// Output chunk offsets of this thread's tile row and part in a W stage:
-// chunk c (k = 8c..8c+7) of row r sits at r*128 + ((c ^ (r & 7)) << 4)
-// (128-byte swizzle, as TMA would write it).
+// Output chunk addresses of this thread's row and half in a stage's W tile:
+// chunk 4h + c (k = 32h + 8c ..) sits at row*128 + (((4h + c) ^ (row & 7)) << 4)
+// (128-byte swizzle).
 struct ChunkAddr {
-    uint32_t off[2];
-    __device__ __forceinline__ ChunkAddr(int row, int p) {
+    uint32_t off[4];
+    __device__ __forceinline__ ChunkAddr(int row, int h) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) off[i] = static_cast<uint32_t>(row * 128 + (((2 * p + i) ^ (row & 7)) << 4));
-    }
-};
-
-// Where a decoded chunk goes: the local stage and the peer's copy of it.
-struct Sink {
-    uint32_t local, remote;
-    __device__ __forceinline__ void put(const ChunkAddr &ca, int i, uint32_t a, uint32_t b, uint32_t c,
-                                        uint32_t d) const {
-        sts128(local + ca.off[i], a, b, c, d);
-        st_cluster_v4(remote + ca.off[i], a, b, c, d);
+        for (int c = 0; c < 4; ++c) off[c] = static_cast<uint32_t>(row * 128 + (((4 * h + c) ^ (row & 7)) << 4));
     }
 };
 
 // Per-type decoders.  slice(): per-superblock state of this thread's row and
-// part p (row = the thread's row of the staged 64-row slice); atom<A>():
-// writes the thread's two chunks of K step A (values 64A + 16p .. +15 of the
-// superblock).  WO = (slice start % 16)/4, the slice's word offset in the
-// staged row (Q2_K, Q6_K); hs16 = 16 when the start is 2 bytes past a word
-// (Q6_K), else 0.
+// half h; atom<A>(): writes the thread's four chunks of K step A (values
+// 64A + 32h .. 64A + 32h + 31 of the superblock).  WO = (slice start % 16)/4,
+// the slice's word offset in the staged row (Q2_K, Q6_K); hs16 = 16 when the
+// start is 2 bytes past a word (Q6_K), else 0.
 template <int TYPE, int WO> struct Dec;
 
-// Q4_K: part p of K step A is sub-block 2A + p/2: the low (p < 2) or high
-// nibbles of qs[32A + 16(p%2) .. +15].
+// Q4_K: sub-block 2A+h holds values 64A+32h..; they are the low (h=0) or
+// high (h=1) nibbles of qs[32A .. 32A+31].
 template <int WO> struct Dec<kQ4_K, WO> {
     pair_t dl2[4], nml2[4];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int p) {
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int h) {
         const uint4 hd = *reinterpret_cast<const uint4 *>(row);   // d, dmin, scales[0..11]
         const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-        const int h = p >> 1;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             uint32_t sc, m;
@@ -276,170 +241,162 @@ template <int WO> struct Dec<kQ4_K, WO> {
                 sc = (lo & 15u) | (((hd.y >> sh) >> 6 & 3u) << 4);
                 m = ((lo >> 4) & 15u) | (((hd.z >> sh) >> 6 & 3u) << 4);
             }
-            const float dl = __fmul_rn(d, u2f_exact(sc));
-            const float nml = -__fmul_rn(dmin, u2f_exact(m));
+            const float dl = __fmul_rn(d, static_cast<float>(sc));
+            const float nml = -__fmul_rn(dmin, static_cast<float>(m));
             dl2[a] = pk2(dl, dl);
             nml2[a] = pk2(nml, nml);
         }
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int p, const Sink &out,
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
-        const uint4 q = *reinterpret_cast<const uint4 *>(row + 16 + 32 * A + 16 * (p & 1));
-        const int sh = 4 * (p >> 1);
-        const uint2 a0 = word_affine((q.x >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-        const uint2 a1 = word_affine((q.y >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-        const uint2 b0 = word_affine((q.z >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-        const uint2 b1 = word_affine((q.w >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-        out.put(ca, 0, a0.x, a0.y, a1.x, a1.y);
-        out.put(ca, 1, b0.x, b0.y, b1.x, b1.y);
+        uint32_t w[8];
+        row_words<16 + 32 * A, 8, false>(row, 0, w);
+        const int sh = 4 * h;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 lo = word_affine((w[2 * c] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            const uint2 hi = word_affine((w[2 * c + 1] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
+        }
     }
 };
 
 // Q2_K: value 128n + 32j + l takes bits 2j..2j+1 of qs[32n + l]; sub-block
-// s = v/16 has scale byte scales[s] (sc low nibble, m high nibble).  Part p of
-// K step A is sub-block 4A + p, with j = 2(A%2) + p/2 and l = 16(p%2)..+15.
-// A 4-bit sc/m pair gives a sub-block only four distinct values,
-// f16(dl*q - ml) for q = 0..3: they are computed exactly once per sub-block
-// and then selected per value with byte permutes (a lookup stored as a
-// low-byte plane and a high-byte plane).  The thread keeps its 32 qs bytes
-// of the slice in registers: K steps 2n and 2n+1 read the same bytes.
+// s = v/16 has scale byte scales[s] (sc low nibble, m high nibble).  A 4-bit
+// sc/m pair gives each sub-block only four distinct values, f16(dl*q - ml)
+// for q = 0..3: they are computed exactly once per sub-block and then
+// selected per value with byte permutes (a lookup stored as a low-byte plane
+// and a high-byte plane).  The thread keeps the slice's 64 qs bytes in
+// registers: K steps 2n and 2n+1 read the same bytes with different j.
 template <int WO> struct Dec<kQ2_K, WO> {
     float d, dmin;
-    uint32_t sc[4], qs[8];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int p) {
+    uint32_t sc[4], qs[16];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int) {
         uint32_t dd[1];
         row_words<80 + 4 * WO, 1, false>(row, 0, dd);
         d = h2f(dd[0]);
         dmin = h2f(dd[0] >> 16);
         row_words<4 * WO, 4, false>(row, 0, sc);
-        uint32_t q0[4], q1[4];
-        row_words<16 + 4 * WO, 4, false>(row + 16 * (p & 1), 0, q0);   // qs[16(p%2) ..]
-        row_words<48 + 4 * WO, 4, false>(row + 16 * (p & 1), 0, q1);   // qs[32 + 16(p%2) ..]
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            qs[k] = q0[k];
-            qs[4 + k] = q1[k];
-        }
+        row_words<16 + 4 * WO, 16, false>(row, 0, qs);
     }
-    template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int p, const Sink &out,
-                                         const ChunkAddr &ca) const {
-        constexpr int n = A / 2;
-        const int sh = 2 * (2 * (A % 2) + (p >> 1));     // 2j
-        const uint32_t b = (sc[A] >> (8 * p)) & 0xffu;   // scale byte of sub-block 4A + p
-        const float dl = __fmul_rn(d, u2f_exact(b & 15u));
-        const float nml = -__fmul_rn(dmin, u2f_exact(b >> 4));
+    // byte-planar lookup for the sub-block with scale byte b
+    __device__ __forceinline__ void lut(uint32_t b, uint32_t &plo, uint32_t &phi) const {
+        const float dl = __fmul_rn(d, static_cast<float>(b & 15u));
+        const float nml = -__fmul_rn(dmin, static_cast<float>(b >> 4));
         const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
         const uint32_t h01 = f2h2(ffma2(dl2, pk2(0.0f, 1.0f), nml2));
         const uint32_t h23 = f2h2(ffma2(dl2, pk2(2.0f, 3.0f), nml2));
-        const uint32_t plo = __byte_perm(h01, h23, 0x6420), phi = __byte_perm(h01, h23, 0x7531);
-        uint32_t v[8];
+        plo = __byte_perm(h01, h23, 0x6420);
+        phi = __byte_perm(h01, h23, 0x7531);
+    }
+    // 4 crumb values in the bytes of u -> 2 half2
+    __device__ __forceinline__ static uint2 pick(uint32_t u, uint32_t plo, uint32_t phi) {
+        const uint32_t sel = u * 0x11u + 0x40404040u;     // byte q -> nibbles (q, q + 4)
+        return make_uint2(__byte_perm(plo, phi, sel), __byte_perm(plo, phi, sel >> 16));
+    }
+    template <int A>
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
+                                         const ChunkAddr &ca) const {
+        constexpr int n = A / 2;
+        const int sh = 2 * (2 * (A % 2) + h);            // 2j
+        const uint32_t sw = sc[A] >> (16 * h);           // scale bytes of sub-blocks 4A+2h, 4A+2h+1
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t sel = ((qs[4 * n + k] >> sh) & 0x03030303u) * 0x11u + 0x40404040u;  // q -> (q, q+4)
-            v[2 * k] = __byte_perm(plo, phi, sel);
-            v[2 * k + 1] = __byte_perm(plo, phi, sel >> 16);
+        for (int half = 0; half < 2; ++half) {           // two sub-blocks of 16 values
+            uint32_t plo, phi;
+            lut((sw >> (8 * half)) & 0xffu, plo, phi);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
+                const uint2 lo = pick((qs[8 * n + 2 * c] >> sh) & 0x03030303u, plo, phi);
+                const uint2 hi = pick((qs[8 * n + 2 * c + 1] >> sh) & 0x03030303u, plo, phi);
+                sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
+            }
         }
-        out.put(ca, 0, v[0], v[1], v[2], v[3]);
-        out.put(ca, 1, v[4], v[5], v[6], v[7]);
     }
 };
 
 // Q6_K: value 128n + 32j + l has low four bits = a nibble (low for j < 2,
 // high for j >= 2) of ql[64n + l + 32(j&1)] and high two bits = bits
-// 2j..2j+1 of qh[32n + l]; sub-block s = v/16 has an int8 scale.  Part p of
-// K step A: j = 2(A%2) + p/2, l = 16(p%2)..+15, sub-block 4A + p.
-// y = d*s*(q - 32), an exact product.  The thread keeps its 16 ql and 16 qh
-// bytes of each half of the slice in registers.
+// 2j..2j+1 of qh[32n + l]; sub-block s = v/16 has an int8 scale.
+// y = d*s*(q - 32), an exact product.  Half h of K step A has j = 2(A%2) + h,
+// so over a slice the thread reads ql[64n + 32h ..+31] and qh[32n ..+31] for
+// n = 0, 1: 32 words, realigned once per slice and kept in registers.
 template <int WO> struct Dec<kQ6_K, WO> {
     float d;
-    uint32_t sc[4], ql[8], qh[8];
-    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int p) {
+    uint32_t sc[4], ql[16], qh[16];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int h) {
         uint32_t dd[1];
         row_words<208 + 4 * WO, 1, true>(row, hs16, dd);
         d = h2f(dd[0]);
         row_words<192 + 4 * WO, 4, true>(row, hs16, sc);
-        const uint8_t *lrow = row + 32 * (p >> 1) + 16 * (p & 1);
-        uint32_t t[4];
-        row_words<4 * WO, 4, true>(lrow, hs16, t);          // ql[32(j&1) + l], n = 0
+        uint32_t t[8];
+        row_words<4 * WO, 8, true>(row + 32 * h, hs16, t);          // ql[32h ..]
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ql[k] = t[k];
-        row_words<64 + 4 * WO, 4, true>(lrow, hs16, t);     // n = 1
+        for (int k = 0; k < 8; ++k) ql[k] = t[k];
+        row_words<64 + 4 * WO, 8, true>(row + 32 * h, hs16, t);     // ql[64 + 32h ..]
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ql[4 + k] = t[k];
-        row_words<128 + 4 * WO, 4, true>(row + 16 * (p & 1), hs16, t);   // qh[l], n = 0
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qh[k] = t[k];
-        row_words<160 + 4 * WO, 4, true>(row + 16 * (p & 1), hs16, t);   // n = 1
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qh[4 + k] = t[k];
+        for (int k = 0; k < 8; ++k) ql[8 + k] = t[k];
+        row_words<128 + 4 * WO, 16, true>(row, hs16, qh);           // qh[0 .. 63]
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int p, const Sink &out,
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
         constexpr int n = A / 2;
         constexpr int nsh = (A % 2) ? 4 : 0;             // j >= 2: high nibble
-        const int hi = p >> 1;                           // j = 2(A%2) + hi
-        const int8_t s = static_cast<int8_t>((sc[A] >> (8 * p)) & 0xffu);
-        const float dl = __fmul_rn(d, static_cast<float>(s));
-        const pair_t dl2 = pk2(dl, dl), nbias2 = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
-        uint32_t v[8];
+        const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);     // -(2^23 + 32)
+        const uint32_t sw = sc[A] >> (16 * h);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t qhw = qh[4 * n + k];
-            // bits 2j..2j+1 of each qh byte moved to bits 4..5
-            const uint32_t hb = ((A % 2) ? (qhw >> (2 * hi)) : (qhw << (4 - 2 * hi))) & 0x30303030u;
-            const uint32_t u = ((ql[4 * n + k] >> nsh) & 0x0F0F0F0Fu) | hb;
-            const uint2 w = word_scaled(u, dl2, nbias2);
-            v[2 * k] = w.x;
-            v[2 * k + 1] = w.y;
+        for (int half = 0; half < 2; ++half) {
+            const int8_t s = static_cast<int8_t>((sw >> (8 * half)) & 0xffu);
+            const float dl = __fmul_rn(d, static_cast<float>(s));
+            const pair_t dl2 = pk2(dl, dl);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
+                uint32_t u[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t qhw = qh[8 * n + 2 * c + k];
+                    // bits 2j..2j+1 of each qh byte moved to bits 4..5: j = 2(A%2) + h
+                    const uint32_t hb = ((A % 2) ? (qhw >> (2 * h)) : (qhw << (4 - 2 * h))) & 0x30303030u;
+                    u[k] = ((ql[8 * n + 2 * c + k] >> nsh) & 0x0F0F0F0Fu) | hb;
+                }
+                const uint2 lo = word_scaled(u[0], dl2, nbias2);
+                const uint2 hi = word_scaled(u[1], dl2, nbias2);
+                sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
+            }
         }
-        out.put(ca, 0, v[0], v[1], v[2], v[3]);
-        out.put(ca, 1, v[4], v[5], v[6], v[7]);
     }
 };
 
-// Q8_0: the slice holds eight 34-byte blocks; part p of K step A is values
-// 16(p%2)..+15 of block 2A + p/2 (bytes 68A + 34(p/2) ..: d, q[32]).
+// Q8_0: the slice holds eight 34-byte blocks; K step A = blocks 2A (h = 0)
+// and 2A+1 (h = 1), i.e. bytes 68A .. 68A+67 = d0, q0[32], d1, q1[32].
 // q + 128 = byte XOR 0x80.
 template <int WO> struct Dec<kQ8_0, WO> {
     __device__ __forceinline__ void slice(const uint8_t *, uint32_t, int) {}
-    template <int A, int P>
-    __device__ __forceinline__ void part(const uint8_t *row, const Sink &out, const ChunkAddr &ca) const {
-        constexpr int B0 = 68 * A + 34 * (P >> 1);       // block start
-        constexpr int Q0 = B0 + 2 + 16 * (P & 1);        // first quant byte of this part
-        uint32_t dw[1], w[5];
-        row_words<B0 & ~3, 1, false>(row, 0, dw);
-        row_words<Q0 & ~3, 5, false>(row, 0, w);
-        const float dv = h2f((B0 & 3) ? (dw[0] >> 16) : dw[0]);
-        const pair_t d2 = pk2(dv, dv), nbias2 = pk2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
-        uint32_t v[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t q = (Q0 & 3) ? __funnelshift_r(w[k], w[k + 1], 16) : w[k];
-            const uint2 y = word_scaled(q ^ 0x80808080u, d2, nbias2);
-            v[2 * k] = y.x;
-            v[2 * k + 1] = y.y;
-        }
-        out.put(ca, 0, v[0], v[1], v[2], v[3]);
-        out.put(ca, 1, v[4], v[5], v[6], v[7]);
-    }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int p, const Sink &out,
+    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
-        switch (p) {                                     // uniform across the warp
-        case 0: part<A, 0>(row, out, ca); break;
-        case 1: part<A, 1>(row, out, ca); break;
-        case 2: part<A, 2>(row, out, ca); break;
-        default: part<A, 3>(row, out, ca); break;
+        uint32_t w[17];
+        row_words<68 * A, 17, false>(row, 0, w);
+        const float dv = h2f(h ? (w[8] >> 16) : w[0]);
+        uint32_t q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = h ? w[k + 9] : __funnelshift_r(w[k], w[k + 1], 16);
+        const pair_t d2 = pk2(dv, dv);
+        const pair_t nbias2 = pk2(-8388736.0f, -8388736.0f);     // -(2^23 + 128)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 lo = word_scaled(q[2 * c] ^ 0x80808080u, d2, nbias2);
+            const uint2 hi = word_scaled(q[2 * c + 1] ^ 0x80808080u, d2, nbias2);
+            sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
         }
     }
 };
 
-// One superblock slice of one row part: four K steps, each waiting for its
-// W stage to be free in both CTAs of the pair, decoding into this CTA's and
-// the peer's copy of it, and signalling both CTAs' MMA threads.
+// One superblock slice of one half-row: four K steps, each waiting for its
+// W stage to be free, decoding into it and signalling the MMA.
 #ifdef QP_NOINLINE_SLICE
 #define QP_SLICE_INLINE __noinline__
 #else
@@ -447,26 +404,19 @@ template <int WO> struct Dec<kQ8_0, WO> {
 #endif
 template <int TYPE, int WO>
 __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int p,
-                                              uint32_t ws_local, uint32_t ws_remote, uint32_t fullw_remote,
-                                              const ChunkAddr &ca, int lane, int &stage, uint32_t &phase,
-                                              uint64_t limit_ns, uint32_t *err) {
+                                              uint32_t ws_addr, const ChunkAddr &ca, int lane, int &stage,
+                                              uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
     constexpr int S = Cfg<TYPE>::WST;
     Dec<TYPE, WO> dec;
     dec.slice(row, hs16, p);
 #define QP_DEQUANT_ATOM(A)                                                                                     \
     {                                                                                                          \
-        if (!wait_phase_warp<true>(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,              \
-                                   kErrTimeoutDequant))                                                        \
+        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
             return false;                                                                                      \
-        const uint32_t so = static_cast<uint32_t>(stage * W_STAGE_BYTES);                                      \
-        dec.template atom<A>(row, hs16, p, Sink{ws_local + so, ws_remote + so}, ca);                           \
+        dec.template atom<A>(row, hs16, p, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
         fence_proxy_async_smem();                                                                              \
-        fence_proxy_async_cluster();                                                                           \
         __syncwarp();                                                                                          \
-        if (lane == 0) {                                                                                       \
-            mbar_arrive(&sh.fullw[stage]);                                                                     \
-            mbar_arrive_cluster(fullw_remote + static_cast<uint32_t>(stage * 8));                              \
-        }                                                                                                      \
+        if (lane == 0) mbar_arrive(&sh.fullw[stage]);                                                          \
         advance(stage, phase, S);                                                                              \
     }
     QP_DEQUANT_ATOM(0)
@@ -477,38 +427,31 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
     return true;
 }
 
-// Decode role: this thread owns row `rl` of the CTA's 64-row quantized slice
-// (tile row 64 * rank + rl) and part p of every K step.
 template <int TYPE>
-__device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_local,
-                                             uint32_t peer, int rl, int tile_row, int p, int lane, int first,
-                                             int count, int stride, int nk, uint64_t limit_ns, uint32_t *err) {
+__device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_addr, int r,
+                                             int p, int lane, int num_tiles, int nk, uint64_t limit_ns,
+                                             uint32_t *err) {
     using C = Cfg<TYPE>;
-    const ChunkAddr ca(tile_row, p);
-    const uint32_t ws_remote = mapa_shared(ws_local, peer);
-    const uint32_t fullw_remote = mapa_shared(smem_u32(sh.fullw), peer);
+    const ChunkAddr ca(r, p);
     int stage = 0, qs = 0;
     uint32_t phase = 0, qphase = 0;
-    for (int tile = first; tile < count; tile += stride) {
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         for (int kb = 0; kb < nk; ++kb) {
             if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) return;
-            const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + rl * QFmt<TYPE>::BOX;
+            const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
             const int rem = (kb * QFmt<TYPE>::SB_BYTES) & 15;
             const uint32_t hs16 = (rem & 2) ? 16u : 0u;
             bool ok;
-#define QP_SLICE(WO) \
-    dequant_slice<TYPE, WO>(sh, row, hs16, p, ws_local, ws_remote, fullw_remote, ca, lane, stage, phase, limit_ns, err)
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = QP_SLICE(0); break;
-                case 1: ok = QP_SLICE(1); break;
-                case 2: ok = QP_SLICE(2); break;
-                default: ok = QP_SLICE(3); break;
+                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = QP_SLICE(0);
+                ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err);
             }
-#undef QP_SLICE
             if (!ok) return;
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.qempty[qs]);
@@ -526,14 +469,6 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         uint32_t *err, uint64_t limit_ns, int inject_stall) {
     using C = Cfg<TYPE>;
     constexpr int XS = C::XST, WS = C::WST;
-    // Work units: fused mode walks (weight tile, token-tile pair) units, one per
-    // cluster, this CTA taking token tile 2*pair + rank; the cached mode walks
-    // (weight tile, token tile) units, one per CTA.
-    const int rank = C::FUSED ? static_cast<int>(cluster_ctarank()) : 0;
-    const int first = C::FUSED ? static_cast<int>(blockIdx.x) / C::PAIR : static_cast<int>(blockIdx.x);
-    const int stride = C::FUSED ? static_cast<int>(gridDim.x) / C::PAIR : static_cast<int>(gridDim.x);
-    auto tile_m0 = [&](int unit) { return (unit % m_tiles) * BM; };
-    auto tile_n0 = [&](int unit) { return ((unit / m_tiles) * C::PAIR + rank) * BN; };
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -559,8 +494,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         }
         if constexpr (C::FUSED) {                        // W16 and quantized-slice rings (fused mode only)
             for (int s = 0; s < WS; ++s) {
-                mbar_init(&sh.fullw[s], 2 * C::DQ_WARPS);  // each dequant warp of both CTAs
-                mbar_init(&sh.emptyw[s], 2);               // MMA commits of both CTAs
+                mbar_init(&sh.fullw[s], C::DQ_WARPS);      // each dequant warp
+                mbar_init(&sh.emptyw[s], 1);               // MMA commit
             }
             for (int s = 0; s < QSTAGES; ++s) {
                 mbar_init(&sh.qfull[s], 1);
@@ -582,7 +517,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync();                 // both CTAs' barriers exist before any remote arrive
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sh.tmem_base;
 
@@ -595,8 +530,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         if (lane == 0) {
             int stage = 0, qs = 0, loads = 0;
             uint32_t phase = 0, qphase = 0;
-            for (int tile = first; tile < num_tiles; tile += stride) {
-                const int m0 = tile_m0(tile), n0 = tile_n0(tile);
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
                 for (int kb = 0; kb < nk; ++kb) {
                     if constexpr (C::FUSED) {
                         if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
@@ -604,8 +539,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                             goto producer_done;
                         const int start = kb * QFmt<TYPE>::SB_BYTES;
                         mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
-                        tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, &tmW, &sh.qfull[qs], (start & ~15) >> 2,
-                                    m0 + rank * C::Q_ROWS);
+                        tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, &tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
                         advance(qs, qphase, QSTAGES);
                     }
 #pragma unroll 1
@@ -638,7 +572,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         if (lane == 0) {
             int stage = 0, wstage = 0, acc = 0;
             uint32_t phase = 0, wphase = 0, acc_phase = 0;
-            for (int tile = first; tile < num_tiles; tile += stride) {
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
@@ -649,8 +583,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                             goto mma_done;
                         if constexpr (C::FUSED) {
-                            if (!wait_phase<true>(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err,
-                                                  kErrTimeoutMma))
+                            if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                                 goto mma_done;
                         }
                         tc_fence_after();
@@ -663,8 +596,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         mma_commit(&sh.emptyx[stage]);     // frees the stages when these MMAs finish
                         advance(stage, phase, XS);
                         if constexpr (C::FUSED) {
-                            // both CTAs' decode warps write this stage in both CTAs
-                            mma_commit_multicast(&sh.emptyw[wstage], 0x3);
+                            mma_commit(&sh.emptyw[wstage]);
                             advance(wstage, wphase, WS);
                         }
                     }
@@ -683,8 +615,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter .. +31
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = first; tile < num_tiles; tile += stride) {
-            const int m0 = tile_m0(tile), n0 = tile_n0(tile);
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
             if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
                                                            sh.abort_flag, err, kErrTimeoutEpilogue)))
                 break;
@@ -714,9 +646,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         // unit u = 0..7 <- warps 6, 7, 8, 10, 11, 12, 14, 15 (none on sub-partition 1)
         const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
         if (warp != 9 && warp != 13) {
-            const int rl = (u & 1) * 32 + lane;            // row of this CTA's 64-row slice
-            dequant_role<TYPE>(sh, qslots, smem_u32(ws), static_cast<uint32_t>(rank ^ 1), rl,
-                               rank * C::Q_ROWS + rl, u >> 1, lane, first, num_tiles, stride, nk, limit_ns, err);
+            const int r = (u & 3) * 32 + lane;             // weight row within the tile
+            dequant_role<TYPE>(sh, qslots, smem_u32(ws), r, u >> 2, lane, num_tiles, nk, limit_ns, err);
         }
     }
 
@@ -728,9 +659,6 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         while (globaltimer_ns() - t0 < 200000ull) {
         }
     }
-    // No CTA leaves while its peer may still write into its shared memory or
-    // arrive on its barriers.
-    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -764,7 +692,7 @@ cudaError_t launch_typed(const GemmArgs &a, EncodeFn enc, cudaStream_t stream) {
     if constexpr (C::FUSED) {
         const int64_t row_bytes = (a.in_f / SB) * QFmt<TYPE>::SB_BYTES;
         if (!encode_2d(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, row_bytes / 4, a.out_f, row_bytes,
-                       QFmt<TYPE>::BOX / 4, C::Q_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+                       QFmt<TYPE>::BOX / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
         if (!encode_2d(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.W, a.in_f, a.out_f, a.in_f * 2, BK, BM,
@@ -773,42 +701,14 @@ cudaError_t launch_typed(const GemmArgs &a, EncodeFn enc, cudaStream_t stream) {
     }
     const int m_tiles = static_cast<int>((a.out_f + BM - 1) / BM);
     const int n_tiles = static_cast<int>((a.T + BN - 1) / BN);
-    // work units: (weight tile, token-tile pair) per cluster in fused mode
-    const int units = m_tiles * ((n_tiles + C::PAIR - 1) / C::PAIR);
+    const int num_tiles = m_tiles * n_tiles;
+    const int grid = num_tiles < a.num_sms ? num_tiles : a.num_sms;
     auto kern = prefill_gemm_kernel<TYPE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if constexpr (C::FUSED) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
-            cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C::PAIR;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // as many resident clusters (CTA pairs, or single CTAs) as the GPU holds
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-        cfg.gridDim = dim3(C::PAIR * a.num_sms / C::PAIR, 1, 1);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-            cudaGetLastError();
-            n = a.num_sms / C::PAIR;
-        }
-        max_clusters = n;
-    }
-    const int clusters = units < max_clusters ? units : max_clusters;
-    cfg.gridDim = dim3(C::PAIR * clusters, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.Y, static_cast<int>(a.out_f), static_cast<int>(a.T),
-                           static_cast<int>(a.in_f / SB), m_tiles, units, a.err, a.wait_limit_ns, a.inject_stall);
-    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmX, tmW, a.Y, static_cast<int>(a.out_f),
+                                                      static_cast<int>(a.T), static_cast<int>(a.in_f / SB),
+                                                      m_tiles, num_tiles, a.err, a.wait_limit_ns, a.inject_stall);
     return cudaGetLastError();
 }
 
