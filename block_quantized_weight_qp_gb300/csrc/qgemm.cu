@@ -53,7 +53,6 @@ constexpr int SB = 256;                       // K per quantized slice (one supe
 constexpr int X_STAGE_BYTES = BN * BK * 2;    // 32 KiB
 constexpr int W_STAGE_BYTES = BM * BK * 2;    // 16 KiB
 constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 256 columns
-constexpr int QSTAGES = 2;                    // quantized slices in flight
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 // Geometry of one quantized slice: SB_BYTES bytes of one row cover 256
@@ -68,19 +67,21 @@ template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 240;
 template <> struct QFmt<kQ8_0> { static constexpr int SB_BYTES = 272, BOX = 272; };  // 8 blocks
 template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };            // fp16 weight
 
-// Pipeline depths.  X tiles (TMA) and fp16 W tiles (written by the dequant
-// warps in fused mode) have rings of their own, so X can be prefetched deeper
-// than the decode runs ahead; the cached mode stages X and W together.
-// Shared memory: XST * 32 KiB + WST * 16 KiB + 2 quantized slices, <= 227 KiB.
-template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3; };   // Q4_K, Q2_K
-template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 2; };
-template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3; };
-template <> struct Depth<0> { static constexpr int XST = 4, WST = 4; };
+// Pipeline depths.  X tiles (TMA), fp16 W tiles (written by the dequant
+// warps in fused mode) and quantized slices (TMA, one superblock = four K
+// steps each) have rings of their own, so X can be prefetched deeper than
+// the decode runs ahead; the cached mode stages X and W together.
+// Shared memory: XST * 32 KiB + WST * 16 KiB + QST slices, <= 227 KiB.
+template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3, QST = 2; };   // Q4_K, Q2_K
+template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 3, QST = 1; };
+template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3, QST = 2; };
+template <> struct Depth<0> { static constexpr int XST = 4, WST = 4, QST = 0; };
 
 template <int TYPE> struct Cfg {
     static constexpr bool FUSED = TYPE != 0;
     static constexpr int XST = Depth<TYPE>::XST;
     static constexpr int WST = Depth<TYPE>::WST;
+    static constexpr int QST = Depth<TYPE>::QST;
     // Dequant warps sit only on SM sub-partitions 0, 2 and 3 (warp w runs on
     // sub-partition w % 4): sub-partition 1 keeps its issue slots for the
     // single MMA-issuing thread of warp 1.  Warps 6..15 minus 9 and 13.
@@ -90,10 +91,10 @@ template <int TYPE> struct Cfg {
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W = OFF_X + XST * X_STAGE_BYTES;
     static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
-    static constexpr int OFF_BAR = OFF_Q + (FUSED ? QSTAGES * Q_SLOT_BYTES : 0);
+    static constexpr int OFF_BAR = OFF_Q + QST * Q_SLOT_BYTES;
     // barriers: fullx[XST], emptyx[XST], fullw[WST], emptyw[WST], qfull[Q], qempty[Q],
     //           accfull[2], accempty[2], done
-    static constexpr int NBAR = 2 * XST + 2 * WST + 2 * QSTAGES + 5;
+    static constexpr int NBAR = 2 * XST + 2 * WST + 2 * QST + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
     static_assert(OFF_Q % 1024 == 0 && Q_SLOT_BYTES % 16 == 0, "alignment");
@@ -224,6 +225,7 @@ template <int TYPE, int WO> struct Dec;
 // Q4_K: sub-block 2A+h holds values 64A+32h..; they are the low (h=0) or
 // high (h=1) nibbles of qs[32A .. 32A+31].
 template <int WO> struct Dec<kQ4_K, WO> {
+    static constexpr bool REGS = false;          // atom() reads the staged slice
     pair_t dl2[4], nml2[4];
     __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int h) {
         const uint4 hd = *reinterpret_cast<const uint4 *>(row);   // d, dmin, scales[0..11]
@@ -270,6 +272,7 @@ template <int WO> struct Dec<kQ4_K, WO> {
 // and a high-byte plane).  The thread keeps the slice's 64 qs bytes in
 // registers: K steps 2n and 2n+1 read the same bytes with different j.
 template <int WO> struct Dec<kQ2_K, WO> {
+    static constexpr bool REGS = true;           // slice() keeps all it needs in registers
     float d, dmin;
     uint32_t sc[4], qs[16];
     __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int) {
@@ -323,6 +326,7 @@ template <int WO> struct Dec<kQ2_K, WO> {
 // so over a slice the thread reads ql[64n + 32h ..+31] and qh[32n ..+31] for
 // n = 0, 1: 32 words, realigned once per slice and kept in registers.
 template <int WO> struct Dec<kQ6_K, WO> {
+    static constexpr bool REGS = true;
     float d;
     uint32_t sc[4], ql[16], qh[16];
     __device__ __forceinline__ void slice(const uint8_t *row, uint32_t hs16, int h) {
@@ -374,6 +378,7 @@ template <int WO> struct Dec<kQ6_K, WO> {
 // and 2A+1 (h = 1), i.e. bytes 68A .. 68A+67 = d0, q0[32], d1, q1[32].
 // q + 128 = byte XOR 0x80.
 template <int WO> struct Dec<kQ8_0, WO> {
+    static constexpr bool REGS = false;
     __device__ __forceinline__ void slice(const uint8_t *, uint32_t, int) {}
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
@@ -396,7 +401,10 @@ template <int WO> struct Dec<kQ8_0, WO> {
 };
 
 // One superblock slice of one half-row: four K steps, each waiting for its
-// W stage to be free, decoding into it and signalling the MMA.
+// W stage to be free, decoding into it and signalling the MMA.  Decoders
+// whose slice() keeps everything the four K steps need in registers (REGS)
+// hand the staged slice back to the producer right away, so the next slice's
+// copy overlaps these four K steps.
 #ifdef QP_NOINLINE_SLICE
 #define QP_SLICE_INLINE __noinline__
 #else
@@ -404,11 +412,15 @@ template <int WO> struct Dec<kQ8_0, WO> {
 #endif
 template <int TYPE, int WO>
 __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int p,
-                                              uint32_t ws_addr, const ChunkAddr &ca, int lane, int &stage,
-                                              uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
+                                              uint32_t ws_addr, const ChunkAddr &ca, uint64_t *qempty, int lane,
+                                              int &stage, uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
     constexpr int S = Cfg<TYPE>::WST;
     Dec<TYPE, WO> dec;
     dec.slice(row, hs16, p);
+    if constexpr (Dec<TYPE, WO>::REGS) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty);
+    }
 #define QP_DEQUANT_ATOM(A)                                                                                     \
     {                                                                                                          \
         if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
@@ -444,18 +456,20 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qs
             bool ok;
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
-                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err); break;
+                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, lane, stage, phase, limit_ns, err);
+                ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err);
             }
             if (!ok) return;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.qempty[qs]);
-            advance(qs, qphase, QSTAGES);
+            if constexpr (!Dec<TYPE, 0>::REGS) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.qempty[qs]);
+            }
+            advance(qs, qphase, C::QST);
         }
     }
 }
@@ -478,8 +492,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     sh.fullw = bars + 2 * XS;
     sh.emptyw = bars + 2 * XS + WS;
     sh.qfull = bars + 2 * XS + 2 * WS;
-    sh.qempty = sh.qfull + QSTAGES;
-    sh.accfull = sh.qempty + QSTAGES;
+    sh.qempty = sh.qfull + C::QST;
+    sh.accfull = sh.qempty + C::QST;
     sh.accempty = sh.accfull + 2;
     sh.done = sh.accfull + 4;
     sh.tmem_base = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -497,7 +511,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                 mbar_init(&sh.fullw[s], C::DQ_WARPS);      // each dequant warp
                 mbar_init(&sh.emptyw[s], 1);               // MMA commit
             }
-            for (int s = 0; s < QSTAGES; ++s) {
+            for (int s = 0; s < C::QST; ++s) {
                 mbar_init(&sh.qfull[s], 1);
                 mbar_init(&sh.qempty[s], C::DQ_WARPS);
             }
@@ -540,7 +554,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         const int start = kb * QFmt<TYPE>::SB_BYTES;
                         mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
                         tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, &tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
-                        advance(qs, qphase, QSTAGES);
+                        advance(qs, qphase, C::QST);
                     }
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
