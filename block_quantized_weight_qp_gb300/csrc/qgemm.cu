@@ -72,7 +72,7 @@ template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };     
 // steps each) have rings of their own, so X can be prefetched deeper than
 // the decode runs ahead; the cached mode stages X and W together.
 // Shared memory: XST * 32 KiB + WST * 16 KiB + QST slices, <= 227 KiB.
-template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 3, QST = 2; };   // Q4_K, Q2_K
+template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 4, QST = 1; };   // Q4_K, Q2_K
 template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 3, QST = 1; };
 template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3, QST = 2; };
 template <> struct Depth<0> { static constexpr int XST = 4, WST = 4, QST = 0; };
@@ -223,11 +223,17 @@ struct ChunkAddr {
 template <int TYPE, int WO> struct Dec;
 
 // Q4_K: sub-block 2A+h holds values 64A+32h..; they are the low (h=0) or
-// high (h=1) nibbles of qs[32A .. 32A+31].
+// high (h=1) nibbles of qs[32A .. 32A+31].  The thread keeps its nibbles of
+// the whole slice (32 words, one per 4 values) in registers.
 template <int WO> struct Dec<kQ4_K, WO> {
-    static constexpr bool REGS = false;          // atom() reads the staged slice
+    static constexpr bool REGS = true;           // slice() keeps all it needs in registers
     pair_t dl2[4], nml2[4];
+    uint32_t qn[32];
     __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int h) {
+        uint32_t w[32];
+        row_words<16, 32, false>(row, 0, w);       // qs[0 .. 127]
+#pragma unroll
+        for (int k = 0; k < 32; ++k) qn[k] = (w[k] >> (4 * h)) & 0x0F0F0F0Fu;
         const uint4 hd = *reinterpret_cast<const uint4 *>(row);   // d, dmin, scales[0..11]
         const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
 #pragma unroll
@@ -250,15 +256,12 @@ template <int WO> struct Dec<kQ4_K, WO> {
         }
     }
     template <int A>
-    __device__ __forceinline__ void atom(const uint8_t *row, uint32_t, int h, uint32_t tile,
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int, uint32_t tile,
                                          const ChunkAddr &ca) const {
-        uint32_t w[8];
-        row_words<16 + 32 * A, 8, false>(row, 0, w);
-        const int sh = 4 * h;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint2 lo = word_affine((w[2 * c] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
-            const uint2 hi = word_affine((w[2 * c + 1] >> sh) & 0x0F0F0F0Fu, dl2[A], nml2[A]);
+            const uint2 lo = word_affine(qn[8 * A + 2 * c], dl2[A], nml2[A]);
+            const uint2 hi = word_affine(qn[8 * A + 2 * c + 1], dl2[A], nml2[A]);
             sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
         }
     }
