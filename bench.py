@@ -202,31 +202,46 @@ class Layer:
                 qp.qp_dequant_f16(qt, w, out_f, in_f, h)
                 self.W16.append(h)
 
-    def flops(self, T=None):
+    def flops(self, T=None, idx=None):
         T = self.T if T is None else T
-        return sum(2 * T * out_f * in_f for name, out_f, in_f, _, _ in self.wl["projections"]
-                   if not self.only or name == self.only)
+        return sum(2 * T * out_f * in_f for i, (name, out_f, in_f, _, _) in enumerate(self.wl["projections"])
+                   if (not self.only or name == self.only) and (idx is None or i in idx))
+
+    def launches(self, grouped=True):
+        """The step's launches as (block type, [projection indices]): with
+        grouping, each run of consecutive projections of one type is one
+        qp_prefill_gemm_group launch; without, one launch per projection."""
+        out = []
+        for i, (name, _, _, _, qt) in enumerate(self.wl["projections"]):
+            if self.only and name != self.only:
+                continue
+            if grouped and out and out[-1][0] == qt and len(out[-1][1]) < 8:
+                out[-1][1].append(i)
+            else:
+                out.append((qt, [i]))
+        return out
 
 
-def run_layer(qp, layer, stream, events=None, mode="fused", chunk=None, X=None, Y=None):
-    """Launch the seven projections (or the one named by layer.only);
-    events[i] = (start, end) recorded around projection i when given."""
-    for i, (name, out_f, in_f, src, qt) in enumerate(layer.wl["projections"]):
-        if layer.only and name != layer.only:
-            continue
-        x = layer.X[src] if X is None else X[src]
-        y = layer.Y[i] if Y is None else Y[i]
+def run_layer(qp, layer, stream, events=None, mode="fused", chunk=None, X=None, Y=None, grouped=True):
+    """Launch the seven projections (or the one named by layer.only) through
+    the grouped entry points; events[k] = (start, end) recorded around
+    launch k of layer.launches(grouped) when given."""
+    for k, (qt, idx) in enumerate(layer.launches(grouped)):
+        descs = []
+        for i in idx:
+            _, out_f, in_f, src, _ = layer.wl["projections"][i]
+            w = layer.W[i] if mode == "fused" else layer.W16[i]
+            descs.append((w, out_f, in_f, layer.X[src] if X is None else X[src],
+                          layer.Y[i] if Y is None else Y[i]))
+        ty = qt if mode == "fused" else 0
         if events is not None:
-            events[i][0].record(stream)
+            events[k][0].record(stream)
         if chunk:
-            qp.qp_prefill_chunked(qt, layer.W[i], layer.W16[i] if layer.W16 else None, out_f, in_f, x, layer.T, y,
-                                  chunk, 0 if mode == "fused" else 1, stream)
-        elif mode == "fused":
-            qp.qp_prefill_gemm(qt, layer.W[i], out_f, in_f, x, layer.T, y, stream)
+            qp.qp_prefill_chunked_group(ty, descs, layer.T, chunk, stream)
         else:
-            qp.qp_prefill_gemm_f16w(layer.W16[i], out_f, in_f, x, layer.T, y, stream)
+            qp.qp_prefill_gemm_group(ty, descs, layer.T, stream)
         if events is not None:
-            events[i][1].record(stream)
+            events[k][1].record(stream)
 
 
 def time_layer(qp, layer, stream, steps, warmup, mode="fused", chunk=None):
@@ -367,15 +382,16 @@ def main_qp(args):
     layer = Layer(wl, rank, device, need_f16=args.mode == "cached", only=args.only_proj)
     T = layer.T
     flops = layer.flops()
-    nproj = len(wl["projections"])
-    nlaunch = 1 if args.only_proj else nproj
+    grouped = not args.no_group
+    launches = layer.launches(grouped)
+    nlaunch = len(launches)
 
-    # ---- timed region: K steps, per-projection events on the launch stream
+    # ---- timed region: K steps, per-launch events on the launch stream
     for _ in range(args.warmup):
-        run_layer(qp, layer, stream, mode=args.mode)
+        run_layer(qp, layer, stream, mode=args.mode, grouped=grouped)
     torch.cuda.synchronize()
     qp.qp_check(stream)
-    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nproj)]
+    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nlaunch)]
               for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -384,7 +400,7 @@ def main_qp(args):
     with sampler:
         e0.record(stream)
         for s in range(args.steps):
-            run_layer(qp, layer, stream, events=events[s], mode=args.mode)
+            run_layer(qp, layer, stream, events=events[s], mode=args.mode, grouped=grouped)
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -393,24 +409,31 @@ def main_qp(args):
     max_ms = max_over_ranks(ms, world, device)
     value = job_throughput(flops, world, max_ms) / 1e12
     tok_s = job_throughput(T, world, max_ms)
+    per_launch = []
+    for k, (qt, idx) in enumerate(launches):
+        t_ms = statistics.mean(events[s][k][0].elapsed_time(events[s][k][1]) for s in range(args.steps))
+        f = layer.flops(idx=idx)
+        per_launch.append({"type": synth.NAMES[qt], "projections": [wl["projections"][i][0] for i in idx],
+                           "ms": round(t_ms, 4), "tflops": round(f / (t_ms / 1e3) / 1e12, 1), "flops": f})
+    # dominant kernel: the launch with the most time (mean over the timed steps)
+    dom_launch = max(per_launch, key=lambda d: d["ms"])
+    dom = dom_launch["type"]
+    achieved = dom_launch["flops"] / (dom_launch["ms"] / 1e3) / 1e12
+    # breakdown by projection: the same projections launched one at a time
     per_proj = []
-    for i, (name, out_f, in_f, _, qt) in enumerate(wl["projections"]):
-        if args.only_proj and name != args.only_proj:
-            continue
-        t_ms = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(args.steps)]
-        f = 2.0 * T * out_f * in_f
-        per_proj.append({"proj": name, "type": synth.NAMES[qt], "out": out_f, "in": in_f,
-                         "ms": round(statistics.mean(t_ms), 4),
-                         "tflops": round(f / (statistics.mean(t_ms) / 1e3) / 1e12, 1)})
-    # dominant kernel: the fused GEMM instantiation with the most time
-    by_type = {}
-    for p in per_proj:
-        d = by_type.setdefault(p["type"], [0.0, 0.0, 0])
-        d[0] += 2.0 * T * p["out"] * p["in"]
-        d[1] += p["ms"]
-        d[2] += 1
-    dom = max(by_type, key=lambda k: by_type[k][1])
-    achieved = by_type[dom][0] / (by_type[dom][1] / 1e3) / 1e12
+    single = layer.launches(grouped=False)
+    ev1 = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in single]
+           for _ in range(args.steps)]
+    run_layer(qp, layer, stream, mode=args.mode, grouped=False)
+    for s in range(args.steps):
+        run_layer(qp, layer, stream, events=ev1[s], mode=args.mode, grouped=False)
+    torch.cuda.synchronize()
+    qp.qp_check(stream)
+    for k, (qt, (i,)) in enumerate(single):
+        name, out_f, in_f, _, _ = wl["projections"][i]
+        t_ms = statistics.mean(ev1[s][k][0].elapsed_time(ev1[s][k][1]) for s in range(args.steps))
+        per_proj.append({"proj": name, "type": synth.NAMES[qt], "out": out_f, "in": in_f, "ms": round(t_ms, 4),
+                         "tflops": round(2.0 * T * out_f * in_f / (t_ms / 1e3) / 1e12, 1)})
     peak = peaks["bf16_tflops"]
     traffic = None
     if NCU_TRAFFIC["source_sha"] and NCU_TRAFFIC["source_sha"] == kernel_source_sha():
@@ -418,8 +441,10 @@ def main_qp(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "traffic_what": NCU_TRAFFIC["what"] if traffic else None,
-                "kernel": ("prefill_gemm_kernel<%s> (fused dequant, tcgen05)" % dom if args.mode == "fused"
-                           else "prefill_gemm_kernel<f16 weight> (cached mode, tcgen05)"),
+                "kernel": ("prefill_gemm_kernel<%s> (fused dequant, tcgen05; one launch over %s)"
+                           % (dom, ",".join(dom_launch["projections"])) if args.mode == "fused"
+                           else "prefill_gemm_kernel<f16 weight> (cached mode, tcgen05; one launch over %s)"
+                           % ",".join(dom_launch["projections"])),
                 "peak_source": "%s dense bf16 burst (fp16 runs at the bf16 rate)" % peak_src}
 
     # ---- end to end through the C ABI with host buffers
@@ -432,6 +457,8 @@ def main_qp(args):
     # Host->device copies of X run on one copy stream and the device->host read
     # of each projection's Y on another as soon as that projection is done,
     # so both directions overlap the GEMMs; steps do not overlap each other.
+    # The read-back of Y bounds this path, so here every projection is its own
+    # launch: its Y starts moving as soon as it is written.
     h2d_s = torch.cuda.Stream(device)
     d2h_streams = [torch.cuda.Stream(device) for _ in range(max(1, args.d2h_streams))]
 
@@ -445,20 +472,24 @@ def main_qp(args):
                 Xd[k].copy_(Xh[k], non_blocking=True)
                 ready[k] = torch.cuda.Event()
                 ready[k].record(h2d_s)
-        for i, (name, out_f, in_f, src, qt) in enumerate(wl["projections"]):
-            if args.only_proj and name != args.only_proj:
-                continue
-            stream.wait_event(ready[src])
-            qp.qp_prefill_gemm(qt, layer.W[i], out_f, in_f, Xd[src], T, layer.Y[i], stream)
+        for qt, idx in layer.launches(grouped=False):
+            descs = []
+            for i in idx:
+                _, out_f, in_f, src, _ = wl["projections"][i]
+                stream.wait_event(ready[src])
+                descs.append((layer.W[i], out_f, in_f, Xd[src], layer.Y[i]))
+            qp.qp_prefill_gemm_group(qt, descs, T, stream)
             done = torch.cuda.Event()
             done.record(stream)
-            # the read-back of Y is split row-wise over the copy streams
+            # the read-back of each Y is split row-wise over the copy streams
             parts = len(d2h_streams)
             rows = -(-T // parts)
-            for j, ds in enumerate(d2h_streams):
-                ds.wait_event(done)
-                with torch.cuda.stream(ds):
-                    Yh[i][j * rows:(j + 1) * rows].copy_(layer.Y[i][j * rows:(j + 1) * rows], non_blocking=True)
+            for i in idx:
+                for j, ds in enumerate(d2h_streams):
+                    ds.wait_event(done)
+                    with torch.cuda.stream(ds):
+                        Yh[i][j * rows:(j + 1) * rows].copy_(layer.Y[i][j * rows:(j + 1) * rows],
+                                                             non_blocking=True)
         for ds in d2h_streams:
             stream.wait_stream(ds)
 
@@ -521,6 +552,7 @@ def main_qp(args):
                             + sum(y.numel() * 4 for y in layer.Y)) / 1e9)},
             "tok_per_s": round(tok_s, 1),
             "pct_dense_fp16_peak": round(100.0 * value / (peak * world), 2),
+            "per_launch": [{k: v for k, v in d.items() if k != "flops"} for d in per_launch],
             "per_projection": per_proj,
             "roofline": roofline,
             "e2e": e2e,
@@ -591,6 +623,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--only-proj", default=None, help="time only this projection (profiling runs)")
+    p.add_argument("--no-group", action="store_true",
+                   help="launch the step's projections one at a time instead of one grouped launch per type")
     p.add_argument("--d2h-streams", type=int, default=1, help="copy streams for the e2e read-back of Y")
     p.add_argument("--mode", choices=["fused", "cached"], default="fused",
                    help="cached: the same step over f16 weights made once by qp_dequant_f16")

@@ -27,8 +27,16 @@ QP_ERR_NO_DEVICE = 7
 
 # Every symbol include/qp.h declares.
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",
-           "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_chunked", "qp_check",
-           "qp_set_wait_limit_ns", "qp_debug_inject_stall")
+           "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_gemm_group", "qp_prefill_chunked_group",
+           "qp_prefill_chunked", "qp_check", "qp_set_wait_limit_ns", "qp_debug_inject_stall")
+
+QP_MAX_GROUP = 8
+
+
+class QPGemmDesc(ctypes.Structure):
+    """qp_gemm_desc: one projection of a grouped call."""
+    _fields_ = [("W", ctypes.c_void_p), ("out_f", ctypes.c_int64), ("in_f", ctypes.c_int64),
+                ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
 
 _lib = None
 
@@ -57,6 +65,8 @@ def load():
         lib.qp_dequant_f16.argtypes = [i, vp, i64, i64, vp, vp]
         lib.qp_prefill_gemm.argtypes = [i, vp, i64, i64, vp, i64, vp, vp]
         lib.qp_prefill_gemm_f16w.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+        lib.qp_prefill_gemm_group.argtypes = [i, ctypes.POINTER(QPGemmDesc), i, i64, vp]
+        lib.qp_prefill_chunked_group.argtypes = [i, ctypes.POINTER(QPGemmDesc), i, i64, i64, vp]
         lib.qp_prefill_chunked.argtypes = [i, vp, vp, i64, i64, vp, i64, vp, i64, i, vp]
         lib.qp_check.argtypes = [vp]
         lib.qp_set_wait_limit_ns.argtypes = [u64]
@@ -64,7 +74,7 @@ def load():
         lib.qp_debug_inject_stall.argtypes = [i]
         lib.qp_debug_inject_stall.restype = None
         for name in ("qp_dequant_f32", "qp_dequant_f16", "qp_prefill_gemm", "qp_prefill_gemm_f16w",
-                     "qp_prefill_chunked", "qp_check"):
+                     "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_check"):
             getattr(lib, name).restype = i
         _lib = lib
     return _lib
@@ -130,6 +140,24 @@ def qp_prefill_gemm(qtype, W, out_f, in_f, X, T, Y, stream=None):
 def qp_prefill_gemm_f16w(W16, out_f, in_f, X, T, Y, stream=None):
     _ok(load().qp_prefill_gemm_f16w(_ptr(W16), out_f, in_f, _ptr(X), T, _ptr(Y), _stream(stream)),
         "qp_prefill_gemm_f16w")
+
+
+def _descs(descs):
+    arr = (QPGemmDesc * max(len(descs), 1))()
+    for k, (W, out_f, in_f, X, Y) in enumerate(descs):
+        arr[k] = QPGemmDesc(_ptr(W), out_f, in_f, _ptr(X), _ptr(Y))
+    return arr
+
+
+def qp_prefill_gemm_group(qtype, descs, T, stream=None):
+    """descs: sequence of (W, out_f, in_f, X, Y); qtype 0 = fp16 weights (cached mode)."""
+    _ok(load().qp_prefill_gemm_group(qtype, _descs(descs), len(descs), T, _stream(stream)),
+        "qp_prefill_gemm_group")
+
+
+def qp_prefill_chunked_group(qtype, descs, T, chunk, stream=None):
+    _ok(load().qp_prefill_chunked_group(qtype, _descs(descs), len(descs), T, chunk, _stream(stream)),
+        "qp_prefill_chunked_group")
 
 
 def qp_prefill_chunked(qtype, W, W16, out_f, in_f, X, T, Y, chunk, mode, stream=None):

@@ -102,29 +102,40 @@ qp_status gemm_shape_ok(int64_t out_f, int64_t in_f, int64_t T) {
     return QP_OK;
 }
 
-qp_status run_gemm(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T, float *Y,
-                   void *stream) {
+static_assert(QP_MAX_GROUP == qp::kMaxGroup, "group limit of the C ABI and the kernel");
+
+// One launch over n already-validated projections of one type.
+qp_status run_gemms(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream) {
     DeviceInfo *d = nullptr;
     qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    qp::GemmArgs a;
-    a.type = type;
-    a.out_f = out_f;
-    a.in_f = in_f;
-    a.T = T;
-    a.W = W;
-    a.X = X;
-    a.Y = Y;
-    a.num_sms = d->num_sms;
-    a.err = d->err;
-    a.wait_limit_ns = g_wait_limit_ns.load();
-    a.inject_stall = g_inject_stall.exchange(-1);
-    const cudaError_t e = qp::launch_prefill_gemm(a, g_encode, static_cast<cudaStream_t>(stream));
+    qp::GemmArgs a[qp::kMaxGroup];
+    const int inject = g_inject_stall.exchange(-1);
+    for (int i = 0; i < n; ++i) {
+        a[i].type = type;
+        a[i].out_f = descs[i].out_f;
+        a[i].in_f = descs[i].in_f;
+        a[i].T = T;
+        a[i].W = descs[i].W;
+        a[i].X = descs[i].X;
+        a[i].Y = descs[i].Y;
+        a[i].num_sms = d->num_sms;
+        a[i].err = d->err;
+        a[i].wait_limit_ns = g_wait_limit_ns.load();
+        a[i].inject_stall = inject;
+    }
+    const cudaError_t e = qp::launch_prefill_gemm(a, n, g_encode, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
     return QP_OK;
+}
+
+qp_status run_gemm(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T, float *Y,
+                   void *stream) {
+    const qp_gemm_desc d = {W, out_f, in_f, X, Y};
+    return run_gemms(type, &d, 1, T, stream);
 }
 
 qp_status check_quant_gemm(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T,
@@ -144,6 +155,19 @@ qp_status check_f16w_gemm(const uint16_t *W16, int64_t out_f, int64_t in_f, cons
     const qp_status s = gemm_shape_ok(out_f, in_f, T);
     if (s != QP_OK) return s;
     if (!aligned16(W16) || !aligned16(X) || !aligned16(Y)) return QP_ERR_MISALIGNED;
+    return QP_OK;
+}
+
+qp_status check_group(int type, const qp_gemm_desc *descs, int n, int64_t T) {
+    if (!descs || n < 1 || n > QP_MAX_GROUP) return QP_ERR_INVALID_PARAMETER;
+    if (type != 0 && !valid_type(type)) return QP_ERR_UNSUPPORTED_TYPE;
+    for (int i = 0; i < n; ++i) {
+        const qp_gemm_desc &g = descs[i];
+        const qp_status s =
+            type == 0 ? check_f16w_gemm(static_cast<const uint16_t *>(g.W), g.out_f, g.in_f, g.X, T, g.Y)
+                      : check_quant_gemm(type, g.W, g.out_f, g.in_f, g.X, T, g.Y);
+        if (s != QP_OK) return s;
+    }
     return QP_OK;
 }
 
@@ -219,6 +243,33 @@ qp_status qp_prefill_gemm_f16w(const uint16_t *W16, int64_t out_f, int64_t in_f,
     const qp_status s = check_f16w_gemm(W16, out_f, in_f, X, T, Y);
     if (s != QP_OK) return s;
     return run_gemm(0, W16, out_f, in_f, X, T, Y, stream);
+}
+
+qp_status qp_prefill_gemm_group(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream) {
+    const qp_status s = check_group(type, descs, n, T);
+    if (s != QP_OK) return s;
+    return run_gemms(type, descs, n, T, stream);
+}
+
+qp_status qp_prefill_chunked_group(int type, const qp_gemm_desc *descs, int n, int64_t T, int64_t chunk,
+                                   void *stream) {
+    if (chunk <= 0) return QP_ERR_INVALID_PARAMETER;
+    qp_status s = check_group(type, descs, n, T);
+    if (s != QP_OK) return s;
+    // Row c of X starts at byte 2*c*in_f, of Y at 4*c*out_f: both stay
+    // 16-byte aligned because in_f % 256 == 0 and out_f % 4 == 0.
+    qp_gemm_desc part[QP_MAX_GROUP];
+    for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+        const int64_t rows = T - c0 < chunk ? T - c0 : chunk;
+        for (int i = 0; i < n; ++i) {
+            part[i] = descs[i];
+            part[i].X = descs[i].X + c0 * descs[i].in_f;
+            part[i].Y = descs[i].Y + c0 * descs[i].out_f;
+        }
+        s = run_gemms(type, part, n, rows, stream);
+        if (s != QP_OK) return s;
+    }
+    return QP_OK;
 }
 
 qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64_t out_f, int64_t in_f,

@@ -34,7 +34,9 @@
 // Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
 // latches an error bit in the device error word, makes every role stop,
 // lets copies in flight land, frees its TMEM and returns.
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -107,6 +109,38 @@ struct Shared {
     uint32_t *tmem_base;
     volatile uint32_t *abort_flag;
 };
+
+// A launch runs up to MAX_GROUPS projections of one weight type over the
+// same T tokens ("groups").  Tiles are numbered group after group, in the
+// order the host chose (longest K first), weight-row tile fastest within a
+// group; CTA b takes tiles b, b + gridDim.x, ...  Every output tile runs the
+// same K loop however the tiles are scheduled, so a projection's result does
+// not depend on what else shares its launch.
+constexpr int MAX_GROUPS = kMaxGroup;
+struct GroupParams {
+    CUtensorMap tmX[MAX_GROUPS];   // X [T x in] fp16, box 64 x 256, 128-B swizzle
+    CUtensorMap tmW[MAX_GROUPS];   // quantized rows (box BOX/4 words x 128 rows) or fp16 W (64 x 128)
+    float *Y[MAX_GROUPS];
+    int out_f[MAX_GROUPS];
+    int nk[MAX_GROUPS];            // 256-value K slices per weight row (in_f / 256)
+    int m_tiles[MAX_GROUPS];       // 128-row weight tiles
+    int tile_end[MAX_GROUPS];      // one past the group's last tile
+    int n_groups, T, num_tiles;
+};
+
+struct TileLoc {
+    int g, m0, n0;
+};
+
+__device__ __forceinline__ TileLoc locate(const GroupParams &p, int tile) {
+    int g = 0, base = 0;
+    while (g + 1 < p.n_groups && tile >= p.tile_end[g]) {
+        base = p.tile_end[g];
+        ++g;
+    }
+    const int t = tile - base;
+    return {g, (t % p.m_tiles[g]) * BM, (t / p.m_tiles[g]) * BN};
+}
 
 // Bounded wait on a barrier phase.  Returns false (and stops every role of
 // this CTA) when the limit passes or another role already gave up.
@@ -443,14 +477,15 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
 }
 
 template <int TYPE>
-__device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qslots, uint32_t ws_addr, int r,
-                                             int p, int lane, int num_tiles, int nk, uint64_t limit_ns,
+__device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams &gp, const uint8_t *qslots,
+                                             uint32_t ws_addr, int r, int p, int lane, uint64_t limit_ns,
                                              uint32_t *err) {
     using C = Cfg<TYPE>;
     const ChunkAddr ca(r, p);
     int stage = 0, qs = 0;
     uint32_t phase = 0, qphase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
+        const int nk = gp.nk[locate(gp, tile).g];
         for (int kb = 0; kb < nk; ++kb) {
             if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) return;
             const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
@@ -481,9 +516,7 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const uint8_t *qs
 
 template <int TYPE>
 __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                        float *__restrict__ Y, int out_f, int T, int nk, int m_tiles, int num_tiles,
-                        uint32_t *err, uint64_t limit_ns, int inject_stall) {
+    prefill_gemm_kernel(const __grid_constant__ GroupParams gp, uint32_t *err, uint64_t limit_ns, int inject_stall) {
     using C = Cfg<TYPE>;
     constexpr int XS = C::XST, WS = C::WST;
     extern __shared__ uint8_t smem_raw[];
@@ -526,8 +559,10 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         mbar_init(sh.done, 1);
         *sh.abort_flag = 0u;
         mbar_fence_init();
-        prefetch_tensormap(&tmX);
-        prefetch_tensormap(&tmW);
+        for (int g = 0; g < gp.n_groups; ++g) {
+            prefetch_tensormap(&gp.tmX[g]);
+            prefetch_tensormap(&gp.tmW[g]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(sh.tmem_base, TMEM_COLS);
@@ -547,8 +582,10 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         if (lane == 0) {
             int stage = 0, qs = 0, loads = 0;
             uint32_t phase = 0, qphase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
+            for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
+                const TileLoc L = locate(gp, tile);
+                const int m0 = L.m0, n0 = L.n0, nk = gp.nk[L.g];
+                const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
                 for (int kb = 0; kb < nk; ++kb) {
                     if constexpr (C::FUSED) {
                         if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
@@ -556,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                             goto producer_done;
                         const int start = kb * QFmt<TYPE>::SB_BYTES;
                         mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
-                        tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, &tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
+                        tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
                         advance(qs, qphase, C::QST);
                     }
 #pragma unroll 1
@@ -572,9 +609,9 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         mbar_arrive_expect_tx(&sh.fullx[stage],
                                               C::FUSED ? X_STAGE_BYTES : X_STAGE_BYTES + W_STAGE_BYTES);
                         if (loads != inject_stall) {
-                            tma_load_2d(xs + stage * X_STAGE_BYTES, &tmX, &sh.fullx[stage], k0, n0);
+                            tma_load_2d(xs + stage * X_STAGE_BYTES, tmX, &sh.fullx[stage], k0, n0);
                             if constexpr (!C::FUSED)
-                                tma_load_2d(ws + stage * W_STAGE_BYTES, &tmW, &sh.fullx[stage], k0, m0);
+                                tma_load_2d(ws + stage * W_STAGE_BYTES, tmW, &sh.fullx[stage], k0, m0);
                         }
                         ++loads;
                         advance(stage, phase, XS);
@@ -589,7 +626,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         if (lane == 0) {
             int stage = 0, wstage = 0, acc = 0;
             uint32_t phase = 0, wphase = 0, acc_phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
+                const int nk = gp.nk[locate(gp, tile).g];
                 if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
@@ -632,8 +670,11 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter .. +31
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
+        const int T = gp.T;
+        for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
+            const TileLoc L = locate(gp, tile);
+            const int m0 = L.m0, n0 = L.n0, out_f = gp.out_f[L.g];
+            float *const Y = gp.Y[L.g];
             if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
                                                            sh.abort_flag, err, kErrTimeoutEpilogue)))
                 break;
@@ -664,7 +705,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
         if (warp != 9 && warp != 13) {
             const int r = (u & 3) * 32 + lane;             // weight row within the tile
-            dequant_role<TYPE>(sh, qslots, smem_u32(ws), r, u >> 2, lane, num_tiles, nk, limit_ns, err);
+            dequant_role<TYPE>(sh, gp, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns, err);
         }
     }
 
@@ -700,45 +741,71 @@ bool encode_2d(EncodeFn enc, CUtensorMap *map, CUtensorMapDataType dt, const voi
 }
 
 template <int TYPE>
-cudaError_t launch_typed(const GemmArgs &a, EncodeFn enc, cudaStream_t stream) {
+bool encode_group(EncodeFn enc, const GemmArgs &a, CUtensorMap *tmX, CUtensorMap *tmW) {
     using C = Cfg<TYPE>;
-    CUtensorMap tmX, tmW;
-    if (!encode_2d(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.in_f, a.T, a.in_f * 2, BK, BN,
+    if (!encode_2d(enc, tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.in_f, a.T, a.in_f * 2, BK, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+        return false;
     if constexpr (C::FUSED) {
         const int64_t row_bytes = (a.in_f / SB) * QFmt<TYPE>::SB_BYTES;
-        if (!encode_2d(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, row_bytes / 4, a.out_f, row_bytes,
-                       QFmt<TYPE>::BOX / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
+        return encode_2d(enc, tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, row_bytes / 4, a.out_f, row_bytes,
+                         QFmt<TYPE>::BOX / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
-        if (!encode_2d(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.W, a.in_f, a.out_f, a.in_f * 2, BK, BM,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
+        return encode_2d(enc, tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.W, a.in_f, a.out_f, a.in_f * 2, BK, BM,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    const int m_tiles = static_cast<int>((a.out_f + BM - 1) / BM);
-    const int n_tiles = static_cast<int>((a.T + BN - 1) / BN);
-    const int num_tiles = m_tiles * n_tiles;
-    const int grid = num_tiles < a.num_sms ? num_tiles : a.num_sms;
+}
+
+// One persistent launch over n projections of type TYPE (same T).  Groups
+// are ordered by in_f, longest first: their tiles take longest, and dealing
+// them out first keeps the CTAs' total work even.
+template <int TYPE>
+cudaError_t launch_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
+    using C = Cfg<TYPE>;
+    if (n < 1 || n > MAX_GROUPS) return cudaErrorInvalidValue;
+    int order[MAX_GROUPS];
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order, order + n, [&](int x, int y) { return a[x].in_f > a[y].in_f; });
+    GroupParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    const int64_t n_tiles = (a[0].T + BN - 1) / BN;
+    int64_t tiles = 0;
+    for (int j = 0; j < n; ++j) {
+        const GemmArgs &g = a[order[j]];
+        if (g.T != a[0].T || !encode_group<TYPE>(enc, g, &gp.tmX[j], &gp.tmW[j])) return cudaErrorInvalidValue;
+        const int64_t m_tiles = (g.out_f + BM - 1) / BM;
+        tiles += m_tiles * n_tiles;
+        if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+        gp.Y[j] = g.Y;
+        gp.out_f[j] = static_cast<int>(g.out_f);
+        gp.nk[j] = static_cast<int>(g.in_f / SB);
+        gp.m_tiles[j] = static_cast<int>(m_tiles);
+        gp.tile_end[j] = static_cast<int>(tiles);
+    }
+    gp.n_groups = n;
+    gp.T = static_cast<int>(a[0].T);
+    gp.num_tiles = static_cast<int>(tiles);
+    const int grid = gp.num_tiles < a[0].num_sms ? gp.num_tiles : a[0].num_sms;
     auto kern = prefill_gemm_kernel<TYPE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmX, tmW, a.Y, static_cast<int>(a.out_f),
-                                                      static_cast<int>(a.T), static_cast<int>(a.in_f / SB),
-                                                      m_tiles, num_tiles, a.err, a.wait_limit_ns, a.inject_stall);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(gp, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_gemm(const GemmArgs &a, void *encode_fn, cudaStream_t stream) {
+cudaError_t launch_prefill_gemm(const GemmArgs *a, int n, void *encode_fn, cudaStream_t stream) {
     const EncodeFn enc = reinterpret_cast<EncodeFn>(encode_fn);
-    switch (a.type) {
-    case 0: return launch_typed<0>(a, enc, stream);
-    case kQ4_K: return launch_typed<kQ4_K>(a, enc, stream);
-    case kQ2_K: return launch_typed<kQ2_K>(a, enc, stream);
-    case kQ6_K: return launch_typed<kQ6_K>(a, enc, stream);
-    case kQ8_0: return launch_typed<kQ8_0>(a, enc, stream);
+    if (n < 1) return cudaErrorInvalidValue;
+    for (int i = 1; i < n; ++i)
+        if (a[i].type != a[0].type) return cudaErrorInvalidValue;
+    switch (a[0].type) {
+    case 0: return launch_typed<0>(a, n, enc, stream);
+    case kQ4_K: return launch_typed<kQ4_K>(a, n, enc, stream);
+    case kQ2_K: return launch_typed<kQ2_K>(a, n, enc, stream);
+    case kQ6_K: return launch_typed<kQ6_K>(a, n, enc, stream);
+    case kQ8_0: return launch_typed<kQ8_0>(a, n, enc, stream);
     default: return cudaErrorInvalidValue;
     }
 }

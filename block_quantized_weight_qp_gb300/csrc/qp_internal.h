@@ -37,7 +37,11 @@ struct GemmArgs {
     int inject_stall;      // test hook: >= 0 makes the producer drop that load
 };
 
-// Builds the tensor maps and launches; `encode` is cuTensorMapEncodeTiled.
-cudaError_t launch_prefill_gemm(const GemmArgs &a, void *encode_fn, cudaStream_t stream);
+// Most projections one launch takes (qp_prefill_gemm_group).
+constexpr int kMaxGroup = 8;
+
+// Builds the tensor maps and launches one persistent kernel over n (1..8)
+// projections of one type and one T; `encode` is cuTensorMapEncodeTiled.
+cudaError_t launch_prefill_gemm(const GemmArgs *a, int n, void *encode_fn, cudaStream_t stream);
 
 }  // namespace qp

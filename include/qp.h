@@ -136,6 +136,45 @@ qp_status qp_prefill_gemm_f16w(const uint16_t *W16, int64_t out_f, int64_t in_f,
                                const uint16_t *X, int64_t T, float *Y, void *stream);
 
 /*
+ * One projection of a grouped call: Y[T x out_f] = X[T x in_f] * W^T, with
+ * the same meaning, layouts and requirements as the arguments of
+ * qp_prefill_gemm (W block-quantized) or qp_prefill_gemm_f16w (W a dense
+ * fp16 [out_f x in_f] weight).  Caller-owned device memory.
+ */
+typedef struct {
+    const void *W;
+    int64_t out_f, in_f;
+    const uint16_t *X;
+    float *Y;
+} qp_gemm_desc;
+
+#define QP_MAX_GROUP 8
+
+/*
+ * Several projections over the same prompt chunk in one launch
+ * (PR #4624 §What changes: the batched prefill runs one GEMM per projection
+ * over the chunk; a layer's projections are independent GEMMs): the n
+ * (1..QP_MAX_GROUP) descriptors share `type` and T and are computed by one
+ * persistent kernel whose CTAs deal out the tiles of all of them, so small
+ * projections do not each leave SMs idle.  type = QP_Q8_0 ... QP_Q6_K runs
+ * the fused mode on block-quantized W; type = 0 runs the cached mode on fp16
+ * W.  Each Y is bitwise what the single-projection call gives.  Descriptors
+ * are validated as those calls validate their arguments (the first failure
+ * is returned and nothing is launched); outputs must not overlap inputs or
+ * each other.  Asynchronous on `stream`.
+ */
+qp_status qp_prefill_gemm_group(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream);
+
+/*
+ * qp_prefill_gemm_group over consecutive row chunks of every X and Y,
+ * [c, min(c + chunk, T)) for c = 0, chunk, 2*chunk, ... (PR #4624 §What
+ * changes: the batched prefill is chunked to bound memory): one launch per
+ * chunk.  Bitwise equal to one unchunked call.  chunk >= 1.
+ */
+qp_status qp_prefill_chunked_group(int type, const qp_gemm_desc *descs, int n, int64_t T, int64_t chunk,
+                                   void *stream);
+
+/*
  * Chunked prefill (PR #4624 §What changes: the batched prefill is chunked to
  * bound memory): runs the projection on consecutive row chunks of X and Y,
  * [c, min(c + chunk, T)) for c = 0, chunk, 2*chunk, ...; a short last chunk

@@ -89,6 +89,38 @@ def test_host_side_argument_checks(call, status):
     assert call(qp.load()) == status
 
 
+def descs(*shapes, W=FAKE, X=FAKE, Y=FAKE):
+    arr = (qp.QPGemmDesc * max(len(shapes), 1))()
+    for k, (out_f, in_f) in enumerate(shapes):
+        arr[k] = qp.QPGemmDesc(W, out_f, in_f, X, Y)
+    return arr
+
+
+@pytest.mark.parametrize("call,status", [
+    (lambda l: l.qp_prefill_gemm_group(qp.Q4_K, None, 1, 16, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256)), 0, 16, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q4_K, descs(*[(256, 256)] * 9), 9, 16, None),
+     qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_gemm_group(3, descs((256, 256)), 1, 16, None), qp.QP_ERR_UNSUPPORTED_TYPE),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256)), 1, 0, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256), (256, 1000)), 2, 16, None),
+     qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q2_K, descs((256, 1024), (256, 512)), 2, 16, None),
+     qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_prefill_gemm_group(0, descs((256, 256), (256, 100)), 2, 16, None),
+     qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q8_0, descs((256, 256), W=None), 1, 16, None),
+     qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_gemm_group(qp.Q8_0, descs((256, 256), (128, 256), Y=FAKE + 4), 2, 16, None),
+     qp.QP_ERR_MISALIGNED),
+    (lambda l: l.qp_prefill_chunked_group(qp.Q4_K, descs((256, 256)), 1, 16, 0, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_chunked_group(qp.Q4_K, descs((256, 256)), 0, 16, 8, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_prefill_chunked_group(0, descs((256, 300)), 1, 16, 8, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+])
+def test_grouped_call_argument_checks(call, status):
+    assert call(qp.load()) == status
+
+
 def test_no_device_is_an_error_not_a_fallback():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -96,3 +128,4 @@ def test_no_device_is_an_error_not_a_fallback():
     lib = qp.load()
     assert lib.qp_dequant_f32(qp.Q4_K, FAKE, 4, 256, FAKE, None) == qp.QP_ERR_NO_DEVICE
     assert lib.qp_prefill_gemm(qp.Q4_K, FAKE, 256, 256, FAKE, 16, FAKE, None) == qp.QP_ERR_NO_DEVICE
+    assert lib.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256), (512, 512)), 2, 16, None) == qp.QP_ERR_NO_DEVICE

@@ -136,6 +136,68 @@ def test_chunked_equals_unchunked_bitwise(cuda_device, mode):
         assert torch().equal(Yc.view(torch().int32), Y.view(torch().int32)), chunk
 
 
+GROUP_SHAPES = [(384, 512), (132, 1024), (1028, 256), (4, 512), (256, 2048), (640, 4096), (132, 2048)]
+
+
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q6_K])
+def test_grouped_launch_equals_single_calls_bitwise(cuda_device, qtype):
+    """One persistent launch over several projections (different out_f and
+    in_f, each with its own X) gives each Y bitwise as its own call does."""
+    t = torch()
+    T = 300
+    shapes = [(o, i) for o, i in GROUP_SHAPES if qp.qp_row_bytes(qtype, i) % 16 == 0]
+    ws = [dev(synth.blocks(qtype, o, i, seed=8, tensor=k)) for k, (o, i) in enumerate(shapes)]
+    Xs = [dev(synth.normal_f16((T, i), seed=8, tensor=50 + k)) for k, (o, i) in enumerate(shapes)]
+    Ys = [t.full((T, o), float("nan"), dtype=t.float32, device="cuda") for o, i in shapes]
+    qp.qp_prefill_gemm_group(qtype, [(w, o, i, X, Y) for w, (o, i), X, Y in zip(ws, shapes, Xs, Ys)], T)
+    qp.qp_check()
+    assert len(shapes) >= 3
+    for w, (o, i), X, Y in zip(ws, shapes, Xs, Ys):
+        Y1 = run_gemm(qtype, w, o, i, X, T)
+        assert t.equal(Y.view(t.int32), Y1.view(t.int32)), (o, i)
+
+
+def test_grouped_launch_cached_mode_and_group_limit(cuda_device):
+    """type 0 runs the cached mode; eight projections (the limit) in one launch."""
+    t = torch()
+    qtype, T = qp.Q4_K, 513
+    shapes = [(256, 256), (128, 512), (512, 256), (4, 1024), (132, 256), (256, 768), (640, 256), (128, 256)]
+    ws = [dev(synth.blocks(qtype, o, i, seed=9, tensor=k)) for k, (o, i) in enumerate(shapes)]
+    W16s = [dequant16_dev(qtype, w, o, i) for w, (o, i) in zip(ws, shapes)]
+    Xs = [dev(synth.normal_f16((T, i), seed=9, tensor=60 + k)) for k, (o, i) in enumerate(shapes)]
+    Yf = [t.empty((T, o), dtype=t.float32, device="cuda") for o, i in shapes]
+    Yc = [t.empty((T, o), dtype=t.float32, device="cuda") for o, i in shapes]
+    qp.qp_prefill_gemm_group(qtype, [(w, o, i, X, Y) for w, (o, i), X, Y in zip(ws, shapes, Xs, Yf)], T)
+    qp.qp_prefill_gemm_group(0, [(w, o, i, X, Y) for w, (o, i), X, Y in zip(W16s, shapes, Xs, Yc)], T)
+    qp.qp_check()
+    for w, W16, (o, i), X, A, B in zip(ws, W16s, shapes, Xs, Yf, Yc):
+        Y1 = run_gemm(qtype, None, o, i, X, T, mode="cached", W16=W16)
+        assert t.equal(B.view(t.int32), Y1.view(t.int32)), (o, i)
+        assert t.equal(A.view(t.int32), B.view(t.int32)), (o, i)   # fused == cached
+    with pytest.raises(qp.QPError):
+        qp.qp_prefill_gemm_group(qtype, [(ws[0], 256, 256, Xs[0], Yf[0])] * 9, T)
+
+
+@pytest.mark.parametrize("mode", ["fused", "cached"])
+def test_chunked_group_equals_unchunked_group_bitwise(cuda_device, mode):
+    t = torch()
+    qtype, T = qp.Q2_K, 777
+    shapes = [(256, 1024), (132, 2048), (512, 1024)]
+    ws = [dev(synth.blocks(qtype, o, i, seed=10, tensor=k)) for k, (o, i) in enumerate(shapes)]
+    if mode == "cached":
+        ws = [dequant16_dev(qtype, w, o, i) for w, (o, i) in zip(ws, shapes)]
+    ty = qtype if mode == "fused" else 0
+    Xs = [dev(synth.normal_f16((T, i), seed=10, tensor=70 + k)) for k, (o, i) in enumerate(shapes)]
+    Y = [t.empty((T, o), dtype=t.float32, device="cuda") for o, i in shapes]
+    qp.qp_prefill_gemm_group(ty, [(w, o, i, X, y) for w, (o, i), X, y in zip(ws, shapes, Xs, Y)], T)
+    for chunk in (777, 256, 300, 1000):
+        Yc = [t.full((T, o), float("nan"), dtype=t.float32, device="cuda") for o, i in shapes]
+        qp.qp_prefill_chunked_group(ty, [(w, o, i, X, y) for w, (o, i), X, y in zip(ws, shapes, Xs, Yc)], T, chunk)
+        qp.qp_check()
+        for a, b in zip(Y, Yc):
+            assert t.equal(a.view(t.int32), b.view(t.int32)), chunk
+
+
 def test_deterministic_and_no_stray_writes(cuda_device):
     t = torch()
     qtype, out_f, in_f, T = qp.Q6_K, 260, 2048, 333
