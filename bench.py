@@ -44,9 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the dominant kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum), from one ncu capture of the kernel source whose hash
 # is recorded; reported only while the source is unchanged.
-NCU_TRAFFIC = {"source_sha": "ee13f2249b402636", "bytes_per_launch": 426917888,
-               "what": "fused Q2_K gate projection 12288x4096, T=8192 (read 83.97 MB + write 342.94 MB); "
-                       "algorithmic 486.3 MB (W 16.5 + X 67.1 + Y 402.7), part of Y still in L2 at kernel end"}
+NCU_TRAFFIC = {"source_sha": "61eb994060f2ab3c", "bytes_per_launch": 1493623232,
+               "what": "fused Q2_K launch over q,k,v,o,gate,up, T=8192 (read 410.43 MB + write 1083.19 MB); "
+                       "algorithmic 1321.9 MB (W 46.8 + X 134.2 + Y 1140.9): X_h is read again by each "
+                       "projection that shares it, and part of Y is still in L2 at kernel end"}
 KERNEL_SOURCES = ["block_quantized_weight_qp_gb300/csrc/qgemm.cu",
                   "block_quantized_weight_qp_gb300/csrc/qp_ptx.cuh"]
 
