@@ -23,9 +23,10 @@ _SRC = [os.path.join(_HERE, "qpo.c")]
 _HDR = [os.path.join(_HERE, "qpo.h")]
 _SO = os.path.join(_HERE, "_build", "libqpo.so")
 
-Q8_0, Q2_K, Q4_K, Q6_K = 8, 10, 12, 14
+F16, Q8_0, Q2_K, Q4_K, Q5_K, Q6_K = 1, 8, 10, 12, 13, 14
 # values per block, bytes per block
-BLOCK = {Q8_0: (32, 34), Q2_K: (256, 84), Q4_K: (256, 144), Q6_K: (256, 210)}
+BLOCK = {F16: (1, 2), Q8_0: (32, 34), Q2_K: (256, 84), Q4_K: (256, 144), Q5_K: (256, 176),
+         Q6_K: (256, 210)}
 
 _lib = None
 

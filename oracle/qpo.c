@@ -19,6 +19,13 @@
  *         high nibble = m;                                   value = d*sc*q - dmin*m
  *   Q6_K 256 values, 210 B: ql:u8[128] | qh:u8[64] | scales:i8[16] | d:f16
  *         sixteen sub-blocks of 16 values;                   value = d*s*(q-32)
+ *   Q5_K 256 values, 176 B: d:f16 | dmin:f16 | scales:u8[12] | qh:u8[32] |
+ *         qs:u8[128]; sub-blocks, scales and mins as in Q4_K; each q has a
+ *         fifth (high) bit held in the qh plane;             value = d*sc*q - dmin*m
+ *   F16     1 value,   2 B: the fp16 weight itself;          value = that fp16
+ * (Q5_K and F16 are in the page's list of types the f32 dequant has device
+ * kernels for, "Qwen3.5 batched prefill has no f32 dequant for IQ2_XXS,
+ * IQ3_S, IQ3_XXS, Q2_K", section Cause.)
  */
 #include "qpo.h"
 
@@ -37,6 +44,8 @@ int qpo_block_info(int type, int64_t *qk, int64_t *block_bytes) {
     case QPO_Q4_K: *qk = 256; *block_bytes = 144; return 0;
     case QPO_Q2_K: *qk = 256; *block_bytes = 84;  return 0;
     case QPO_Q6_K: *qk = 256; *block_bytes = 210; return 0;
+    case QPO_Q5_K: *qk = 256; *block_bytes = 176; return 0;
+    case QPO_F16:  *qk = 1;   *block_bytes = 2;   return 0;
     default: return -1;
     }
 }
@@ -198,12 +207,42 @@ static float decode_q6_k(const uint8_t *b, int v) {
     return dl * (float)(q - 32);
 }
 
+/* Q5_K: value v lies in sub-block s = v/32 and 64-value group g = v/64; the
+ * low four bits of its 5-bit q are the Q4_K nibble (low nibble of
+ * qs[32g + v%32] for the first 32 values of the group, high nibble for the
+ * last 32) and its fifth bit is bit s of qh[v%32]. */
+static float decode_q5_k(const uint8_t *b, int v) {
+    const float d = qpo_f16_to_f32(rd16(b + 0));
+    const float dmin = qpo_f16_to_f32(rd16(b + 2));
+    const uint8_t *scales = b + 4;
+    const uint8_t *qh = b + 16;
+    const uint8_t *qs = b + 48;
+    const int s = v / 32, g = v / 64, l = v % 32;
+    int sc, m;
+    q4_k_scale_min(scales, s, &sc, &m);
+    const uint8_t byte = qs[32 * g + l];
+    const int lo = (v % 64 < 32) ? (byte & 0x0f) : (byte >> 4);
+    const int q = lo | (((qh[l] >> s) & 1) << 4);
+    const float dl = d * (float)sc;
+    const float ml = dmin * (float)m;
+    const float dq = dl * (float)q;
+    return dq - ml;
+}
+
+/* F16: the block is one fp16 weight; its value is that number. */
+static float decode_f16(const uint8_t *b, int v) {
+    (void)v;
+    return qpo_f16_to_f32(rd16(b));
+}
+
 float qpo_decode_value(int type, const uint8_t *block, int v) {
     switch (type) {
     case QPO_Q8_0: return decode_q8_0(block, v);
     case QPO_Q4_K: return decode_q4_k(block, v);
     case QPO_Q2_K: return decode_q2_k(block, v);
     case QPO_Q6_K: return decode_q6_k(block, v);
+    case QPO_Q5_K: return decode_q5_k(block, v);
+    case QPO_F16: return decode_f16(block, v);
     default: return NAN;
     }
 }

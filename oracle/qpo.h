@@ -43,10 +43,10 @@ extern "C" {
 #endif
 
 /* GGUF type ids. */
-enum { QPO_Q8_0 = 8, QPO_Q2_K = 10, QPO_Q4_K = 12, QPO_Q6_K = 14 };
+enum { QPO_F16 = 1, QPO_Q8_0 = 8, QPO_Q2_K = 10, QPO_Q4_K = 12, QPO_Q5_K = 13, QPO_Q6_K = 14 };
 
 /* Values per block and bytes per block; returns 0 on success, -1 if the type
- * is not one of the four. */
+ * is not one of the six. */
 int qpo_block_info(int type, int64_t *qk, int64_t *block_bytes);
 
 /* Exact binary16 -> binary32. */

@@ -20,6 +20,9 @@
  *         [0, 15], 2-bit q on [0, 3]); d, dmin.
  *   Q6_K: 128 ql and 64 qh bytes uniform (6-bit q uniform on [0, 63]);
  *         16 int8 scales uniform on [-127, 127]; d.
+ *   Q5_K: d, dmin; 12 scale bytes, 32 qh bytes and 128 qs bytes uniform
+ *         (6-bit scale/min uniform on [0, 63], 5-bit q on [0, 31]).
+ *   F16:  one weight per block, standard normal snapped to fp16.
  *   X:    standard normal (Box-Muller), snapped to fp16.
  */
 #include <math.h>
@@ -102,6 +105,16 @@ void synth_blocks(int type, uint64_t key, int64_t nblocks, uint8_t *out) {
             fill_bytes(key, i0 + 2, p, 80);
             put16(p + 80, scale_sample(draw(key, i0)));
             put16(p + 82, scale_sample(draw(key, i0 + 1)));
+        } else if (type == 13) {                 /* Q5_K, 176 B */
+            uint8_t *p = out + b * 176;
+            put16(p + 0, scale_sample(draw(key, i0)));
+            put16(p + 2, scale_sample(draw(key, i0 + 1)));
+            fill_bytes(key, i0 + 2, p + 4, 172);
+        } else if (type == 1) {                  /* F16, 2 B */
+            const uint64_t z = draw(key, i0);
+            const double u1 = ((double)(z >> 32) + 1.0) * (1.0 / 4294967296.0);
+            const double u2 = (double)(z & 0xffffffffu) * (1.0 / 4294967296.0);
+            put16(out + b * 2, snap_f16(sqrt(-2.0 * log(u1)) * cos(6.283185307179586476925286766559 * u2)));
         } else if (type == 14) {                 /* Q6_K, 210 B */
             uint8_t *p = out + b * 210;
             fill_bytes(key, i0 + 2, p, 192);

@@ -6,7 +6,8 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-TYPES = {"Q8_0": (8, 32, 34), "Q2_K": (10, 256, 84), "Q4_K": (12, 256, 144), "Q6_K": (14, 256, 210)}
+TYPES = {"Q8_0": (8, 32, 34), "Q2_K": (10, 256, 84), "Q4_K": (12, 256, 144), "Q5_K": (13, 256, 176),
+         "Q6_K": (14, 256, 210)}
 
 
 def load(path):

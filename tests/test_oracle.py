@@ -20,8 +20,9 @@ import oracle
 import synth
 from golden_blocks import fixtures, load
 
-Q8_0, Q2_K, Q4_K, Q6_K = oracle.Q8_0, oracle.Q2_K, oracle.Q4_K, oracle.Q6_K
-ALL = [Q8_0, Q2_K, Q4_K, Q6_K]
+Q8_0, Q2_K, Q4_K, Q5_K, Q6_K = oracle.Q8_0, oracle.Q2_K, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K
+F16 = oracle.F16
+ALL = [Q8_0, Q2_K, Q4_K, Q5_K, Q6_K]
 
 
 def f16bits(x):
@@ -109,6 +110,20 @@ def pack_q4_k(d, dmin, sc, m, q):
     return b
 
 
+def pack_q5_k(d, dmin, sc, m, q):
+    """Q4_K's fields with 5-bit q: the low four bits where Q4_K keeps q, the
+    fifth bit of value v in bit v//32 of qh[v % 32] (qh sits before qs)."""
+    b4 = pack_q4_k(d, dmin, sc, m, np.asarray(q) & 15)
+    b = np.zeros(176, np.uint8)
+    b[0:16] = b4[0:16]
+    qh = np.zeros(32, np.int64)
+    for v in range(256):
+        qh[v % 32] |= (int(q[v]) >> 4) << (v // 32)
+    b[16:48] = qh
+    b[48:176] = b4[16:144]
+    return b
+
+
 def pack_q2_k(d, dmin, sc, m, q):
     b = np.zeros(84, np.uint8)
     b[0:16] = np.asarray(sc) | (np.asarray(m) << 4)
@@ -151,6 +166,8 @@ def rand_fields(rng, qtype):
         return d, None, None, None, rng.integers(-127, 128, 32)
     if qtype == Q4_K:
         return d, dmin, rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 16, 256)
+    if qtype == Q5_K:
+        return d, dmin, rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 32, 256)
     if qtype == Q2_K:
         return d, dmin, rng.integers(0, 16, 16), rng.integers(0, 16, 16), rng.integers(0, 4, 256)
     return d, None, rng.integers(-127, 128, 16), None, rng.integers(0, 64, 256)
@@ -160,7 +177,7 @@ def closed_form(qtype, d, dmin, sc, m, q):
     """Value formulas of the workload definition, in exact fp64."""
     if qtype == Q8_0:
         return [d * q[v] for v in range(32)]
-    if qtype == Q4_K:
+    if qtype in (Q4_K, Q5_K):
         return [d * sc[v // 32] * q[v] - dmin * m[v // 32] for v in range(256)]
     if qtype == Q2_K:
         return [d * sc[v // 16] * q[v] - dmin * m[v // 16] for v in range(256)]
@@ -172,6 +189,8 @@ def pack(qtype, d, dmin, sc, m, q):
         return pack_q8_0(d, q)
     if qtype == Q4_K:
         return pack_q4_k(d, dmin, sc, m, q)
+    if qtype == Q5_K:
+        return pack_q5_k(d, dmin, sc, m, q)
     if qtype == Q2_K:
         return pack_q2_k(d, dmin, sc, m, q)
     return pack_q6_k(d, sc, q)
@@ -229,6 +248,22 @@ def test_nibble_and_crumb_extraction_all_bytes():
             assert vals[v] == (byte >> (2 * ((v % 128) // 32))) & 3
 
 
+def test_q5_k_high_bit_extraction_all_bytes():
+    """Every qh byte value at every qh position: value v gets bit v//32 of
+    qh[v % 32] as its fifth bit (q = 16 * that bit with the nibbles zero)."""
+    b = pack_q5_k(1.0, 0.0, np.ones(8, int), np.zeros(8, int), np.zeros(256, int))
+    for byte in range(256):
+        b[16:48] = byte
+        vals = oracle.dequant_f32(Q5_K, b, 1, 256)[0]
+        for v in range(256):
+            assert vals[v] == 16 * ((byte >> (v // 32)) & 1)
+    for l in range(32):                      # one position at a time
+        b[16:48] = 0
+        b[16 + l] = 0xff
+        vals = oracle.dequant_f32(Q5_K, b, 1, 256)[0]
+        assert np.array_equal(np.nonzero(vals)[0], np.arange(l, 256, 32))
+
+
 def test_q6_k_all_low_high_combinations():
     d = 1.0
     for lo, hi in itertools.product(range(16), range(4)):
@@ -241,11 +276,11 @@ def test_q6_k_all_low_high_combinations():
 # ------------------------------------------------------------ bit flips ---
 # Reading-independent structure checks.
 
-QREGION = {Q8_0: (2, 34), Q4_K: (16, 144), Q2_K: (16, 80), Q6_K: (0, 192)}
-SREGION = {Q4_K: (4, 16), Q2_K: (0, 16), Q6_K: (192, 208)}
-DOFF = {Q8_0: 0, Q4_K: 0, Q2_K: 80, Q6_K: 208}
-QBITS = {Q8_0: 8, Q4_K: 4, Q2_K: 2, Q6_K: 6}
-SUB = {Q4_K: 32, Q2_K: 16, Q6_K: 16}
+QREGION = {Q8_0: (2, 34), Q4_K: (16, 144), Q5_K: (16, 176), Q2_K: (16, 80), Q6_K: (0, 192)}
+SREGION = {Q4_K: (4, 16), Q5_K: (4, 16), Q2_K: (0, 16), Q6_K: (192, 208)}
+DOFF = {Q8_0: 0, Q4_K: 0, Q5_K: 0, Q2_K: 80, Q6_K: 208}
+QBITS = {Q8_0: 8, Q4_K: 4, Q5_K: 5, Q2_K: 2, Q6_K: 6}
+SUB = {Q4_K: 32, Q5_K: 32, Q2_K: 16, Q6_K: 16}
 
 
 def base_block(qtype, q_ones):
@@ -254,8 +289,8 @@ def base_block(qtype, q_ones):
     bb = oracle.BLOCK[qtype][1]
     b = np.zeros(bb, np.uint8)
     b[DOFF[qtype]:DOFF[qtype] + 2] = np.array([2.0 ** -6], np.float16).view(np.uint8)
-    if qtype in (Q4_K, Q2_K):
-        off = 2 if qtype == Q4_K else 82
+    if qtype in (Q4_K, Q5_K, Q2_K):
+        off = 82 if qtype == Q2_K else 2
         b[off:off + 2] = np.array([2.0 ** -7], np.float16).view(np.uint8)
     lo, hi = QREGION[qtype]
     if q_ones:
@@ -294,7 +329,7 @@ def test_every_quant_bit_moves_exactly_one_value(qtype):
             assert weights == [2 ** k for k in range(QBITS[qtype])]
 
 
-@pytest.mark.parametrize("qtype", [Q4_K, Q2_K, Q6_K])
+@pytest.mark.parametrize("qtype", [Q4_K, Q5_K, Q2_K, Q6_K])
 def test_every_scale_bit_moves_one_aligned_subblock(qtype):
     qk = oracle.BLOCK[qtype][0]
     b0 = base_block(qtype, q_ones=True)
@@ -316,8 +351,9 @@ def test_every_scale_bit_moves_one_aligned_subblock(qtype):
             per_sub[s].append(delta[0])
     d, dmin = 2.0 ** -6, 2.0 ** -7
     for s, deltas in per_sub.items():
-        if qtype == Q4_K:      # 6-bit sc (step d*15*2^k) and 6-bit m (step -dmin*2^k)
-            sc_w = sorted(round(x / (d * 15)) for x in deltas if x > 0)
+        if qtype in (Q4_K, Q5_K):   # 6-bit sc (step d*qmax*2^k) and 6-bit m (step -dmin*2^k)
+            qmax = 15 if qtype == Q4_K else 31
+            sc_w = sorted(round(x / (d * qmax)) for x in deltas if x > 0)
             m_w = sorted(round(-x / dmin) for x in deltas if x < 0)
             assert sc_w == [1, 2, 4, 8, 16, 32] and m_w == [1, 2, 4, 8, 16, 32], (s, deltas)
         elif qtype == Q2_K:    # 4-bit sc (d*3*2^k) and 4-bit m (-dmin*2^k)
@@ -336,8 +372,8 @@ def requant_search(qtype, d, dmin, y):
     reproduce y exactly (f32 arithmetic, each operation rounded)."""
     f = np.float32
     d, dmin = f(d), f(dmin)
-    if qtype == Q4_K:
-        nsub, sub, scr, qr = 8, 32, 64, 16
+    if qtype in (Q4_K, Q5_K):
+        nsub, sub, scr, qr = 8, 32, 64, 16 if qtype == Q4_K else 32
     else:
         nsub, sub, scr, qr = 16, 16, 16, 4
     sc_out, m_out, q_out = [], [], np.zeros(256, np.int64)
@@ -362,15 +398,15 @@ def requant_search(qtype, d, dmin, y):
     return sc_out, m_out, q_out
 
 
-@pytest.mark.parametrize("qtype", [Q4_K, Q2_K])
+@pytest.mark.parametrize("qtype", [Q4_K, Q5_K, Q2_K])
 def test_requant_round_trip(qtype):
     w = synth.blocks(qtype, 1, 256, seed=11, tensor=qtype)
     y = oracle.dequant_f32(qtype, w, 1, 256)[0]
-    dof = 0 if qtype == Q4_K else 80
+    dof = 80 if qtype == Q2_K else 0
     d = float(w[0, dof:dof + 2].view(np.float16)[0])
     dmin = float(w[0, dof + 2:dof + 4].view(np.float16)[0])
     sc, m, q = requant_search(qtype, d, dmin, y)
-    packer = pack_q4_k if qtype == Q4_K else pack_q2_k
+    packer = {Q4_K: pack_q4_k, Q5_K: pack_q5_k, Q2_K: pack_q2_k}[qtype]
     b2 = packer(d, dmin, np.array(sc), np.array(m), q)
     y2 = oracle.dequant_f32(qtype, b2, 1, 256)[0]
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
@@ -440,8 +476,23 @@ def test_nan_and_inf_scales_propagate():
 
 def test_bad_type_rejected():
     with pytest.raises(KeyError):
-        oracle.dequant_f32(13, np.zeros(16, np.uint8), 1, 16)
-    assert oracle.lib().qpo_dequant_f32(13, None, 1, 1, None) == -1
+        oracle.dequant_f32(11, np.zeros(16, np.uint8), 1, 16)
+    assert oracle.lib().qpo_dequant_f32(11, None, 1, 1, None) == -1
+
+
+def test_f16_weights_decode_to_their_value_for_every_bit_pattern():
+    """F16 "blocks" are single fp16 weights: the f32 dequant is the exact
+    widening (numpy's IEEE conversion), the f16 dequant gives the same bits
+    back (NaNs stay NaN)."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    y = oracle.dequant_f32(F16, h.view(np.uint8), 1, 65536)[0]
+    want = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(y), nan)
+    assert np.array_equal(y[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    y16 = oracle.dequant_f16(F16, h.view(np.uint8), 1, 65536)[0]
+    assert np.array_equal(y16[~nan], h[~nan])
+    assert np.all(np.isnan(y16[nan].view(np.float16)))
 
 
 # ----------------------------------------------------------------- GEMM ---

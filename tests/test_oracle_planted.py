@@ -2,7 +2,8 @@
 
 The six fault classes are the ones "Qwen3.5 batched prefill has no f32
 dequant for IQ2_XXS, IQ3_S, IQ3_XXS, Q2_K" (§Acceptance) plants in its
-kernels: signs, high bits, scale selector, d, row stride and tail guard.
+kernels: signs, high bits, scale selector, d, row stride and tail guard;
+a seventh plants a Q5_K high-bit-plane index slip.
 Each is planted in a copy of the oracle source on the CPU, compiled, and the
 pin tests are run against that copy (QPO_LIB); they must fail.  The restored
 oracle passing is the rest of the suite.
@@ -27,6 +28,9 @@ PLANTS = {
                    "const int64_t nb = cols / qk;\n    const uint8_t *base = (const uint8_t *)blocks;\n#pragma omp parallel for schedule(static)\n    for (int64_t r = 0; r < rows; ++r) {\n        for (int64_t c = 0; c < cols; ++c) {\n            const uint8_t *blk = base + (r * nb + c / qk) * bb;\n            out[r * cols + c] = qpo_decode_value"),
     # writes the padding values of a partial last block (into the next row,
     # and for the last row into the wrapper's NaN guard band)
+    # the fifth bit of a Q5_K value taken from the neighbouring sub-block's bit
+    "q5_k_high_bit": ("const int q = lo | (((qh[l] >> s) & 1) << 4);",
+                      "const int q = lo | (((qh[l] >> (s ^ 1)) & 1) << 4);"),
     "tail_guard": ("for (int64_t c = 0; c < cols; ++c) {\n            const uint8_t *blk = base + (r * nb + c / qk) * bb;\n            out[r * cols + c] = qpo_decode_value(type, blk, (int)(c % qk));",
                    "for (int64_t c = 0; c < nb * qk; ++c) {\n            const uint8_t *blk = base + (r * nb + c / qk) * bb;\n            out[r * cols + c] = qpo_decode_value(type, blk, (int)(c % qk));"),
 }
