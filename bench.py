@@ -269,7 +269,8 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
     import torch
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     cases = [("Q4_K", qp.Q4_K, 4096, 4096, 12), ("Q8_0", qp.Q8_0, 4096, 4096, 13),
-             ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15)]
+             ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15),
+             ("Q5_K", qp.Q5_K, 4096, 4096, 16), ("F16", qp.F16, 4096, 4096, 17)]
     out = {}
     for name, qt, rows, cols, tid in cases:
         if only and not any(o.startswith(name) for o in only):
@@ -525,6 +526,11 @@ def main_qp(args):
             rows["qwen3_1p7b_q4k_t2048"] = {"ms": round(ms17, 4), "tflops": round(l17.flops() / ms17 / 1e9, 1),
                                             "tok_per_s": round(l17.T / ms17 * 1e3, 1)}
             del l17
+            l5k = Layer(workloads.WORKLOADS["qwen3_8b_q5k_t8192"], rank, device)
+            ms5k = time_layer(qp, l5k, stream, max(5, args.steps // 2), 3)
+            rows["qwen3_8b_q5k_t8192"] = {"ms": round(ms5k, 4), "tflops": round(l5k.flops() / ms5k / 1e9, 1),
+                                          "tok_per_s": round(l5k.T / ms5k * 1e3, 1)}
+            del l5k
             wl5 = workloads.WORKLOADS["qwen3_8b_q4k_t31258_chunk4864"]
             l5 = Layer(wl5, rank, device, need_f16=True)
             ms_f = time_layer(qp, l5, stream, 3, 1, mode="fused", chunk=wl5["chunk"])

@@ -13,8 +13,8 @@ import os
 
 from . import _build
 
-Q8_0, Q2_K, Q4_K, Q6_K = 8, 10, 12, 14
-TYPES = {"Q8_0": Q8_0, "Q2_K": Q2_K, "Q4_K": Q4_K, "Q6_K": Q6_K}
+F16, Q8_0, Q2_K, Q4_K, Q5_K, Q6_K = 1, 8, 10, 12, 13, 14
+TYPES = {"F16": F16, "Q8_0": Q8_0, "Q2_K": Q2_K, "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K}
 
 QP_OK = 0
 QP_ERR_INVALID_PARAMETER = 1

@@ -34,7 +34,10 @@ void *g_encode = nullptr;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{-1};
 
-bool valid_type(int t) { return t == qp::kQ8_0 || t == qp::kQ2_K || t == qp::kQ4_K || t == qp::kQ6_K; }
+bool valid_type(int t) {
+    return t == qp::kF16 || t == qp::kQ8_0 || t == qp::kQ2_K || t == qp::kQ4_K || t == qp::kQ5_K ||
+           t == qp::kQ6_K;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -82,13 +85,15 @@ qp_status device_info(DeviceInfo **out) {
     return QP_OK;
 }
 
-int64_t qk_of(int t) { return t == qp::kQ8_0 ? 32 : 256; }
+int64_t qk_of(int t) { return t == qp::kF16 ? 1 : (t == qp::kQ8_0 ? 32 : 256); }
 int64_t bytes_of(int t) {
     switch (t) {
     case qp::kQ8_0: return 34;
     case qp::kQ2_K: return 84;
     case qp::kQ4_K: return 144;
+    case qp::kQ5_K: return 176;
     case qp::kQ6_K: return 210;
+    case qp::kF16: return 2;
     default: return -1;
     }
 }
@@ -112,7 +117,7 @@ qp_status run_gemms(int type, const qp_gemm_desc *descs, int n, int64_t T, void 
     qp::GemmArgs a[qp::kMaxGroup];
     const int inject = g_inject_stall.exchange(-1);
     for (int i = 0; i < n; ++i) {
-        a[i].type = type;
+        a[i].type = type == qp::kF16 ? 0 : type;   // F16 weights are the cached mode's dense fp16 W
         a[i].out_f = descs[i].out_f;
         a[i].in_f = descs[i].in_f;
         a[i].T = T;

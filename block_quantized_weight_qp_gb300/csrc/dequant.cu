@@ -87,6 +87,36 @@ struct RawQ4K {
     }
 };
 
+// Q5_K: Q4_K's fields and nibble order, plus a 32-byte plane qh before qs
+// holding each value's fifth bit: run t (sub-block t) takes bit t of
+// qh[0..31].  q <= 31 still fits the exact byte-to-float step.
+struct RawQ5K {
+    uint4 hd, h0, h1, q0, q1;
+    __device__ __forceinline__ void load(const uint8_t *b, int t) {
+        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
+        h0 = __ldg(reinterpret_cast<const uint4 *>(b + 16));
+        h1 = __ldg(reinterpret_cast<const uint4 *>(b + 32));
+        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 48 + 32 * (t >> 1)));
+        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 64 + 32 * (t >> 1)));
+    }
+    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
+        const int sh = 8 * (t & 3);
+        const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
+        const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
+        const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
+        const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
+        const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
+        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
+        const int nsh = 4 * (t & 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            affine4(((w[k] >> nsh) & 0x0F0F0F0Fu) | (((h[k] >> t) & 0x01010101u) << 4), dl2, nml2, y[2 * k],
+                    y[2 * k + 1]);
+    }
+};
+
 // Q2_K: value 128n + 32j + l takes bits 2j..2j+1 of qs[32n + l]; run t has
 // n = t/4, j = t%4, sub-blocks 2t (l < 16) and 2t+1, scale bytes scales[2t],
 // scales[2t+1] (sc low nibble, m high nibble).
@@ -169,6 +199,7 @@ struct RawQ80 {
 
 template <int TYPE> struct RawOf;
 template <> struct RawOf<kQ4_K> { using T = RawQ4K; };
+template <> struct RawOf<kQ5_K> { using T = RawQ5K; };
 template <> struct RawOf<kQ2_K> { using T = RawQ2K; };
 template <> struct RawOf<kQ6_K> { using T = RawQ6K; };
 template <> struct RawOf<kQ8_0> { using T = RawQ80; };
@@ -236,7 +267,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
     using S = Stage<OutT>;
     using Raw = typename RawOf<TYPE>::T;
     constexpr int QK = TYPE == kQ8_0 ? 32 : 256;
-    constexpr int BB = TYPE == kQ8_0 ? 34 : (TYPE == kQ4_K ? 144 : (TYPE == kQ2_K ? 84 : 210));
+    constexpr int BB =
+        TYPE == kQ8_0 ? 34 : (TYPE == kQ4_K ? 144 : (TYPE == kQ5_K ? 176 : (TYPE == kQ2_K ? 84 : 210)));
     constexpr int BPW = blocks_per_warp<TYPE>();
     constexpr int RUNS_PER_BLOCK = 32 / BPW;                  // 8 (K-quants) or 1 (Q8_0)
     __shared__ __align__(16) uint8_t stage_all[WARPS * 32 * S::PITCH];
@@ -339,6 +371,48 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
     return cudaGetLastError();
 }
 
+// F16 weights: each "block" is one fp16 value and rows carry no padding, so
+// the input and the output hold the same n values in the same order: a flat
+// conversion (exact widening to f32) or copy (f16), 8 values = one 16-byte
+// load per thread and step; a last partial group of 8 is done value by value.
+template <typename OutT>
+__global__ void __launch_bounds__(256) f16_weights_kernel(const uint16_t *__restrict__ in, int64_t n,
+                                                          OutT *__restrict__ out) {
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(in) + i);
+        if constexpr (sizeof(OutT) == 4) {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                f[2 * k] = h2f(w[k]);
+                f[2 * k + 1] = h2f(w[k] >> 16);
+            }
+            float4 *o = reinterpret_cast<float4 *>(out) + 2 * i;
+            __stcs(o, make_float4(f[0], f[1], f[2], f[3]));
+            __stcs(o + 1, make_float4(f[4], f[5], f[6], f[7]));
+        } else {
+            __stcs(reinterpret_cast<uint4 *>(out) + i, v);
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < n - 8 * n8) {
+        const int64_t j = 8 * n8 + threadIdx.x;
+        if constexpr (sizeof(OutT) == 4) out[j] = h2f(in[j]);
+        else out[j] = in[j];
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_f16(const uint16_t *in, int64_t n, OutT *out, cudaStream_t stream, int num_sms) {
+    const int64_t want = (n / 8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+    f16_weights_kernel<OutT><<<grid, 256, 0, stream>>>(in, n, out);
+    return cudaGetLastError();
+}
+
 template <typename OutT>
 cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream,
                      int num_sms) {
@@ -346,7 +420,9 @@ cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, O
     case kQ8_0: return launch<kQ8_0>(blocks, rows, cols, out, stream, num_sms);
     case kQ2_K: return launch<kQ2_K>(blocks, rows, cols, out, stream, num_sms);
     case kQ4_K: return launch<kQ4_K>(blocks, rows, cols, out, stream, num_sms);
+    case kQ5_K: return launch<kQ5_K>(blocks, rows, cols, out, stream, num_sms);
     case kQ6_K: return launch<kQ6_K>(blocks, rows, cols, out, stream, num_sms);
+    case kF16: return launch_f16(static_cast<const uint16_t *>(blocks), rows * cols, out, stream, num_sms);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -64,6 +64,7 @@ constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 // into each smem row.
 template <int TYPE> struct QFmt;
 template <> struct QFmt<kQ4_K> { static constexpr int SB_BYTES = 144, BOX = 144; };
+template <> struct QFmt<kQ5_K> { static constexpr int SB_BYTES = 176, BOX = 176; };
 template <> struct QFmt<kQ2_K> { static constexpr int SB_BYTES = 84, BOX = 112; };
 template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 240; };
 template <> struct QFmt<kQ8_0> { static constexpr int SB_BYTES = 272, BOX = 272; };  // 8 blocks
@@ -74,7 +75,7 @@ template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };     
 // steps each) have rings of their own, so X can be prefetched deeper than
 // the decode runs ahead; the cached mode stages X and W together.
 // Shared memory: XST * 32 KiB + WST * 16 KiB + QST slices, <= 227 KiB.
-template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 4, QST = 1; };   // Q4_K, Q2_K
+template <int TYPE> struct Depth { static constexpr int XST = 4, WST = 4, QST = 1; };   // Q4_K, Q5_K, Q2_K
 template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 3, QST = 1; };
 template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3, QST = 2; };
 template <> struct Depth<0> { static constexpr int XST = 4, WST = 4, QST = 0; };
@@ -256,6 +257,31 @@ struct ChunkAddr {
 // start is 2 bytes past a word (Q6_K), else 0.
 template <int TYPE, int WO> struct Dec;
 
+// Q4_K / Q5_K scales: the 6-bit (sc, m) pairs of sub-blocks 2a + h (a =
+// 0..3) from d, dmin and the 12 packed scale bytes (hd = the block's first
+// 16 bytes), as dl = d*sc and -ml = -(dmin*m) pairs.
+__device__ __forceinline__ void k4_scales(const uint4 &hd, int h, pair_t (&dl2)[4], pair_t (&nml2)[4]) {
+    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        uint32_t sc, m;
+        if (a < 2) {                                 // s = 2a + h < 4: bytes s, s + 4
+            const int sh = 8 * (2 * a + h);
+            sc = (hd.y >> sh) & 63u;
+            m = (hd.z >> sh) & 63u;
+        } else {                                     // s >= 4, t = s - 4: bytes t + 8, t, t + 4
+            const int sh = 8 * (2 * (a - 2) + h);
+            const uint32_t lo = hd.w >> sh;
+            sc = (lo & 15u) | (((hd.y >> sh) >> 6 & 3u) << 4);
+            m = ((lo >> 4) & 15u) | (((hd.z >> sh) >> 6 & 3u) << 4);
+        }
+        const float dl = __fmul_rn(d, static_cast<float>(sc));
+        const float nml = -__fmul_rn(dmin, static_cast<float>(m));
+        dl2[a] = pk2(dl, dl);
+        nml2[a] = pk2(nml, nml);
+    }
+}
+
 // Q4_K: sub-block 2A+h holds values 64A+32h..; they are the low (h=0) or
 // high (h=1) nibbles of qs[32A .. 32A+31].  The thread keeps its nibbles of
 // the whole slice (32 words, one per 4 values) in registers.
@@ -268,26 +294,35 @@ template <int WO> struct Dec<kQ4_K, WO> {
         row_words<16, 32, false>(row, 0, w);       // qs[0 .. 127]
 #pragma unroll
         for (int k = 0; k < 32; ++k) qn[k] = (w[k] >> (4 * h)) & 0x0F0F0F0Fu;
-        const uint4 hd = *reinterpret_cast<const uint4 *>(row);   // d, dmin, scales[0..11]
-        const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+        k4_scales(*reinterpret_cast<const uint4 *>(row), h, dl2, nml2);
+    }
+    template <int A>
+    __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int, uint32_t tile,
+                                         const ChunkAddr &ca) const {
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            uint32_t sc, m;
-            if (a < 2) {                                 // s = 2a + h < 4: bytes s, s + 4
-                const int sh = 8 * (2 * a + h);
-                sc = (hd.y >> sh) & 63u;
-                m = (hd.z >> sh) & 63u;
-            } else {                                     // s >= 4, t = s - 4: bytes t + 8, t, t + 4
-                const int sh = 8 * (2 * (a - 2) + h);
-                const uint32_t lo = hd.w >> sh;
-                sc = (lo & 15u) | (((hd.y >> sh) >> 6 & 3u) << 4);
-                m = ((lo >> 4) & 15u) | (((hd.z >> sh) >> 6 & 3u) << 4);
-            }
-            const float dl = __fmul_rn(d, static_cast<float>(sc));
-            const float nml = -__fmul_rn(dmin, static_cast<float>(m));
-            dl2[a] = pk2(dl, dl);
-            nml2[a] = pk2(nml, nml);
+        for (int c = 0; c < 4; ++c) {
+            const uint2 lo = word_affine(qn[8 * A + 2 * c], dl2[A], nml2[A]);
+            const uint2 hi = word_affine(qn[8 * A + 2 * c + 1], dl2[A], nml2[A]);
+            sts128(tile + ca.off[c], lo.x, lo.y, hi.x, hi.y);
         }
+    }
+};
+
+// Q5_K: Q4_K's sub-blocks, scales and nibbles (qs now at byte 48), plus the
+// fifth bit of value 64A + 32h + l in bit 2A + h of qh[l] (bytes 16..47),
+// merged into the nibble words once per slice; q <= 31.
+template <int WO> struct Dec<kQ5_K, WO> {
+    static constexpr bool REGS = true;
+    pair_t dl2[4], nml2[4];
+    uint32_t qn[32];
+    __device__ __forceinline__ void slice(const uint8_t *row, uint32_t, int h) {
+        uint32_t qh[8], w[32];
+        row_words<16, 8, false>(row, 0, qh);       // qh[0 .. 31]
+        row_words<48, 32, false>(row, 0, w);       // qs[0 .. 127]
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            qn[k] = ((w[k] >> (4 * h)) & 0x0F0F0F0Fu) | (((qh[k & 7] >> (2 * (k >> 3) + h)) & 0x01010101u) << 4);
+        k4_scales(*reinterpret_cast<const uint4 *>(row), h, dl2, nml2);
     }
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int, uint32_t tile,
@@ -803,6 +838,7 @@ cudaError_t launch_prefill_gemm(const GemmArgs *a, int n, void *encode_fn, cudaS
     switch (a[0].type) {
     case 0: return launch_typed<0>(a, n, enc, stream);
     case kQ4_K: return launch_typed<kQ4_K>(a, n, enc, stream);
+    case kQ5_K: return launch_typed<kQ5_K>(a, n, enc, stream);
     case kQ2_K: return launch_typed<kQ2_K>(a, n, enc, stream);
     case kQ6_K: return launch_typed<kQ6_K>(a, n, enc, stream);
     case kQ8_0: return launch_typed<kQ8_0>(a, n, enc, stream);

@@ -8,9 +8,11 @@
 namespace qp {
 
 // GGUF type ids.
+constexpr int kF16 = 1;
 constexpr int kQ8_0 = 8;
 constexpr int kQ2_K = 10;
 constexpr int kQ4_K = 12;
+constexpr int kQ5_K = 13;
 constexpr int kQ6_K = 14;
 
 // Device error word bits (OR-ed by kernels, read and cleared by qp_check).

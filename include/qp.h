@@ -42,7 +42,14 @@
  *                                                        value = d*sc*q - dmin*m
  *   QP_Q6_K 256 / 210: ql:u8[128] (low 4 bits), qh:u8[64] (high 2 bits),
  *                      scales:int8[16], d:f16;           value = d*s*(q-32)
- * The byte layout within a block is the GGUF one.
+ *   QP_Q5_K 256 / 176: d:f16, dmin:f16, scales:u8[12] (as Q4_K), qh:u8[32]
+ *                      (fifth bit of each q), qs:u8[128] (low 4 bits);
+ *                                                        value = d*sc*q - dmin*m
+ *   QP_F16    1 / 2:   one fp16 weight;                  value = that number
+ * The byte layout within a block is the GGUF one.  (Q5_K and F16 are in the
+ * list of types the f32 dequant has device kernels for, issue #4952
+ * §Cause.)  For F16 the GEMM entry points run the cached-f16 kernel on W
+ * itself: qp_prefill_gemm(QP_F16, W16, ...) equals qp_prefill_gemm_f16w.
  */
 #ifndef QP_H
 #define QP_H
@@ -55,9 +62,11 @@ extern "C" {
 
 /* Block types; the values are the GGUF type ids. */
 typedef enum {
+    QP_F16 = 1,
     QP_Q8_0 = 8,
     QP_Q2_K = 10,
     QP_Q4_K = 12,
+    QP_Q5_K = 13,
     QP_Q6_K = 14
 } qp_type;
 

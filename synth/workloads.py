@@ -7,7 +7,7 @@ o reads its own attention-output input X_o [T x hidden] and down its MLP
 input X_f [T x ffn] (there is no attention or MLP between them here, so each
 is an independent standard-normal fp16 tensor).  Weights are [out x in].
 """
-from . import Q2_K, Q4_K, Q6_K, Q8_0
+from . import Q2_K, Q4_K, Q5_K, Q6_K, Q8_0
 
 # (name, out, in, input)
 def layer_shapes(hidden, kv, ffn):
@@ -32,6 +32,9 @@ WORKLOADS = {
     # Qwen3-8B-shaped layer, all Q4_K, a 31,258-token prompt in chunks of 4,864
     "qwen3_8b_q4k_t31258_chunk4864": dict(seed=4, T=31258, chunk=4864, dims=QWEN3_8B,
                                           projections=[p + (Q4_K,) for p in layer_shapes(**QWEN3_8B)]),
+    # Qwen3-8B-shaped layer, all Q5_K, 8192 tokens (the Q5_K row of the next types)
+    "qwen3_8b_q5k_t8192": dict(seed=5, T=8192, dims=QWEN3_8B,
+                               projections=[p + (Q5_K,) for p in layer_shapes(**QWEN3_8B)]),
 }
 
 # Dequant sweep: Q4_K 4096x4096 and 37x1000 (last superblock of each row holds 232 values).

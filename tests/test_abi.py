@@ -47,7 +47,9 @@ def test_block_info_and_row_bytes():
     assert qp.qp_block_info(qp.Q6_K) == (256, 210)
     assert qp.qp_row_bytes(qp.Q4_K, 1000) == 4 * 144
     assert qp.qp_row_bytes(qp.Q8_0, 33) == 2 * 34
-    assert qp.qp_row_bytes(13, 256) == -1 and qp.qp_row_bytes(qp.Q4_K, 0) == -1
+    assert qp.qp_block_info(qp.Q5_K) == (256, 176) and qp.qp_block_info(qp.F16) == (1, 2)
+    assert qp.qp_row_bytes(qp.F16, 1000) == 2000 and qp.qp_row_bytes(qp.Q5_K, 300) == 2 * 176
+    assert qp.qp_row_bytes(11, 256) == -1 and qp.qp_row_bytes(qp.Q4_K, 0) == -1
     with pytest.raises(qp.QPError) as e:
         qp.qp_block_info(21)
     assert e.value.status == qp.QP_ERR_UNSUPPORTED_TYPE

@@ -13,7 +13,7 @@ from qp_testutil import dev, guard_intact, guarded
 
 pytestmark = pytest.mark.gpu
 
-TYPES = {"Q8_0": qp.Q8_0, "Q2_K": qp.Q2_K, "Q4_K": qp.Q4_K, "Q6_K": qp.Q6_K}
+TYPES = {"Q8_0": qp.Q8_0, "Q2_K": qp.Q2_K, "Q4_K": qp.Q4_K, "Q5_K": qp.Q5_K, "Q6_K": qp.Q6_K, "F16": qp.F16}
 
 SHAPES = [
     ("Q8_0", 256, 512),        # the Q8_0 tiny weight
@@ -32,6 +32,13 @@ SHAPES = [
     ("Q8_0", 1, 31),
     ("Q4_K", 3, 4),            # f32 rows 16-byte aligned, f16 rows not
     ("Q6_K", 2, 6),
+    ("Q5_K", 1024, 4096),
+    ("Q5_K", 37, 1000),
+    ("Q5_K", 3, 255),
+    ("F16", 256, 512),
+    ("F16", 7, 33),            # 231 values: a last partial group of 8
+    ("F16", 1, 1),
+    ("F16", 3, 1000),
 ]
 
 

@@ -72,6 +72,9 @@ SMALL = [
     (qp.Q4_K, 132, 256, 1),        # partial weight tile, one token
     (qp.Q4_K, 4, 256, 3),
     (qp.Q2_K, 1028, 1024, 260),
+    (qp.Q5_K, 384, 512, 300),
+    (qp.Q5_K, 132, 2048, 77),
+    (qp.F16, 260, 512, 129),       # fp16 weights: the cached-mode kernel
 ]
 
 
@@ -92,7 +95,7 @@ def test_gemm_q8_0_tiny_workload(cuda_device):
     check_against_oracle(qtype, w, X, Y, what="q8_0_tiny")
 
 
-@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q6_K])
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
 def test_one_hot_rows_reproduce_f16_weights_exactly(cuda_device, qtype):
     out_f, in_f = 256, 2048
     w = synth.blocks(qtype, out_f, in_f, seed=5, tensor=qtype)
@@ -106,7 +109,7 @@ def test_one_hot_rows_reproduce_f16_weights_exactly(cuda_device, qtype):
         assert np.array_equal(Y[t_], W16[:, k]), k
 
 
-@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q6_K])
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
 def test_fused_equals_cached_f16_bitwise(cuda_device, qtype):
     out_f, in_f, T = 384, 2048, 600
     w = synth.blocks(qtype, out_f, in_f, seed=6, tensor=qtype)
@@ -139,7 +142,7 @@ def test_chunked_equals_unchunked_bitwise(cuda_device, mode):
 GROUP_SHAPES = [(384, 512), (132, 1024), (1028, 256), (4, 512), (256, 2048), (640, 4096), (132, 2048)]
 
 
-@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q6_K])
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
 def test_grouped_launch_equals_single_calls_bitwise(cuda_device, qtype):
     """One persistent launch over several projections (different out_f and
     in_f, each with its own X) gives each Y bitwise as its own call does."""
