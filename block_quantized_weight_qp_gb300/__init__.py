@@ -28,9 +28,22 @@ QP_ERR_NO_DEVICE = 7
 # Every symbol include/qp.h declares.
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",
            "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_gemm_group", "qp_prefill_chunked_group",
-           "qp_prefill_chunked", "qp_check", "qp_set_wait_limit_ns", "qp_debug_inject_stall")
+           "qp_prefill_chunked", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
+           "qp_debug_inject_stall")
 
 QP_MAX_GROUP = 8
+
+
+class QPProjShape(ctypes.Structure):
+    """qp_proj_shape: one projection for the fit planner."""
+    _fields_ = [("type", ctypes.c_int), ("out_f", ctypes.c_int64), ("in_f", ctypes.c_int64)]
+
+
+class QPPrefillPlan(ctypes.Structure):
+    """qp_prefill_plan: the planner's answer."""
+    _fields_ = [("mode", ctypes.c_int), ("chunk", ctypes.c_int64), ("weight_bytes", ctypes.c_int64),
+                ("f16_cache_bytes", ctypes.c_int64), ("act_bytes_per_row", ctypes.c_int64),
+                ("total_bytes", ctypes.c_int64)]
 
 
 class QPGemmDesc(ctypes.Structure):
@@ -68,13 +81,16 @@ def load():
         lib.qp_prefill_gemm_group.argtypes = [i, ctypes.POINTER(QPGemmDesc), i, i64, vp]
         lib.qp_prefill_chunked_group.argtypes = [i, ctypes.POINTER(QPGemmDesc), i, i64, i64, vp]
         lib.qp_prefill_chunked.argtypes = [i, vp, vp, i64, i64, vp, i64, vp, i64, i, vp]
+        lib.qp_plan_prefill.argtypes = [ctypes.POINTER(QPProjShape), i, i64, i64, i64, i64, i64,
+                                        ctypes.POINTER(QPPrefillPlan)]
         lib.qp_check.argtypes = [vp]
         lib.qp_set_wait_limit_ns.argtypes = [u64]
         lib.qp_set_wait_limit_ns.restype = None
         lib.qp_debug_inject_stall.argtypes = [i]
         lib.qp_debug_inject_stall.restype = None
         for name in ("qp_dequant_f32", "qp_dequant_f16", "qp_prefill_gemm", "qp_prefill_gemm_f16w",
-                     "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_check"):
+                     "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_plan_prefill",
+                     "qp_check"):
             getattr(lib, name).restype = i
         _lib = lib
     return _lib
@@ -163,6 +179,17 @@ def qp_prefill_chunked_group(qtype, descs, T, chunk, stream=None):
 def qp_prefill_chunked(qtype, W, W16, out_f, in_f, X, T, Y, chunk, mode, stream=None):
     _ok(load().qp_prefill_chunked(qtype, _ptr(W), _ptr(W16), out_f, in_f, _ptr(X), T, _ptr(Y), chunk, mode,
                                   _stream(stream)), "qp_prefill_chunked")
+
+
+def qp_plan_prefill(shapes, T, free_bytes, kv_bytes=0, reserve_bytes=0, max_chunk=0):
+    """shapes: sequence of (type, out_f, in_f).  Returns a dict of the plan."""
+    arr = (QPProjShape * max(len(shapes), 1))()
+    for k, (t, o, i_) in enumerate(shapes):
+        arr[k] = QPProjShape(t, o, i_)
+    plan = QPPrefillPlan()
+    _ok(load().qp_plan_prefill(arr, len(shapes), T, free_bytes, kv_bytes, reserve_bytes, max_chunk,
+                               ctypes.byref(plan)), "qp_plan_prefill")
+    return {f: getattr(plan, f) for f, _ in QPPrefillPlan._fields_}
 
 
 def qp_check(stream=None):

@@ -294,6 +294,46 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
     return QP_OK;
 }
 
+qp_status qp_plan_prefill(const qp_proj_shape *proj, int n, int64_t T, int64_t free_bytes, int64_t kv_bytes,
+                          int64_t reserve_bytes, int64_t max_chunk, qp_prefill_plan *out) {
+    if (!proj || !out || n < 1 || T < 1 || free_bytes < 0 || kv_bytes < 0 || reserve_bytes < 0)
+        return QP_ERR_INVALID_PARAMETER;
+    int64_t wb = 0, cache = 0, act = 0;
+    for (int i = 0; i < n; ++i) {
+        const qp_proj_shape &p = proj[i];
+        if (p.out_f < 1 || p.in_f < 1) return QP_ERR_INVALID_PARAMETER;
+        if (!valid_type(p.type)) return QP_ERR_UNSUPPORTED_TYPE;
+        wb += p.out_f * qp_row_bytes(p.type, p.in_f);
+        if (p.type != qp::kF16) cache += p.out_f * p.in_f * 2;
+        act += 2 * p.in_f + 4 * p.out_f;
+    }
+    const int64_t cap = max_chunk > 0 && max_chunk < T ? max_chunk : T;
+    // largest chunk <= cap with fixed + chunk * act <= free; 0 if none
+    auto fit = [&](int64_t fixed) -> int64_t {
+        if (fixed > free_bytes) return 0;
+        int64_t rows = (free_bytes - fixed) / act;
+        if (rows > cap) rows = cap;
+        if (rows >= 256) rows -= rows % 256;
+        return rows;
+    };
+    out->weight_bytes = wb;
+    out->f16_cache_bytes = cache;
+    out->act_bytes_per_row = act;
+    const int64_t base = wb + kv_bytes + reserve_bytes;
+    int64_t c = fit(base + cache);
+    if (c >= 1) {
+        out->mode = 1;
+        out->chunk = c;
+        out->total_bytes = base + cache + c * act;
+        return QP_OK;
+    }
+    c = fit(base);
+    out->mode = c >= 1 ? 0 : -1;
+    out->chunk = c;
+    out->total_bytes = c >= 1 ? base + c * act : 0;
+    return QP_OK;
+}
+
 qp_status qp_check(void *stream) {
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);

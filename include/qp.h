@@ -196,6 +196,47 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
                              int64_t chunk, int mode, void *stream);
 
 /*
+ * Prefill fit planner (PR #4624 §What changes: the FP16 batched prefill is
+ * taken only when weights + FP16 cache + KV + prefill reserve fit in free
+ * VRAM, and the resident estimate is read from the projection tensors'
+ * own bytes; CUDA prefill VRAM loans PR, §Individual feature evidence: free
+ * memory sets the prompt chunk).  Host only; needs no device.
+ *
+ * For the n projections `proj` (block type, out_f, in_f) of a prompt of T
+ * rows it computes
+ *   weight_bytes      = sum out_f * qp_row_bytes(type, in_f)
+ *   f16_cache_bytes   = sum out_f * in_f * 2       (the cached mode's copies)
+ *   act_bytes_per_row = sum (2 * in_f + 4 * out_f) (each projection's X and
+ *                       Y row; an upper bound when projections share X)
+ * and picks, in this order:
+ *   mode 1 (cached f16) if weights + f16 cache + kv_bytes + reserve_bytes
+ *          + chunk * act_bytes_per_row <= free_bytes for some chunk >= 1,
+ *   mode 0 (fused, no f16 copies) if the same holds without the f16 cache,
+ *   mode -1 otherwise (does not fit: the caller keeps its serial path).
+ * chunk = the largest number of rows <= min(T, max_chunk) that fits,
+ * rounded down to a multiple of 256 (the GEMM's token tile) when it is at
+ * least 256; max_chunk <= 0 means no cap.  With mode -1, chunk = 0.
+ * total_bytes = the memory the chosen plan needs.  Type F16 counts its
+ * weight bytes once (it is its own f16 copy).
+ * Errors: QP_ERR_INVALID_PARAMETER (null pointer, n < 1, T < 1, a negative
+ * byte count, out_f or in_f < 1), QP_ERR_UNSUPPORTED_TYPE.
+ */
+typedef struct {
+    int type;
+    int64_t out_f, in_f;
+} qp_proj_shape;
+
+typedef struct {
+    int mode;
+    int64_t chunk;
+    int64_t weight_bytes, f16_cache_bytes, act_bytes_per_row, total_bytes;
+} qp_prefill_plan;
+
+qp_status qp_plan_prefill(const qp_proj_shape *proj, int n, int64_t T, int64_t free_bytes,
+                          int64_t kv_bytes, int64_t reserve_bytes, int64_t max_chunk,
+                          qp_prefill_plan *out);
+
+/*
  * Synchronize `stream`, then read and clear the device error word.
  * Returns QP_OK, QP_ERR_TIMEOUT (a bounded wait inside a GEMM ran out; its
  * output is incomplete) or QP_ERR_CUDA (the stream reported an error).
