@@ -316,6 +316,64 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
     return out
 
 
+def bench_gemv(qp, layer, stream, device, peaks, steps=20):
+    """The decode GEMV over the layer's seven weights for T = 1 and 8 token
+    rows.  The weights (88 MB here) would fit in L2, so before every timed
+    step a 256 MB buffer is written (outside the timed region: events bracket
+    the GEMV launches of each step only).  GB/s counts the weight bytes plus
+    the X and Y bytes of a step."""
+    import torch
+    wl = layer.wl
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    wbytes = sum(w.numel() for w in layer.W)
+    out = {}
+    for T in (1, 8):
+        dims = workloads.input_dims(wl)
+        X = {k: torch.from_numpy(synth.normal_f16((T, d), seed=wl["seed"], tensor=3000 + i)).to(device)
+             for i, (k, d) in enumerate(dims.items())}
+        Y = [torch.empty((T, o), dtype=torch.float32, device=device) for _, o, _, _, _ in wl["projections"]]
+
+        def step():
+            for i, (_, o, n, src, qt) in enumerate(wl["projections"]):
+                qp.qp_decode_gemv(qt, layer.W[i], o, n, X[src], T, Y[i], stream)
+
+        step()
+        torch.cuda.synchronize()
+        # the seven launches captured once in a CUDA graph (as a decode loop
+        # would run them); eager launches are timed too: there the host's
+        # per-call cost shows between the microsecond kernels
+        cap = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for i, (_, o, n, src, qt) in enumerate(wl["projections"]):
+                    qp.qp_decode_gemv(qt, layer.W[i], o, n, X[src], T, Y[i], cap)
+        torch.cuda.synchronize()
+        res = {}
+        for how in ("graph", "eager"):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                if how == "graph":
+                    graph.replay()
+                else:
+                    step()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            res[how] = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+        qp.qp_check(stream)
+        del graph
+        ms = res["graph"]
+        nbytes = wbytes + sum(x.numel() * 2 for x in X.values()) + sum(y.numel() * 4 for y in Y)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out["T%d" % T] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1),
+                          "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 1),
+                          "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4)}
+    del flush
+    return out
+
+
 def cpu_oracle_sample(wl, seconds=10.0, rows_max=4096):
     """The CPU oracle as it stands on a bounded sample of the workload: it
     dequantizes all seven weights to f32 and computes the fp64 projection for
@@ -365,12 +423,28 @@ def main_dequant_only(args):
     print(json.dumps({"dequant": rows}))
 
 
+def main_gemv_only(args):
+    """Decode GEMV row only (profiling runs): the workload's weights, T = 1 and 8."""
+    import torch
+
+    import block_quantized_weight_qp_gb300 as qp
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    qp.load()
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(device)
+    layer = Layer(workloads.WORKLOADS[args.workload], 0, device)
+    print(json.dumps({"decode_gemv": bench_gemv(qp, layer, stream, device, peaks, steps=args.steps)}))
+
+
 def main_qp(args):
     import torch
 
     import block_quantized_weight_qp_gb300 as qp
     if args.dequant_only:
         return main_dequant_only(args)
+    if args.gemv_only:
+        return main_gemv_only(args)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -531,6 +605,7 @@ def main_qp(args):
             rows["qwen3_8b_q5k_t8192"] = {"ms": round(ms5k, 4), "tflops": round(l5k.flops() / ms5k / 1e9, 1),
                                           "tok_per_s": round(l5k.T / ms5k * 1e3, 1)}
             del l5k
+            rows["decode_gemv_" + args.workload] = bench_gemv(qp, layer, stream, device, peaks)
             wl5 = workloads.WORKLOADS["qwen3_8b_q4k_t31258_chunk4864"]
             l5 = Layer(wl5, rank, device, need_f16=True)
             ms_f = time_layer(qp, l5, stream, 3, 1, mode="fused", chunk=wl5["chunk"])
@@ -636,6 +711,7 @@ def parse_args(argv=None):
     p.add_argument("--mode", choices=["fused", "cached"], default="fused",
                    help="cached: the same step over f16 weights made once by qp_dequant_f16")
     p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")
+    p.add_argument("--gemv-only", action="store_true", help="only the decode GEMV row")
     p.add_argument("--dequant-cases", default=None, help="e.g. Q4_K_f16,Q2_K_f32 (with --dequant-only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-rows", type=int, default=8)

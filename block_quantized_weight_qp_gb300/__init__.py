@@ -28,10 +28,11 @@ QP_ERR_NO_DEVICE = 7
 # Every symbol include/qp.h declares.
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",
            "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_gemm_group", "qp_prefill_chunked_group",
-           "qp_prefill_chunked", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
+           "qp_prefill_chunked", "qp_decode_gemv", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
            "qp_debug_inject_stall")
 
 QP_MAX_GROUP = 8
+QP_GEMV_MAX_T = 8
 
 
 class QPProjShape(ctypes.Structure):
@@ -83,6 +84,7 @@ def load():
         lib.qp_prefill_chunked.argtypes = [i, vp, vp, i64, i64, vp, i64, vp, i64, i, vp]
         lib.qp_plan_prefill.argtypes = [ctypes.POINTER(QPProjShape), i, i64, i64, i64, i64, i64,
                                         ctypes.POINTER(QPPrefillPlan)]
+        lib.qp_decode_gemv.argtypes = [i, vp, i64, i64, vp, i64, vp, vp]
         lib.qp_check.argtypes = [vp]
         lib.qp_set_wait_limit_ns.argtypes = [u64]
         lib.qp_set_wait_limit_ns.restype = None
@@ -90,7 +92,7 @@ def load():
         lib.qp_debug_inject_stall.restype = None
         for name in ("qp_dequant_f32", "qp_dequant_f16", "qp_prefill_gemm", "qp_prefill_gemm_f16w",
                      "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_plan_prefill",
-                     "qp_check"):
+                     "qp_decode_gemv", "qp_check"):
             getattr(lib, name).restype = i
         _lib = lib
     return _lib
@@ -179,6 +181,11 @@ def qp_prefill_chunked_group(qtype, descs, T, chunk, stream=None):
 def qp_prefill_chunked(qtype, W, W16, out_f, in_f, X, T, Y, chunk, mode, stream=None):
     _ok(load().qp_prefill_chunked(qtype, _ptr(W), _ptr(W16), out_f, in_f, _ptr(X), T, _ptr(Y), chunk, mode,
                                   _stream(stream)), "qp_prefill_chunked")
+
+
+def qp_decode_gemv(qtype, W, out_f, in_f, X, T, Y, stream=None):
+    _ok(load().qp_decode_gemv(qtype, _ptr(W), out_f, in_f, _ptr(X), T, _ptr(Y), _stream(stream)),
+        "qp_decode_gemv")
 
 
 def qp_plan_prefill(shapes, T, free_bytes, kv_bytes=0, reserve_bytes=0, max_chunk=0):

@@ -21,6 +21,7 @@ SOURCES = {
     "api.cu": [],
     "dequant.cu": ["-fmad=false"],
     "qgemm.cu": [],
+    "gemv.cu": [],
 }
 
 

@@ -294,6 +294,25 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
     return QP_OK;
 }
 
+qp_status qp_decode_gemv(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T,
+                         float *Y, void *stream) {
+    if (!W || !X || !Y || out_f < 1 || in_f < 1 || T < 1) return QP_ERR_INVALID_PARAMETER;
+    if (!valid_type(type)) return QP_ERR_UNSUPPORTED_TYPE;
+    if (T > QP_GEMV_MAX_T || in_f % 32 != 0 || in_f % qk_of(type) != 0 || out_f > (int64_t(1) << 30) ||
+        in_f > (int64_t(1) << 24) || qp::gemv_smem_bytes(T, in_f) > 232448)
+        return QP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(W) || !aligned16(X) || (reinterpret_cast<uintptr_t>(Y) & 3u) != 0) return QP_ERR_MISALIGNED;
+    DeviceInfo *d = nullptr;
+    const qp_status s = device_info(&d);
+    if (s != QP_OK) return s;
+    if (qp::launch_decode_gemv(type, W, qp_row_bytes(type, in_f), out_f, in_f, X, T, Y,
+                               static_cast<cudaStream_t>(stream), d->num_sms) != cudaSuccess) {
+        cudaGetLastError();
+        return QP_ERR_CUDA;
+    }
+    return QP_OK;
+}
+
 qp_status qp_plan_prefill(const qp_proj_shape *proj, int n, int64_t T, int64_t free_bytes, int64_t kv_bytes,
                           int64_t reserve_bytes, int64_t max_chunk, qp_prefill_plan *out) {
     if (!proj || !out || n < 1 || T < 1 || free_bytes < 0 || kv_bytes < 0 || reserve_bytes < 0)

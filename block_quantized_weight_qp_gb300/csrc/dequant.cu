@@ -26,183 +26,13 @@
 
 #include "qp_decode.cuh"
 #include "qp_internal.h"
+#include "qp_runs.cuh"
 
 namespace qp {
 namespace {
 
-__device__ __forceinline__ uint32_t ldg16(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned short *>(p));
-}
+using namespace runs;
 
-__device__ __forceinline__ uint32_t ldg32(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
-}
-
-// Raw bytes of one lane's run, loaded one loop step ahead of their decode.
-// Two-byte aligned runs (Q6_K, Q8_0) are fetched as aligned words starting
-// up to 2 bytes early (never before the block array, which is 16-byte
-// aligned) and realigned when decoded; every load stays inside
-// [run start - 2, run end).
-struct Span32 {
-    uint32_t a[9];
-    uint32_t sh;                                          // 0 or 16: realignment shift
-    __device__ __forceinline__ void load(const uint8_t *p) {
-        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p) & 2u);
-        const uint8_t *q = p - mis;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) a[k] = ldg32(q + 4 * k);
-        a[8] = mis ? ldg16(p + 30) : 0u;
-        sh = mis ? 16u : 0u;
-    }
-    __device__ __forceinline__ uint32_t word(int k) const { return __funnelshift_r(a[k], a[k + 1], sh); }
-};
-
-// ---------------------------------------------------------- per-type runs --
-// Run t (0..7) of the superblock at b: values 32t..32t+31, decoded to 16 f32
-// pairs.
-
-// Q4_K: run t is sub-block t: the low (t even) or high nibbles of
-// qs[32(t/2) .. +31]; its 6-bit scale/min are unpacked from the 12 scale
-// bytes (t < 4: low 6 bits of bytes t and t+4; t >= 4: nibbles of byte t+4
-// plus the top two bits of bytes t-4 and t).
-struct RawQ4K {
-    uint4 hd, q0, q1;
-    __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
-        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 16 + 32 * (t >> 1)));
-        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 32 + 32 * (t >> 1)));
-    }
-    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
-        const int sh = 8 * (t & 3);
-        const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
-        const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
-        const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
-        const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
-        const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
-        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-        const int nsh = 4 * (t & 1);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) affine4((w[k] >> nsh) & 0x0F0F0F0Fu, dl2, nml2, y[2 * k], y[2 * k + 1]);
-    }
-};
-
-// Q5_K: Q4_K's fields and nibble order, plus a 32-byte plane qh before qs
-// holding each value's fifth bit: run t (sub-block t) takes bit t of
-// qh[0..31].  q <= 31 still fits the exact byte-to-float step.
-struct RawQ5K {
-    uint4 hd, h0, h1, q0, q1;
-    __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
-        h0 = __ldg(reinterpret_cast<const uint4 *>(b + 16));
-        h1 = __ldg(reinterpret_cast<const uint4 *>(b + 32));
-        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 48 + 32 * (t >> 1)));
-        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 64 + 32 * (t >> 1)));
-    }
-    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
-        const int sh = 8 * (t & 3);
-        const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
-        const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
-        const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
-        const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
-        const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
-        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-        const int nsh = 4 * (t & 1);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const uint32_t h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            affine4(((w[k] >> nsh) & 0x0F0F0F0Fu) | (((h[k] >> t) & 0x01010101u) << 4), dl2, nml2, y[2 * k],
-                    y[2 * k + 1]);
-    }
-};
-
-// Q2_K: value 128n + 32j + l takes bits 2j..2j+1 of qs[32n + l]; run t has
-// n = t/4, j = t%4, sub-blocks 2t (l < 16) and 2t+1, scale bytes scales[2t],
-// scales[2t+1] (sc low nibble, m high nibble).
-struct RawQ2K {
-    uint32_t w[8], sb, dd;
-    __device__ __forceinline__ void load(const uint8_t *b, int t) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = ldg32(b + 16 + 32 * (t >> 2) + 4 * k);
-        sb = ldg32(b + 4 * (t >> 1));
-        dd = ldg32(b + 80);                                // d | dmin << 16
-    }
-    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
-        const uint32_t sbt = sb >> (16 * (t & 1));         // scales[2t] | scales[2t+1] << 8
-        const float d = h2f(dd), dmin = h2f(dd >> 16);
-        const int sh = 2 * (t & 3);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t s = (sbt >> (8 * half)) & 0xffu;
-            const float dl = __fmul_rn(d, u2f_exact(s & 15u));
-            const float nml = -__fmul_rn(dmin, u2f_exact(s >> 4));
-            const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * half + k;
-                affine4((w[i] >> sh) & 0x03030303u, dl2, nml2, y[2 * i], y[2 * i + 1]);
-            }
-        }
-    }
-};
-
-// Q6_K: value 128n + 32j + l has low four bits = a nibble (low for j < 2,
-// high for j >= 2) of ql[64n + l + 32(j&1)] and high two bits = bits
-// 2j..2j+1 of qh[32n + l]; run t has n = t/4, j = t%4, sub-blocks 2t and
-// 2t+1 with int8 scales.  y = d*s*(q - 32), an exact product.
-struct RawQ6K {
-    Span32 ql, qh;
-    uint32_t sb, db;
-    __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        ql.load(b + 64 * (t >> 2) + 32 * (t & 1));
-        qh.load(b + 128 + 32 * (t >> 2));
-        sb = ldg16(b + 192 + 2 * t);                       // two int8 scales
-        db = ldg16(b + 208);
-    }
-    __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
-        const int j = t & 3;
-        const float d = h2f(db);
-        const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
-        const int nsh = j >= 2 ? 4 : 0;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t s = (sb >> (8 * half)) & 0xffu;
-            const float dl = __fmul_rn(d, __fsub_rn(u2f_exact(s ^ 0x80u), 128.0f));   // exact int8 value
-            const pair_t dl2 = pk2(dl, dl);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * half + k;
-                const uint32_t u =
-                    ((ql.word(i) >> nsh) & 0x0F0F0F0Fu) | (((qh.word(i) >> (2 * j)) << 4) & 0x30303030u);
-                scaled4(u, dl2, nbias2, y[2 * i], y[2 * i + 1]);
-            }
-        }
-    }
-};
-
-// Q8_0: one block = one run of 32 values; q + 128 = byte ^ 0x80.
-struct RawQ80 {
-    Span32 q;
-    uint32_t db;
-    __device__ __forceinline__ void load(const uint8_t *b, int) {
-        q.load(b + 2);
-        db = ldg16(b);
-    }
-    __device__ __forceinline__ void decode(int, pair_t (&y)[16]) const {
-        const float d = h2f(db);
-        const pair_t d2 = pk2(d, d), nbias2 = pk2(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) scaled4(q.word(k) ^ 0x80808080u, d2, nbias2, y[2 * k], y[2 * k + 1]);
-    }
-};
-
-template <int TYPE> struct RawOf;
-template <> struct RawOf<kQ4_K> { using T = RawQ4K; };
-template <> struct RawOf<kQ5_K> { using T = RawQ5K; };
-template <> struct RawOf<kQ2_K> { using T = RawQ2K; };
-template <> struct RawOf<kQ6_K> { using T = RawQ6K; };
-template <> struct RawOf<kQ8_0> { using T = RawQ80; };
 
 // ----------------------------------------------------------------- kernel --
 

@@ -123,6 +123,22 @@ def test_grouped_call_argument_checks(call, status):
     assert call(qp.load()) == status
 
 
+@pytest.mark.parametrize("call,status", [
+    (lambda l: l.qp_decode_gemv(qp.Q4_K, None, 256, 256, FAKE, 1, FAKE, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 256, 256, FAKE, 0, FAKE, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 0, 256, FAKE, 1, FAKE, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv(11, FAKE, 256, 256, FAKE, 1, FAKE, None), qp.QP_ERR_UNSUPPORTED_TYPE),
+    (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 256, 256, FAKE, 9, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 256, 288, FAKE, 1, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE, 256, 48, FAKE, 1, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv(qp.F16, FAKE, 256, 13056, FAKE, 8, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE + 8, 256, 64, FAKE, 1, FAKE, None), qp.QP_ERR_MISALIGNED),
+    (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE, 256, 64, FAKE, 1, FAKE + 2, None), qp.QP_ERR_MISALIGNED),
+])
+def test_decode_gemv_argument_checks(call, status):
+    assert call(qp.load()) == status
+
+
 def test_no_device_is_an_error_not_a_fallback():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -131,3 +147,4 @@ def test_no_device_is_an_error_not_a_fallback():
     assert lib.qp_dequant_f32(qp.Q4_K, FAKE, 4, 256, FAKE, None) == qp.QP_ERR_NO_DEVICE
     assert lib.qp_prefill_gemm(qp.Q4_K, FAKE, 256, 256, FAKE, 16, FAKE, None) == qp.QP_ERR_NO_DEVICE
     assert lib.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256), (512, 512)), 2, 16, None) == qp.QP_ERR_NO_DEVICE
+    assert lib.qp_decode_gemv(qp.Q4_K, FAKE, 256, 256, FAKE, 1, FAKE, None) == qp.QP_ERR_NO_DEVICE

@@ -1,0 +1,71 @@
+"""GPU parity of qp_decode_gemv (the decode-side projection over the same
+weight blocks, T = 1..8 token rows) against the CPU oracle's fp64
+reference: the GEMM tolerance of the workload definition, exact one-hot
+rows (the GEMV multiplies the exact f32 weights), determinism."""
+import numpy as np
+import pytest
+
+import block_quantized_weight_qp_gb300 as qp
+import oracle
+import synth
+from qp_testutil import assert_gemm_within_tolerance, dev
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    (qp.Q4_K, 384, 4096, 1),
+    (qp.Q4_K, 37, 1024, 3),          # a partial warp of rows
+    (qp.Q2_K, 256, 4096, 8),
+    (qp.Q6_K, 132, 12288, 8),        # T * in_f too large for f32 staging: f16 path
+    (qp.Q6_K, 64, 2048, 1),
+    (qp.Q5_K, 200, 2048, 5),
+    (qp.Q8_0, 256, 512, 8),
+    (qp.Q8_0, 9, 96, 2),             # three runs per row: most lanes idle
+    (qp.F16, 260, 1024, 4),
+    (qp.F16, 1, 32, 1),
+]
+
+
+def gemv(qtype, Wd, out_f, in_f, Xd, T):
+    import torch
+    Y = torch.full((T, out_f), float("nan"), dtype=torch.float32, device="cuda")
+    qp.qp_decode_gemv(qtype, Wd, out_f, in_f, Xd, T, Y)
+    qp.qp_check()
+    return Y
+
+
+@pytest.mark.parametrize("qtype,out_f,in_f,T", CASES, ids=lambda x: str(x))
+def test_decode_gemv_vs_oracle(cuda_device, qtype, out_f, in_f, T):
+    w = synth.blocks(qtype, out_f, in_f, seed=out_f + T, tensor=qtype)
+    X = synth.normal_f16((T, in_f), seed=out_f + T, tensor=200)
+    Y = gemv(qtype, dev(w), out_f, in_f, dev(X), T).cpu().numpy()
+    W = oracle.dequant_f32(qtype, w, out_f, in_f)
+    Yref, A = oracle.gemm_f64(X, W)
+    assert_gemm_within_tolerance(Y, Yref, A, "gemv %d %dx%d T=%d" % (qtype, out_f, in_f, T))
+
+
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
+def test_decode_gemv_one_hot_rows_give_the_f32_weights(cuda_device, qtype):
+    out_f, in_f = 96, 2048
+    w = synth.blocks(qtype, out_f, in_f, seed=13, tensor=qtype)
+    W = oracle.dequant_f32(qtype, w, out_f, in_f)
+    for ks in ([0, 31, 32, 255, 256, 1000, 2047, 1024], [7], [2046, 1]):
+        X = np.zeros((len(ks), in_f), np.float16)
+        for t, k in enumerate(ks):
+            X[t, k] = 1.0
+        Y = gemv(qtype, dev(w), out_f, in_f, dev(X), len(ks)).cpu().numpy()
+        for t, k in enumerate(ks):
+            # the dot product adds the weight to +0 partial sums: a -0 weight (Q6_K q = 32
+            # under a negative scale) comes out +0, as IEEE addition gives
+            want = W[:, k] + np.float32(0.0)
+            assert np.array_equal(Y[t].view(np.uint32), want.view(np.uint32)), (qtype, k)
+
+
+def test_decode_gemv_is_deterministic(cuda_device):
+    import torch
+    qtype, out_f, in_f, T = qp.Q2_K, 1024, 4096, 8
+    Wd = dev(synth.blocks(qtype, out_f, in_f, seed=14, tensor=1))
+    Xd = dev(synth.normal_f16((T, in_f), seed=14, tensor=2))
+    a = gemv(qtype, Wd, out_f, in_f, Xd, T)
+    b = gemv(qtype, Wd, out_f, in_f, Xd, T)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
