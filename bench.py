@@ -452,6 +452,7 @@ def main_qp(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     qp.load()
+    qp.qp_set_gemm_cta_pairs(args.cta_pairs)
     peaks, peak_src = load_peaks()
     wl = workloads.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(device)
@@ -514,13 +515,15 @@ def main_qp(args):
     traffic = None
     if NCU_TRAFFIC["source_sha"] and NCU_TRAFFIC["source_sha"] == kernel_source_sha():
         traffic = NCU_TRAFFIC["bytes_per_launch"]
+    kname = (("pair_fused_kernel", " cta_group::2 on CTA pairs", "pair_gemm_kernel") if args.cta_pairs
+             else ("prefill_gemm_kernel", " on one CTA per tile", "prefill_gemm_kernel"))
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "traffic_what": NCU_TRAFFIC["what"] if traffic else None,
-                "kernel": ("prefill_gemm_kernel<%s> (fused dequant, tcgen05; one launch over %s)"
-                           % (dom, ",".join(dom_launch["projections"])) if args.mode == "fused"
-                           else "prefill_gemm_kernel<f16 weight> (cached mode, tcgen05; one launch over %s)"
-                           % ",".join(dom_launch["projections"])),
+                "kernel": ("%s<%s> (fused dequant, tcgen05%s; one launch over %s)"
+                           % (kname[0], dom, kname[1], ",".join(dom_launch["projections"])) if args.mode == "fused"
+                           else "%s<f16 weight> (cached mode, tcgen05%s; one launch over %s)"
+                           % (kname[2], kname[1], ",".join(dom_launch["projections"]))),
                 "peak_source": "%s dense bf16 burst (fp16 runs at the bf16 rate)" % peak_src}
 
     # ---- end to end through the C ABI with host buffers
@@ -627,6 +630,7 @@ def main_qp(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded; weights and activations drawn as the workload states)",
             "config": {"workload": args.workload, "T": T, "tokens_per_rank": T, "mode": args.mode,
+                       "tiling": "cta_pairs" if args.cta_pairs else "one_cta",
                        "projections": "q,k,v,o,gate,up (Q2_K) + down (Q6_K); hidden 4096, kv 1024, ffn 12288",
                        "accumulate": "f32", "parallelism": "replicas x%d (weak scaling, no collective)" % world,
                        "l2": "inputs larger than L2: each step streams %.2f GB of X, W and Y" % (
@@ -708,6 +712,8 @@ def parse_args(argv=None):
     p.add_argument("--no-group", action="store_true",
                    help="launch the step's projections one at a time instead of one grouped launch per type")
     p.add_argument("--d2h-streams", type=int, default=1, help="copy streams for the e2e read-back of Y")
+    p.add_argument("--cta-pairs", type=int, choices=[0, 1], default=1,
+                   help="GEMM tiling: 1 = 256-row tiles on CTA pairs (default), 0 = 128-row tiles on one CTA")
     p.add_argument("--mode", choices=["fused", "cached"], default="fused",
                    help="cached: the same step over f16 weights made once by qp_dequant_f16")
     p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")

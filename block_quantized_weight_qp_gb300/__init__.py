@@ -29,7 +29,7 @@ QP_ERR_NO_DEVICE = 7
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",
            "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_gemm_group", "qp_prefill_chunked_group",
            "qp_prefill_chunked", "qp_decode_gemv", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
-           "qp_debug_inject_stall")
+           "qp_debug_inject_stall", "qp_set_gemm_cta_pairs")
 
 QP_MAX_GROUP = 8
 QP_GEMV_MAX_T = 8
@@ -90,6 +90,8 @@ def load():
         lib.qp_set_wait_limit_ns.restype = None
         lib.qp_debug_inject_stall.argtypes = [i]
         lib.qp_debug_inject_stall.restype = None
+        lib.qp_set_gemm_cta_pairs.argtypes = [i]
+        lib.qp_set_gemm_cta_pairs.restype = None
         for name in ("qp_dequant_f32", "qp_dequant_f16", "qp_prefill_gemm", "qp_prefill_gemm_f16w",
                      "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_plan_prefill",
                      "qp_decode_gemv", "qp_check"):
@@ -209,3 +211,7 @@ def qp_set_wait_limit_ns(ns):
 
 def qp_debug_inject_stall(load_index):
     load().qp_debug_inject_stall(int(load_index))
+
+
+def qp_set_gemm_cta_pairs(on):
+    load().qp_set_gemm_cta_pairs(1 if on else 0)

@@ -33,6 +33,7 @@ DeviceInfo g_dev[kMaxDevices];
 void *g_encode = nullptr;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{-1};
+std::atomic<int> g_cta_pairs{1};
 
 bool valid_type(int t) {
     return t == qp::kF16 || t == qp::kQ8_0 || t == qp::kQ2_K || t == qp::kQ4_K || t == qp::kQ5_K ||
@@ -128,6 +129,7 @@ qp_status run_gemms(int type, const qp_gemm_desc *descs, int n, int64_t T, void 
         a[i].err = d->err;
         a[i].wait_limit_ns = g_wait_limit_ns.load();
         a[i].inject_stall = inject;
+        a[i].cta_pairs = g_cta_pairs.load() != 0;
     }
     const cudaError_t e = qp::launch_prefill_gemm(a, n, g_encode, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -373,5 +375,7 @@ qp_status qp_check(void *stream) {
 void qp_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 2000000000ull); }
 
 void qp_debug_inject_stall(int load_index) { g_inject_stall.store(load_index); }
+
+void qp_set_gemm_cta_pairs(int on) { g_cta_pairs.store(on != 0); }
 
 }  // extern "C"

@@ -5,13 +5,23 @@
 // Q2_K", §Cause: the weights are the per-type dequantized blocks, and the f16
 // mode works from an f16 copy of them).
 //
-// Two modes share one persistent, warp-specialized kernel:
+// Two modes:
 //   FUSED  W is block-quantized.  TMA stages one superblock-wide slice of 128
 //          weight rows (raw bytes) into shared memory; eight dequant warps
 //          decode it into fp16, written straight into the 128-byte-swizzled
 //          K-major layout the tensor cores read.
 //   F16W   W is a dense fp16 weight (the cached mode), staged by TMA.
-// Roles (one CTA per SM, tiles 128 weight rows x 256 tokens, K step 64):
+// Two tilings of each, all persistent and warp-specialized:
+//   CTA pairs (default; pair_fused_kernel, pair_gemm_kernel): a cluster of
+//          two CTAs on two SMs computes a 256-row x 256-token tile with the
+//          paired MMA (tcgen05 cta_group::2, M = 256); each CTA stages (or
+//          decodes) its own 128 weight rows and 128 of the tokens, so each
+//          SM's shared memory carries half the token operand.
+//   one CTA (prefill_gemm_kernel): 128-row x 256-token tiles, M = 128.
+// Both run each output through the same K steps and give bitwise equal Y.
+// Roles (one-CTA kernel; the pair kernels keep the same warp layout, with
+// the MMA issued by the first CTA of the pair; tiles 128 weight rows x 256
+// tokens, K step 64):
 //   warp 0      TMA producer (X tiles; quantized slices or fp16 W tiles)
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
 //               M=128 (weight rows) N=256 (tokens) K=16, fp32 accumulators
@@ -482,11 +492,10 @@ template <int WO> struct Dec<kQ8_0, WO> {
 #else
 #define QP_SLICE_INLINE __forceinline__
 #endif
-template <int TYPE, int WO>
+template <int TYPE, int WO, int S>
 __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int p,
                                               uint32_t ws_addr, const ChunkAddr &ca, uint64_t *qempty, int lane,
                                               int &stage, uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
-    constexpr int S = Cfg<TYPE>::WST;
     Dec<TYPE, WO> dec;
     dec.slice(row, hs16, p);
     if constexpr (Dec<TYPE, WO>::REGS) {
@@ -511,38 +520,39 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
     return true;
 }
 
-template <int TYPE>
-__device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams &gp, const uint8_t *qslots,
-                                             uint32_t ws_addr, int r, int p, int lane, uint64_t limit_ns,
-                                             uint32_t *err) {
-    using C = Cfg<TYPE>;
+// (first, stride): this CTA's tile sequence.
+template <int TYPE, int WST, int QST>
+__device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams &gp, int first, int stride,
+                                             const uint8_t *qslots, uint32_t ws_addr, int r, int p, int lane,
+                                             uint64_t limit_ns, uint32_t *err) {
+    constexpr int Q_SLOT_BYTES = BM * QFmt<TYPE>::BOX;
     const ChunkAddr ca(r, p);
     int stage = 0, qs = 0;
     uint32_t phase = 0, qphase = 0;
-    for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
+    for (int tile = first; tile < gp.num_tiles; tile += stride) {
         const int nk = gp.nk[locate(gp, tile).g];
         for (int kb = 0; kb < nk; ++kb) {
             if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) return;
-            const uint8_t *row = qslots + qs * C::Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
+            const uint8_t *row = qslots + qs * Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
             const int rem = (kb * QFmt<TYPE>::SB_BYTES) & 15;
             const uint32_t hs16 = (rem & 2) ? 16u : 0u;
             bool ok;
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                case 1: ok = dequant_slice<TYPE, 1>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                case 2: ok = dequant_slice<TYPE, 2>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                default: ok = dequant_slice<TYPE, 3>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 0: ok = dequant_slice<TYPE, 0, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = dequant_slice<TYPE, 0>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err);
+                ok = dequant_slice<TYPE, 0, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err);
             }
             if (!ok) return;
             if constexpr (!Dec<TYPE, 0>::REGS) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.qempty[qs]);
             }
-            advance(qs, qphase, C::QST);
+            advance(qs, qphase, QST);
         }
     }
 }
@@ -740,7 +750,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
         if (warp != 9 && warp != 13) {
             const int r = (u & 3) * 32 + lane;             // weight row within the tile
-            dequant_role<TYPE>(sh, gp, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns, err);
+            dequant_role<TYPE, C::WST, C::QST>(sh, gp, blockIdx.x, gridDim.x, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns,
+                                       err);
         }
     }
 
@@ -755,6 +766,432 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// --------------------------------------------------- CTA-pair cached GEMM --
+//
+// The cached (fp16 weight) mode as clusters of two CTAs sharing one
+// tcgen05.mma.cta_group::2: a pair tile is 256 weight rows x 256 tokens;
+// CTA r of the pair stages weight rows m0 + 128r and tokens n0 + 128r (its
+// halves of A and B, 16 KiB each per K step) with the pair form of TMA,
+// whose bytes complete on the leader's (rank 0) barrier; the leader issues
+// M = 256, N = 256 MMAs over both CTAs' shared memory, each CTA's TMEM
+// receiving its 128 rows of the accumulator, and multicasts its commits to
+// both CTAs; each CTA's epilogue drains its own rows and signals the leader.
+// Per SM a K step moves half the token operand of the single-CTA kernel.
+// ACC = accumulators in TMEM (256 columns each).
+template <int ACC> struct PairCfg {
+    static constexpr int ST = 6;
+    static constexpr int HALF_BYTES = 128 * BK * 2;              // 16 KiB
+    static constexpr int STAGE_BYTES = 2 * HALF_BYTES;           // A half + B half
+    static constexpr int OFF_BAR = ST * STAGE_BYTES;
+    static constexpr int NBAR = 2 * ST + 5;                      // full, empty, accfull[2], accempty[2], done
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 6 * 32;
+    static constexpr uint32_t COLS = 256u * ACC;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+constexpr uint32_t IDESC_PAIR = idesc_f16_f32(2 * BM, BN);
+
+template <int ACC>
+__global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
+    pair_gemm_kernel(const __grid_constant__ GroupParams gp, uint32_t *err, uint64_t limit_ns, int inject_stall) {
+    using P = PairCfg<ACC>;
+    const uint32_t rank = cluster_ctarank();
+    const int first = static_cast<int>(blockIdx.x) / 2, stride = static_cast<int>(gridDim.x) / 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
+    uint64_t *full = bars, *empty = bars + P::ST, *accfull = bars + 2 * P::ST, *accempty = accfull + 2,
+             *done = accfull + 4;
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + P::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + P::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::ST; ++s) {
+            mbar_init(&full[s], 1);         // leader: its producer's arrive with both CTAs' bytes
+            mbar_init(&empty[s], 1);        // the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&accfull[a], 1);      // the leader's multicast commit
+            mbar_init(&accempty[a], 8);     // leader: four epilogue warps of each CTA
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0u;
+        mbar_fence_init();
+        for (int g = 0; g < gp.n_groups; ++g) {
+            prefetch_tensormap(&gp.tmX[g]);
+            prefetch_tensormap(&gp.tmW[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_base, P::COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();                         // both CTAs' barriers and TMEM exist
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base;
+    const bool alloc_ok = tmem == ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_base), rank ^ 1u));
+    if (!alloc_ok && threadIdx.x == 0) atomicOr(err, kErrPairAlloc);
+
+    uint8_t *stages = smem;
+    if (alloc_ok && warp == 0) {
+        // --------------------------------------------------------- producer --
+        if (lane == 0) {
+            int stage = 0, loads = 0;
+            uint32_t phase = 0;
+            for (int tile = first; tile < gp.num_tiles; tile += stride) {
+                const TileLoc L = locate(gp, tile);
+                const int m0 = 2 * L.m0 + 128 * static_cast<int>(rank), n0 = L.n0 + 128 * static_cast<int>(rank);
+                const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
+                for (int k = 0; k < gp.nk[L.g] * (SB / BK); ++k) {
+                    if (!wait_phase(&empty[stage], phase ^ 1u, limit_ns, abort_flag, err, kErrTimeoutProducer))
+                        goto producer_done;
+                    const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0u);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P::STAGE_BYTES);
+                    uint8_t *st = stages + stage * P::STAGE_BYTES;
+                    if (loads++ != inject_stall) {   // test hook: leave one stage's copies unissued
+                        tma_load_2d_pair(st, tmW, bar, k * BK, m0);
+                        tma_load_2d_pair(st + P::HALF_BYTES, tmX, bar, k * BK, n0);
+                    }
+                    advance(stage, phase, P::ST);
+                }
+            }
+        producer_done:;
+        }
+        __syncwarp();
+    } else if (alloc_ok && warp == 1) {
+        // -------------------------------------------------- MMA (leader only) --
+        if (lane == 0 && rank == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            for (int tile = first; tile < gp.num_tiles; tile += stride) {
+                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
+                if (!wait_phase(&accempty[acc], acc_phase ^ 1u, limit_ns, abort_flag, err, kErrTimeoutMma))
+                    goto mma_done;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+                for (int k = 0; k < nks; ++k) {
+                    if (!wait_phase(&full[stage], phase, limit_ns, abort_flag, err, kErrTimeoutMma)) goto mma_done;
+                    tc_fence_after();
+                    uint8_t *st = stages + stage * P::STAGE_BYTES;
+                    const uint64_t adesc = desc_sw128_kmajor(smem_u32(st));
+                    const uint64_t bdesc = desc_sw128_kmajor(smem_u32(st + P::HALF_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | kk) != 0);
+                    mma_commit_pair_multicast(&empty[stage], 0x3);
+                    advance(stage, phase, P::ST);
+                }
+                mma_commit_pair_multicast(&accfull[acc], 0x3);
+                advance(acc, acc_phase, ACC);
+            }
+        mma_done:
+            mma_commit_pair_multicast(done, 0x1);
+            wait_phase(done, 0, limit_ns, abort_flag, err, kErrTimeoutMma);
+        }
+        __syncwarp();
+    } else if (alloc_ok && warp < 6) {
+        // --------------------------------------------------------- epilogue --
+        const int quarter = warp & 3;
+        const uint32_t accempty_leader = mapa_shared(smem_u32(accempty), 0u);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const int T = gp.T;
+        for (int tile = first; tile < gp.num_tiles; tile += stride) {
+            const TileLoc L = locate(gp, tile);
+            const int out_f = gp.out_f[L.g], n0 = L.n0;
+            const int o = 2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+            float *const Y = gp.Y[L.g];
+            if (!__all_sync(0xffffffffu, wait_phase(&accfull[acc], acc_phase, limit_ns, abort_flag, err,
+                                                      kErrTimeoutEpilogue)))
+                break;
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_wait_ld();
+                const int t0 = n0 + c * 32;
+                if (o < out_f) {
+                    float *yp = Y + static_cast<int64_t>(t0) * out_f + o;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (t0 + j < T) __stcs(yp + static_cast<int64_t>(j) * out_f, __uint_as_float(r[j]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(accempty_leader + static_cast<uint32_t>(acc * 8));
+            advance(acc, acc_phase, ACC);
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+    }
+    cluster_sync();                         // nothing of either CTA still in flight
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, P::COLS);
+    }
+}
+
+// ---------------------------------------------------- CTA-pair fused GEMM --
+//
+// The fused mode on CTA pairs, as the cached mode above: a pair tile is 256
+// weight rows x 256 tokens; CTA r decodes weight rows m0 + 128r (its half of
+// A) into its own shared memory exactly as the single-CTA kernel does, and
+// stages tokens n0 + 128r (its half of B) with the pair form of TMA.  The
+// leader's MMA thread waits for the token halves (TMA bytes on its fullx),
+// its own decode warps (fullw) and the peer's (peerw: one arrival per stage
+// from the peer's forwarding thread, which waits on the peer's own fullw),
+// issues the M = 256 MMAs and multicasts its commits: the stages' emptyx /
+// emptyw and the accumulators' accfull in both CTAs.
+// Ring depths: the token ring (16 KiB stages) is the one that pays for depth
+// (measured on the Q2_K / Q6_K layer: 4 -> 6 -> 8 stages, +5% then +0.5%);
+// more fp16 W stages or a second slice slot did not help.
+template <int TYPE> struct PairDepth { static constexpr int XST = 8, WST = 4, QST = 1; };
+template <> struct PairDepth<kQ8_0> { static constexpr int XST = 5, WST = 4, QST = 2; };
+
+template <int TYPE> struct PairFCfg {
+    static constexpr int XST = PairDepth<TYPE>::XST, WST = PairDepth<TYPE>::WST, QST = PairDepth<TYPE>::QST;
+    static constexpr int X_HALF = 128 * BK * 2;                  // 16 KiB: this CTA's 128 tokens
+    static constexpr int DQ_WARPS = 8;
+    static constexpr int THREADS = 16 * 32;
+    static constexpr int Q_SLOT_BYTES = BM * QFmt<TYPE>::BOX;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_W = OFF_X + XST * X_HALF;
+    static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_Q + QST * Q_SLOT_BYTES;
+    // fullx, emptyx, fullw, emptyw, peerw, qfull, qempty, accfull[2], accempty[2], done
+    static constexpr int NBAR = 2 * XST + 3 * WST + 2 * QST + 5;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static_assert(OFF_Q % 1024 == 0 && SMEM_BYTES <= 232448, "shared memory layout");
+};
+
+template <int TYPE>
+__global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
+    pair_fused_kernel(const __grid_constant__ GroupParams gp, uint32_t *err, uint64_t limit_ns, int inject_stall) {
+    using C = PairFCfg<TYPE>;
+    constexpr int XS = C::XST, WS = C::WST, QS = C::QST;
+    const uint32_t rank = cluster_ctarank();
+    const int first = static_cast<int>(blockIdx.x) / 2, stride = static_cast<int>(gridDim.x) / 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    Shared sh;
+    sh.fullx = bars;
+    sh.emptyx = bars + XS;
+    sh.fullw = bars + 2 * XS;
+    sh.emptyw = sh.fullw + WS;
+    uint64_t *peerw = sh.emptyw + WS;
+    sh.qfull = peerw + WS;
+    sh.qempty = sh.qfull + QS;
+    sh.accfull = sh.qempty + QS;
+    sh.accempty = sh.accfull + 2;
+    sh.done = sh.accfull + 4;
+    sh.tmem_base = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    sh.abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < XS; ++s) {
+            mbar_init(&sh.fullx[s], 1);            // leader: its producer's arrive with both token halves' bytes
+            mbar_init(&sh.emptyx[s], 1);           // the leader's multicast commit
+        }
+        for (int s = 0; s < WS; ++s) {
+            mbar_init(&sh.fullw[s], C::DQ_WARPS);  // this CTA's decode warps
+            mbar_init(&sh.emptyw[s], 1);           // the leader's multicast commit
+            mbar_init(&peerw[s], 1);               // leader: the peer's forwarding thread
+        }
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(&sh.qfull[s], 1);
+            mbar_init(&sh.qempty[s], C::DQ_WARPS);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sh.accfull[a], 1);
+            mbar_init(&sh.accempty[a], 8);         // leader: four epilogue warps of each CTA
+        }
+        mbar_init(sh.done, 1);
+        *sh.abort_flag = 0u;
+        mbar_fence_init();
+        for (int g = 0; g < gp.n_groups; ++g) {
+            prefetch_tensormap(&gp.tmX[g]);
+            prefetch_tensormap(&gp.tmW[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sh.tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *sh.tmem_base;
+    const bool alloc_ok = tmem == ld_shared_cluster_u32(mapa_shared(smem_u32(sh.tmem_base), rank ^ 1u));
+    if (!alloc_ok && threadIdx.x == 0) atomicOr(err, kErrPairAlloc);
+
+    uint8_t *xs = smem + C::OFF_X;
+    uint8_t *ws = smem + C::OFF_W;
+    uint8_t *qslots = smem + C::OFF_Q;
+
+    if (alloc_ok && warp == 0) {
+        // --------------------------------------------------------- producer --
+        if (lane == 0) {
+            int stage = 0, qs = 0, loads = 0;
+            uint32_t phase = 0, qphase = 0;
+            for (int tile = first; tile < gp.num_tiles; tile += stride) {
+                const TileLoc L = locate(gp, tile);
+                const int m0 = 2 * L.m0 + 128 * static_cast<int>(rank), n0 = L.n0 + 128 * static_cast<int>(rank);
+                const int nk = gp.nk[L.g];
+                const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
+                                           kErrTimeoutProducer))
+                        goto producer_done;
+                    const int start = kb * QFmt<TYPE>::SB_BYTES;
+                    mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
+                    tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
+                    advance(qs, qphase, QS);
+#pragma unroll 1
+                    for (int a = 0; a < SB / BK; ++a) {
+                        if (!wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,
+                                        kErrTimeoutProducer))
+                            goto producer_done;
+                        if (rank == 0) mbar_arrive_expect_tx(&sh.fullx[stage], 2 * C::X_HALF);
+                        if (loads != inject_stall)
+                            tma_load_2d_pair(xs + stage * C::X_HALF, tmX, mapa_shared(smem_u32(&sh.fullx[stage]), 0u),
+                                             kb * SB + a * BK, n0);
+                        ++loads;
+                        advance(stage, phase, XS);
+                    }
+                }
+            }
+        producer_done:;
+        }
+        __syncwarp();
+    } else if (alloc_ok && warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA (leader) --
+            int stage = 0, wstage = 0, acc = 0;
+            uint32_t phase = 0, wphase = 0, acc_phase = 0;
+            for (int tile = first; tile < gp.num_tiles; tile += stride) {
+                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
+                if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err,
+                                      kErrTimeoutMma))
+                    goto mma_done;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+                for (int k = 0; k < nks; ++k) {
+                    if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma) ||
+                        !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma) ||
+                        !wait_phase(&peerw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                        goto mma_done;
+                    tc_fence_after();
+                    const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wstage * W_STAGE_BYTES));
+                    const uint64_t bdesc = desc_sw128_kmajor(smem_u32(xs + stage * C::X_HALF));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | kk) != 0);
+                    mma_commit_pair_multicast(&sh.emptyx[stage], 0x3);
+                    mma_commit_pair_multicast(&sh.emptyw[wstage], 0x3);
+                    advance(stage, phase, XS);
+                    advance(wstage, wphase, WS);
+                }
+                mma_commit_pair_multicast(&sh.accfull[acc], 0x3);
+                advance(acc, acc_phase, 2);
+            }
+        mma_done:
+            mma_commit_pair_multicast(sh.done, 0x1);
+            wait_phase(sh.done, 0, limit_ns, sh.abort_flag, err, kErrTimeoutMma);
+        } else if (lane == 0) {
+            // ----------------------------------- forwarding thread (peer) --
+            // one arrival on the leader's peerw per stage this CTA's decode
+            // warps complete (their stores were made visible to the tensor
+            // cores before they arrived; the release carries them on)
+            const uint32_t peerw_leader = mapa_shared(smem_u32(peerw), 0u);
+            int wstage = 0;
+            uint32_t wphase = 0;
+            for (int tile = first; tile < gp.num_tiles; tile += stride) {
+                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
+                for (int k = 0; k < nks; ++k) {
+                    if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant))
+                        goto fwd_done;
+                    mbar_arrive_remote(peerw_leader + static_cast<uint32_t>(wstage * 8));
+                    advance(wstage, wphase, WS);
+                }
+            }
+        fwd_done:;
+        }
+        __syncwarp();
+    } else if (alloc_ok && warp < 6) {
+        // --------------------------------------------------------- epilogue --
+        const int quarter = warp & 3;
+        const uint32_t accempty_leader = mapa_shared(smem_u32(sh.accempty), 0u);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const int T = gp.T;
+        for (int tile = first; tile < gp.num_tiles; tile += stride) {
+            const TileLoc L = locate(gp, tile);
+            const int out_f = gp.out_f[L.g], n0 = L.n0;
+            const int o = 2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+            float *const Y = gp.Y[L.g];
+            if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
+                                                                 sh.abort_flag, err, kErrTimeoutEpilogue)))
+                break;
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_wait_ld();
+                const int t0 = n0 + c * 32;
+                if (o < out_f) {
+                    float *yp = Y + static_cast<int64_t>(t0) * out_f + o;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (t0 + j < T) __stcs(yp + static_cast<int64_t>(j) * out_f, __uint_as_float(r[j]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(accempty_leader + static_cast<uint32_t>(acc * 8));
+            advance(acc, acc_phase, 2);
+        }
+    } else if (alloc_ok) {
+        // ------------------------------------------------------------ decode --
+        const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
+        if (warp != 9 && warp != 13) {
+            const int r = (u & 3) * 32 + lane;                 // this CTA's weight row
+            dequant_role<TYPE, WS, QS>(sh, gp, first, stride, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns,
+                                         err);
+        }
+    }
+
+    __syncthreads();
+    if (*sh.abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+    }
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
@@ -775,13 +1212,15 @@ bool encode_2d(EncodeFn enc, CUtensorMap *map, CUtensorMapDataType dt, const voi
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of one projection: X boxes of x_rows tokens (256 for one CTA,
+// 128 for a CTA pair) x 64 values; W boxes of 128 rows (quantized slice or
+// fp16 K step).
 template <int TYPE>
-bool encode_group(EncodeFn enc, const GemmArgs &a, CUtensorMap *tmX, CUtensorMap *tmW) {
-    using C = Cfg<TYPE>;
-    if (!encode_2d(enc, tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.in_f, a.T, a.in_f * 2, BK, BN,
+bool encode_group(EncodeFn enc, const GemmArgs &a, CUtensorMap *tmX, CUtensorMap *tmW, uint32_t x_rows) {
+    if (!encode_2d(enc, tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.in_f, a.T, a.in_f * 2, BK, x_rows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return false;
-    if constexpr (C::FUSED) {
+    if constexpr (TYPE != 0) {
         const int64_t row_bytes = (a.in_f / SB) * QFmt<TYPE>::SB_BYTES;
         return encode_2d(enc, tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, row_bytes / 4, a.out_f, row_bytes,
                          QFmt<TYPE>::BOX / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -791,26 +1230,26 @@ bool encode_group(EncodeFn enc, const GemmArgs &a, CUtensorMap *tmX, CUtensorMap
     }
 }
 
-// One persistent launch over n projections of type TYPE (same T).  Groups
+// The launch's GroupParams over n projections of type TYPE (same T).  Groups
 // are ordered by in_f, longest first: their tiles take longest, and dealing
-// them out first keeps the CTAs' total work even.
+// them out first keeps the CTAs' total work even.  A tile is 128 weight rows
+// (one CTA) or 256 (a CTA pair) by 256 tokens.
 template <int TYPE>
-cudaError_t launch_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
-    using C = Cfg<TYPE>;
-    if (n < 1 || n > MAX_GROUPS) return cudaErrorInvalidValue;
+bool build_group(const GemmArgs *a, int n, EncodeFn enc, bool pair, GroupParams &gp) {
+    if (n < 1 || n > MAX_GROUPS) return false;
     int order[MAX_GROUPS];
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order, order + n, [&](int x, int y) { return a[x].in_f > a[y].in_f; });
-    GroupParams gp;
     std::memset(&gp, 0, sizeof(gp));
+    const int64_t rows_per_tile = pair ? 2 * BM : BM;
     const int64_t n_tiles = (a[0].T + BN - 1) / BN;
     int64_t tiles = 0;
     for (int j = 0; j < n; ++j) {
         const GemmArgs &g = a[order[j]];
-        if (g.T != a[0].T || !encode_group<TYPE>(enc, g, &gp.tmX[j], &gp.tmW[j])) return cudaErrorInvalidValue;
-        const int64_t m_tiles = (g.out_f + BM - 1) / BM;
+        if (g.T != a[0].T || !encode_group<TYPE>(enc, g, &gp.tmX[j], &gp.tmW[j], pair ? BN / 2 : BN)) return false;
+        const int64_t m_tiles = (g.out_f + rows_per_tile - 1) / rows_per_tile;
         tiles += m_tiles * n_tiles;
-        if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+        if (tiles > INT32_MAX) return false;
         gp.Y[j] = g.Y;
         gp.out_f[j] = static_cast<int>(g.out_f);
         gp.nk[j] = static_cast<int>(g.in_f / SB);
@@ -820,12 +1259,75 @@ cudaError_t launch_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t st
     gp.n_groups = n;
     gp.T = static_cast<int>(a[0].T);
     gp.num_tiles = static_cast<int>(tiles);
+    return true;
+}
+
+// One-CTA kernel: one persistent CTA per SM.
+template <int TYPE>
+cudaError_t launch_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
+    using C = Cfg<TYPE>;
+    GroupParams gp;
+    if (!build_group<TYPE>(a, n, enc, false, gp)) return cudaErrorInvalidValue;
     const int grid = gp.num_tiles < a[0].num_sms ? gp.num_tiles : a[0].num_sms;
     auto kern = prefill_gemm_kernel<TYPE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(gp, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
     return cudaGetLastError();
+}
+
+// CTA-pair kernels: clusters of two, as many as the GPU holds at once.
+template <typename Kern, typename... Args>
+cudaError_t launch_clusters(Kern kern, int threads, int smem, const GroupParams &gp, int num_sms, int &max_clusters,
+                            cudaStream_t stream, Args... args) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters == 0) {
+        cfg.gridDim = dim3(num_sms, 1, 1);
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess || c < 1) {
+            cudaGetLastError();
+            c = num_sms / 2;
+        }
+        max_clusters = c;
+    }
+    const int clusters = gp.num_tiles < max_clusters ? gp.num_tiles : max_clusters;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, gp, args...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int TYPE>
+cudaError_t launch_pair_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
+    GroupParams gp;
+    if (!build_group<TYPE>(a, n, enc, true, gp)) return cudaErrorInvalidValue;
+    static int max_clusters = 0;
+    if constexpr (TYPE == 0) {
+        using P = PairCfg<2>;
+        return launch_clusters(pair_gemm_kernel<2>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, max_clusters,
+                               stream, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
+    } else {
+        using P = PairFCfg<TYPE>;
+        return launch_clusters(pair_fused_kernel<TYPE>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, max_clusters,
+                               stream, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
+    }
+}
+
+template <int TYPE>
+cudaError_t launch_any(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
+    return a[0].cta_pairs ? launch_pair_typed<TYPE>(a, n, enc, stream) : launch_typed<TYPE>(a, n, enc, stream);
 }
 
 }  // namespace
@@ -836,12 +1338,12 @@ cudaError_t launch_prefill_gemm(const GemmArgs *a, int n, void *encode_fn, cudaS
     for (int i = 1; i < n; ++i)
         if (a[i].type != a[0].type) return cudaErrorInvalidValue;
     switch (a[0].type) {
-    case 0: return launch_typed<0>(a, n, enc, stream);
-    case kQ4_K: return launch_typed<kQ4_K>(a, n, enc, stream);
-    case kQ5_K: return launch_typed<kQ5_K>(a, n, enc, stream);
-    case kQ2_K: return launch_typed<kQ2_K>(a, n, enc, stream);
-    case kQ6_K: return launch_typed<kQ6_K>(a, n, enc, stream);
-    case kQ8_0: return launch_typed<kQ8_0>(a, n, enc, stream);
+    case 0: return launch_any<0>(a, n, enc, stream);
+    case kQ4_K: return launch_any<kQ4_K>(a, n, enc, stream);
+    case kQ5_K: return launch_any<kQ5_K>(a, n, enc, stream);
+    case kQ2_K: return launch_any<kQ2_K>(a, n, enc, stream);
+    case kQ6_K: return launch_any<kQ6_K>(a, n, enc, stream);
+    case kQ8_0: return launch_any<kQ8_0>(a, n, enc, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -20,6 +20,7 @@ constexpr uint32_t kErrTimeoutProducer = 1u << 0;
 constexpr uint32_t kErrTimeoutMma = 1u << 1;
 constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDequant = 1u << 3;
+constexpr uint32_t kErrPairAlloc = 1u << 4;  // the CTA pair got different TMEM addresses
 
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
                                cudaStream_t stream, int num_sms);
@@ -37,6 +38,7 @@ struct GemmArgs {
     uint32_t *err;         // device error word
     uint64_t wait_limit_ns;
     int inject_stall;      // test hook: >= 0 makes the producer drop that load
+    bool cta_pairs;        // two-CTA (M = 256) tiles, else one CTA (M = 128)
 };
 
 // Most projections one launch takes (qp_prefill_gemm_group).

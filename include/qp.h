@@ -285,6 +285,17 @@ void qp_set_wait_limit_ns(uint64_t ns);
  */
 void qp_debug_inject_stall(int load_index);
 
+/*
+ * Tiling of the prefill GEMM kernels (qp_prefill_gemm*, qp_prefill_chunked*).
+ * 1 (the default): a tile is 256 weight rows x 256 tokens computed by a
+ * cluster of two CTAs on two SMs with the paired tensor-core MMA
+ * (tcgen05 cta_group::2, M = 256); each CTA decodes and stages its own 128
+ * weight rows and 128 of the tokens.  0: a tile is 128 weight rows x 256
+ * tokens on one CTA (M = 128).  Both compute every output with the same
+ * sequence of K steps.  Applies to launches made after the call; host only.
+ */
+void qp_set_gemm_cta_pairs(int on);
+
 #ifdef __cplusplus
 }
 #endif

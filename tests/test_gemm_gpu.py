@@ -28,6 +28,15 @@ def torch():
     return t
 
 
+@pytest.fixture(params=[1, 0], ids=["cta_pairs", "one_cta"])
+def tiling(request):
+    """Runs the test on both GEMM tilings: CTA pairs (256-row tiles, the
+    default) and one CTA per 128-row tile."""
+    qp.qp_set_gemm_cta_pairs(request.param)
+    yield request.param
+    qp.qp_set_gemm_cta_pairs(1)
+
+
 def run_gemm(qtype, Wd, out_f, in_f, Xd, T, mode="fused", W16=None, chunk=None):
     t = torch()
     Y = t.empty((T, out_f), dtype=t.float32, device="cuda")
@@ -79,7 +88,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("qtype,out_f,in_f,T", SMALL, ids=lambda x: str(x))
-def test_gemm_small_shapes_vs_oracle(cuda_device, qtype, out_f, in_f, T):
+def test_gemm_small_shapes_vs_oracle(cuda_device, tiling, qtype, out_f, in_f, T):
     w = synth.blocks(qtype, out_f, in_f, seed=out_f + T, tensor=qtype)
     X = synth.normal_f16((T, in_f), seed=out_f + T, tensor=100)
     Y = run_gemm(qtype, dev(w), out_f, in_f, dev(X), T).cpu().numpy()
@@ -96,7 +105,7 @@ def test_gemm_q8_0_tiny_workload(cuda_device):
 
 
 @pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
-def test_one_hot_rows_reproduce_f16_weights_exactly(cuda_device, qtype):
+def test_one_hot_rows_reproduce_f16_weights_exactly(cuda_device, tiling, qtype):
     out_f, in_f = 256, 2048
     w = synth.blocks(qtype, out_f, in_f, seed=5, tensor=qtype)
     ks = [0, 1, 15, 16, 31, 32, 63, 64, 100, 127, 128, 255, 256, 511, 1000, 1023, 1024, 2047]
@@ -110,7 +119,7 @@ def test_one_hot_rows_reproduce_f16_weights_exactly(cuda_device, qtype):
 
 
 @pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
-def test_fused_equals_cached_f16_bitwise(cuda_device, qtype):
+def test_fused_equals_cached_f16_bitwise(cuda_device, tiling, qtype):
     out_f, in_f, T = 384, 2048, 600
     w = synth.blocks(qtype, out_f, in_f, seed=6, tensor=qtype)
     X = synth.normal_f16((T, in_f), seed=6, tensor=1)
@@ -119,6 +128,28 @@ def test_fused_equals_cached_f16_bitwise(cuda_device, qtype):
     Yf = run_gemm(qtype, Wd, out_f, in_f, Xd, T)
     Yc = run_gemm(qtype, None, out_f, in_f, Xd, T, mode="cached", W16=W16)
     assert torch().equal(Yf.view(torch().int32), Yc.view(torch().int32))
+
+
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
+def test_cta_pair_and_one_cta_tilings_agree_bitwise(cuda_device, qtype):
+    """Both tilings run every output through the same K steps of 64 (four
+    K = 16 MMAs each, in order) into an fp32 accumulator; only the number of
+    weight rows per MMA differs (256 across two SMs, or 128).  Shapes cover a
+    pair tile whose second CTA holds no weight rows (out_f = 132, 4) and
+    ragged token tails."""
+    t = torch()
+    in_f = 2048                       # a row of every type is a whole number of 16-byte units
+    for out_f, T in ((384, 300), (132, 77), (4, 3), (1028, 513)):
+        w = synth.blocks(qtype, out_f, in_f, seed=out_f + 7, tensor=qtype)
+        X = synth.normal_f16((T, in_f), seed=out_f + 7, tensor=1)
+        Wd, Xd = dev(w), dev(X)
+        try:
+            qp.qp_set_gemm_cta_pairs(0)
+            Y1 = run_gemm(qtype, Wd, out_f, in_f, Xd, T)
+        finally:
+            qp.qp_set_gemm_cta_pairs(1)
+        Y2 = run_gemm(qtype, Wd, out_f, in_f, Xd, T)
+        assert t.equal(Y1.view(t.int32), Y2.view(t.int32)), (out_f, in_f, T)
 
 
 @pytest.mark.parametrize("mode", ["fused", "cached"])
@@ -281,7 +312,7 @@ def test_long_chunked_prefill_sampled_rows(cuda_device):
         assert_gemm_within_tolerance(Ys, Yref, A, "chunked/%s" % pname)
 
 
-def test_bounded_wait_reports_timeout_and_recovers(cuda_device):
+def test_bounded_wait_reports_timeout_and_recovers(cuda_device, tiling):
     """A stage whose copy is never issued: the waits run out after the limit,
     the kernel records the timeout, frees its TMEM and returns; the next call
     runs normally in the same context."""
