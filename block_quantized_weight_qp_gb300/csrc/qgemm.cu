@@ -131,6 +131,7 @@ constexpr int MAX_GROUPS = kMaxGroup;
 struct GroupParams {
     CUtensorMap tmX[MAX_GROUPS];   // X [T x in] fp16, box 64 x 256, 128-B swizzle
     CUtensorMap tmW[MAX_GROUPS];   // quantized rows (box BOX/4 words x 128 rows) or fp16 W (64 x 128)
+    CUtensorMap tmY[MAX_GROUPS];   // Y [T x out] fp32, box 32 x 32 (CTA-pair epilogue stores)
     float *Y[MAX_GROUPS];
     int out_f[MAX_GROUPS];
     int nk[MAX_GROUPS];            // 256-value K slices per weight row (in_f / 256)
@@ -781,11 +782,49 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
 // both CTAs; each CTA's epilogue drains its own rows and signals the leader.
 // Per SM a K step moves half the token operand of the single-CTA kernel.
 // ACC = accumulators in TMEM (256 columns each).
+// Drains this warp's share of one accumulator: TMEM lanes = weight rows
+// o0 .. o0 + 31 (one per lane), 256 columns = tokens n0 .. n0 + 255, into Y
+// [T x out_f], 32 tokens at a time.  Each 32 x 32 block is transposed
+// through one of this warp's EPI_BUFS staging buffers (4 KiB, token-major
+// rows of 32 weight rows: lanes write consecutive words, so no bank
+// conflicts) and written by a TMA bulk store, which leaves out what lies past
+// out_f or T; `nst` counts this warp's stores so far.  Against plain stores
+// from registers this takes the per-token address and bounds arithmetic and
+// the global stores off the SM's load/store path, which the decode warps
+// share (measured: +17% on a 1.7B-shaped Q4_K layer at T = 2048, whose
+// tiles are short in K; +3% on the 8B-shaped layer at T = 8192).
+template <int EPI_BUFS>
+__device__ __forceinline__ void drain_acc(uint32_t taddr, const CUtensorMap *tmY, int out_f, int T, int o0, int n0,
+                                          uint32_t stage, int lane, uint32_t &nst) {
+    if (o0 >= out_f) return;                    // every row of this warp lies past the weight's end
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const int t0 = n0 + c * 32;
+        if (t0 >= T) break;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_wait_ld();
+        const uint32_t buf = stage + (nst % EPI_BUFS) * 4096u;
+        if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();   // the buffer's last store has read it
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sts32(buf + static_cast<uint32_t>(j * 128 + lane * 4), r[j]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, buf, o0, t0);
+            bulk_commit_group();
+        }
+        ++nst;
+    }
+}
+
 template <int ACC> struct PairCfg {
-    static constexpr int ST = 6;
+    static constexpr int ST = 6, EPI = 2;
     static constexpr int HALF_BYTES = 128 * BK * 2;              // 16 KiB
     static constexpr int STAGE_BYTES = 2 * HALF_BYTES;           // A half + B half
-    static constexpr int OFF_BAR = ST * STAGE_BYTES;
+    static constexpr int OFF_EPI = ST * STAGE_BYTES;             // 4 epilogue warps x EPI x 4 KiB
+    static constexpr int OFF_BAR = OFF_EPI + 4 * EPI * 4096;
     static constexpr int NBAR = 2 * ST + 5;                      // full, empty, accfull[2], accempty[2], done
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -900,38 +939,25 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
         // --------------------------------------------------------- epilogue --
         const int quarter = warp & 3;
         const uint32_t accempty_leader = mapa_shared(smem_u32(accempty), 0u);
+        const uint32_t epi = smem_u32(smem + P::OFF_EPI) + static_cast<uint32_t>(quarter * P::EPI * 4096);
         int acc = 0;
-        uint32_t acc_phase = 0;
-        const int T = gp.T;
+        uint32_t acc_phase = 0, nst = 0;
         for (int tile = first; tile < gp.num_tiles; tile += stride) {
             const TileLoc L = locate(gp, tile);
-            const int out_f = gp.out_f[L.g], n0 = L.n0;
-            const int o = 2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
-            float *const Y = gp.Y[L.g];
             if (!__all_sync(0xffffffffu, wait_phase(&accfull[acc], acc_phase, limit_ns, abort_flag, err,
                                                       kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const uint32_t taddr =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c * 32, r);
-                tmem_wait_ld();
-                const int t0 = n0 + c * 32;
-                if (o < out_f) {
-                    float *yp = Y + static_cast<int64_t>(t0) * out_f + o;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (t0 + j < T) __stcs(yp + static_cast<int64_t>(j) * out_f, __uint_as_float(r[j]));
-                }
-            }
+            drain_acc<P::EPI>(taddr, &gp.tmY[L.g], gp.out_f[L.g], gp.T,
+                              2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32, L.n0, epi, lane, nst);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(accempty_leader + static_cast<uint32_t>(acc * 8));
             advance(acc, acc_phase, ACC);
         }
+        if (lane == 0) bulk_wait_all();         // Y stores complete before the CTA's shared memory goes
     }
 
     __syncthreads();
@@ -958,14 +984,16 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
 // from the peer's forwarding thread, which waits on the peer's own fullw),
 // issues the M = 256 MMAs and multicasts its commits: the stages' emptyx /
 // emptyw and the accumulators' accfull in both CTAs.
-// Ring depths: the token ring (16 KiB stages) is the one that pays for depth
-// (measured on the Q2_K / Q6_K layer: 4 -> 6 -> 8 stages, +5% then +0.5%);
-// more fp16 W stages or a second slice slot did not help.
-template <int TYPE> struct PairDepth { static constexpr int XST = 8, WST = 4, QST = 1; };
-template <> struct PairDepth<kQ8_0> { static constexpr int XST = 5, WST = 4, QST = 2; };
+// Ring depths and epilogue staging buffers per warp.  The token ring (16 KiB
+// stages) is the one that pays for depth (measured on the Q2_K / Q6_K layer:
+// 4 -> 6 -> 8 stages, +5% then +0.5%); more fp16 W stages or a second slice
+// slot did not help.
+template <int TYPE> struct PairDepth { static constexpr int XST = 6, WST = 4, QST = 1, EPI = 2; };
+template <> struct PairDepth<kQ8_0> { static constexpr int XST = 4, WST = 4, QST = 2, EPI = 1; };
 
 template <int TYPE> struct PairFCfg {
     static constexpr int XST = PairDepth<TYPE>::XST, WST = PairDepth<TYPE>::WST, QST = PairDepth<TYPE>::QST;
+    static constexpr int EPI = PairDepth<TYPE>::EPI;
     static constexpr int X_HALF = 128 * BK * 2;                  // 16 KiB: this CTA's 128 tokens
     static constexpr int DQ_WARPS = 8;
     static constexpr int THREADS = 16 * 32;
@@ -973,12 +1001,13 @@ template <int TYPE> struct PairFCfg {
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W = OFF_X + XST * X_HALF;
     static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
-    static constexpr int OFF_BAR = OFF_Q + QST * Q_SLOT_BYTES;
+    static constexpr int OFF_EPI = OFF_Q + QST * Q_SLOT_BYTES;   // 4 epilogue warps x EPI x 4 KiB
+    static constexpr int OFF_BAR = OFF_EPI + 4 * EPI * 4096;
     // fullx, emptyx, fullw, emptyw, peerw, qfull, qempty, accfull[2], accempty[2], done
     static constexpr int NBAR = 2 * XST + 3 * WST + 2 * QST + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static_assert(OFF_Q % 1024 == 0 && SMEM_BYTES <= 232448, "shared memory layout");
+    static_assert(OFF_Q % 1024 == 0 && OFF_EPI % 128 == 0 && SMEM_BYTES <= 232448, "shared memory layout");
 };
 
 template <int TYPE>
@@ -1140,38 +1169,25 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
         // --------------------------------------------------------- epilogue --
         const int quarter = warp & 3;
         const uint32_t accempty_leader = mapa_shared(smem_u32(sh.accempty), 0u);
+        const uint32_t epi = smem_u32(smem + C::OFF_EPI) + static_cast<uint32_t>(quarter * C::EPI * 4096);
         int acc = 0;
-        uint32_t acc_phase = 0;
-        const int T = gp.T;
+        uint32_t acc_phase = 0, nst = 0;
         for (int tile = first; tile < gp.num_tiles; tile += stride) {
             const TileLoc L = locate(gp, tile);
-            const int out_f = gp.out_f[L.g], n0 = L.n0;
-            const int o = 2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
-            float *const Y = gp.Y[L.g];
             if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
                                                                  sh.abort_flag, err, kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const uint32_t taddr =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c * 32, r);
-                tmem_wait_ld();
-                const int t0 = n0 + c * 32;
-                if (o < out_f) {
-                    float *yp = Y + static_cast<int64_t>(t0) * out_f + o;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (t0 + j < T) __stcs(yp + static_cast<int64_t>(j) * out_f, __uint_as_float(r[j]));
-                }
-            }
+            drain_acc<C::EPI>(taddr, &gp.tmY[L.g], gp.out_f[L.g], gp.T,
+                              2 * L.m0 + 128 * static_cast<int>(rank) + quarter * 32, L.n0, epi, lane, nst);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(accempty_leader + static_cast<uint32_t>(acc * 8));
             advance(acc, acc_phase, 2);
         }
+        if (lane == 0) bulk_wait_all();         // Y stores complete before the CTA's shared memory goes
     } else if (alloc_ok) {
         // ------------------------------------------------------------ decode --
         const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
@@ -1251,6 +1267,10 @@ bool build_group(const GemmArgs *a, int n, EncodeFn enc, bool pair, GroupParams 
         tiles += m_tiles * n_tiles;
         if (tiles > INT32_MAX) return false;
         gp.Y[j] = g.Y;
+        // the pair kernels store Y by TMA (the C ABI keeps Y 16-byte aligned, out_f % 4 == 0)
+        if (pair && !encode_2d(enc, &gp.tmY[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.Y, g.out_f, g.T, g.out_f * 4, 32,
+                               32, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
         gp.out_f[j] = static_cast<int>(g.out_f);
         gp.nk[j] = static_cast<int>(g.in_f / SB);
         gp.m_tiles[j] = static_cast<int>(m_tiles);
