@@ -318,10 +318,14 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
 
 def bench_gemv(qp, layer, stream, device, peaks, steps=20):
     """The decode GEMV over the layer's seven weights for T = 1 and 8 token
-    rows.  The weights (88 MB here) would fit in L2, so before every timed
-    step a 256 MB buffer is written (outside the timed region: events bracket
-    the GEMV launches of each step only).  GB/s counts the weight bytes plus
-    the X and Y bytes of a step."""
+    rows, as one grouped launch per block type (qp_decode_gemv_group: the six
+    Q2_K projections, then the Q6_K down projection), captured in a CUDA
+    graph as a decode loop would run it.  Also timed: the same launches made
+    eagerly, and the seven projections launched one at a time (graph).  The
+    weights (88 MB here) would fit in L2, so before every timed step a 256 MB
+    buffer is written (outside the timed region: events bracket the GEMV
+    launches of each step only).  GB/s counts the weight bytes plus the X and
+    Y bytes of a step."""
     import torch
     wl = layer.wl
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
@@ -333,43 +337,49 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
              for i, (k, d) in enumerate(dims.items())}
         Y = [torch.empty((T, o), dtype=torch.float32, device=device) for _, o, _, _, _ in wl["projections"]]
 
-        def step():
-            for i, (_, o, n, src, qt) in enumerate(wl["projections"]):
-                qp.qp_decode_gemv(qt, layer.W[i], o, n, X[src], T, Y[i], stream)
+        def grouped(st):
+            for qt, idx in layer.launches(True):
+                descs = [(layer.W[i], wl["projections"][i][1], wl["projections"][i][2],
+                          X[wl["projections"][i][3]], Y[i]) for i in idx]
+                qp.qp_decode_gemv_group(qt, descs, T, st)
 
-        step()
+        def single(st):
+            for i, (_, o, n, src, qt) in enumerate(wl["projections"]):
+                qp.qp_decode_gemv(qt, layer.W[i], o, n, X[src], T, Y[i], st)
+
+        grouped(stream)
+        single(stream)
         torch.cuda.synchronize()
-        # the seven launches captured once in a CUDA graph (as a decode loop
-        # would run them); eager launches are timed too: there the host's
-        # per-call cost shows between the microsecond kernels
         cap = torch.cuda.Stream(device)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                for i, (_, o, n, src, qt) in enumerate(wl["projections"]):
-                    qp.qp_decode_gemv(qt, layer.W[i], o, n, X[src], T, Y[i], cap)
+        graphs = {}
+        for name, fn in (("grouped", grouped), ("single", single)):
+            graphs[name] = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graphs[name], stream=cap):
+                    fn(cap)
         torch.cuda.synchronize()
         res = {}
-        for how in ("graph", "eager"):
+        for how in ("grouped", "single", "eager"):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
             for e0, e1 in ev:
                 flush.fill_(1)
                 e0.record(stream)
-                if how == "graph":
-                    graph.replay()
+                if how == "eager":
+                    grouped(stream)
                 else:
-                    step()
+                    graphs[how].replay()
                 e1.record(stream)
             torch.cuda.synchronize()
             res[how] = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
         qp.qp_check(stream)
-        del graph
-        ms = res["graph"]
+        del graphs
+        ms = res["grouped"]
         nbytes = wbytes + sum(x.numel() * 2 for x in X.values()) + sum(y.numel() * 4 for y in Y)
         gbs = nbytes / (ms / 1e3) / 1e9
         out["T%d" % T] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1),
                           "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 1),
-                          "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4)}
+                          "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4),
+                          "one_launch_per_projection_ms": round(res["single"], 4)}
     del flush
     return out
 

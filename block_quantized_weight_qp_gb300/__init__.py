@@ -28,7 +28,7 @@ QP_ERR_NO_DEVICE = 7
 # Every symbol include/qp.h declares.
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",
            "qp_prefill_gemm", "qp_prefill_gemm_f16w", "qp_prefill_gemm_group", "qp_prefill_chunked_group",
-           "qp_prefill_chunked", "qp_decode_gemv", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
+           "qp_prefill_chunked", "qp_decode_gemv", "qp_decode_gemv_group", "qp_plan_prefill", "qp_check", "qp_set_wait_limit_ns",
            "qp_debug_inject_stall", "qp_set_gemm_cta_pairs")
 
 QP_MAX_GROUP = 8
@@ -85,6 +85,7 @@ def load():
         lib.qp_plan_prefill.argtypes = [ctypes.POINTER(QPProjShape), i, i64, i64, i64, i64, i64,
                                         ctypes.POINTER(QPPrefillPlan)]
         lib.qp_decode_gemv.argtypes = [i, vp, i64, i64, vp, i64, vp, vp]
+        lib.qp_decode_gemv_group.argtypes = [i, ctypes.POINTER(QPGemmDesc), i, i64, vp]
         lib.qp_check.argtypes = [vp]
         lib.qp_set_wait_limit_ns.argtypes = [u64]
         lib.qp_set_wait_limit_ns.restype = None
@@ -94,7 +95,7 @@ def load():
         lib.qp_set_gemm_cta_pairs.restype = None
         for name in ("qp_dequant_f32", "qp_dequant_f16", "qp_prefill_gemm", "qp_prefill_gemm_f16w",
                      "qp_prefill_gemm_group", "qp_prefill_chunked_group", "qp_prefill_chunked", "qp_plan_prefill",
-                     "qp_decode_gemv", "qp_check"):
+                     "qp_decode_gemv", "qp_decode_gemv_group", "qp_check"):
             getattr(lib, name).restype = i
         _lib = lib
     return _lib
@@ -188,6 +189,11 @@ def qp_prefill_chunked(qtype, W, W16, out_f, in_f, X, T, Y, chunk, mode, stream=
 def qp_decode_gemv(qtype, W, out_f, in_f, X, T, Y, stream=None):
     _ok(load().qp_decode_gemv(qtype, _ptr(W), out_f, in_f, _ptr(X), T, _ptr(Y), _stream(stream)),
         "qp_decode_gemv")
+
+
+def qp_decode_gemv_group(qtype, descs, T, stream=None):
+    """descs: sequence of (W, out_f, in_f, X, Y), all of type qtype."""
+    _ok(load().qp_decode_gemv_group(qtype, _descs(descs), len(descs), T, _stream(stream)), "qp_decode_gemv_group")
 
 
 def qp_plan_prefill(shapes, T, free_bytes, kv_bytes=0, reserve_bytes=0, max_chunk=0):

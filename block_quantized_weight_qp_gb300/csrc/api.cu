@@ -296,23 +296,50 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
     return QP_OK;
 }
 
-qp_status qp_decode_gemv(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T,
-                         float *Y, void *stream) {
+qp_status check_gemv(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T,
+                     const float *Y) {
     if (!W || !X || !Y || out_f < 1 || in_f < 1 || T < 1) return QP_ERR_INVALID_PARAMETER;
     if (!valid_type(type)) return QP_ERR_UNSUPPORTED_TYPE;
     if (T > QP_GEMV_MAX_T || in_f % 32 != 0 || in_f % qk_of(type) != 0 || out_f > (int64_t(1) << 30) ||
-        in_f > (int64_t(1) << 24) || qp::gemv_smem_bytes(T, in_f) > 232448)
+        in_f > (int64_t(1) << 24))
         return QP_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(W) || !aligned16(X) || (reinterpret_cast<uintptr_t>(Y) & 3u) != 0) return QP_ERR_MISALIGNED;
+    return QP_OK;
+}
+
+qp_status run_gemv(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream) {
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    if (qp::launch_decode_gemv(type, W, qp_row_bytes(type, in_f), out_f, in_f, X, T, Y,
-                               static_cast<cudaStream_t>(stream), d->num_sms) != cudaSuccess) {
+    qp::GemvArgs a[qp::kMaxGroup];
+    for (int i = 0; i < n; ++i)
+        a[i] = qp::GemvArgs{descs[i].W, qp_row_bytes(type, descs[i].in_f), descs[i].out_f, descs[i].in_f, T,
+                            descs[i].X, descs[i].Y};
+    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), d->num_sms) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
     return QP_OK;
+}
+
+qp_status qp_decode_gemv(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X, int64_t T,
+                         float *Y, void *stream) {
+    const qp_status s = check_gemv(type, W, out_f, in_f, X, T, Y);
+    if (s != QP_OK) return s;
+    const qp_gemm_desc d = {W, out_f, in_f, X, Y};
+    return run_gemv(type, &d, 1, T, stream);
+}
+
+qp_status qp_decode_gemv_group(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream) {
+    if (!descs || n < 1 || n > QP_MAX_GROUP) return QP_ERR_INVALID_PARAMETER;
+    for (int i = 0; i < n; ++i) {
+        const qp_status s = check_gemv(type, descs[i].W, descs[i].out_f, descs[i].in_f, descs[i].X, T, descs[i].Y);
+        if (s != QP_OK) return s;
+    }
+    int64_t blocks = 0;
+    for (int i = 0; i < n; ++i) blocks += (descs[i].out_f + 7) / 8;
+    if (blocks > INT32_MAX) return QP_ERR_UNSUPPORTED_SHAPE;
+    return run_gemv(type, descs, n, T, stream);
 }
 
 qp_status qp_plan_prefill(const qp_proj_shape *proj, int n, int64_t T, int64_t free_bytes, int64_t kv_bytes,

@@ -48,13 +48,15 @@ constexpr int kMaxGroup = 8;
 // projections of one type and one T; `encode` is cuTensorMapEncodeTiled.
 cudaError_t launch_prefill_gemm(const GemmArgs *a, int n, void *encode_fn, cudaStream_t stream);
 
-// Decode GEMV (T = 1..8 token rows) over a block-quantized or F16 weight;
-// row_bytes = qp_row_bytes(type, in_f).  X staging needs
-// gemv_smem_bytes(T, in_f) <= the per-block shared-memory limit.
-cudaError_t launch_decode_gemv(int type, const void *W, int64_t row_bytes, int64_t out_f, int64_t in_f,
-                               const uint16_t *X, int64_t T, float *Y, cudaStream_t stream, int num_sms);
-// (the kernel is compiled for 1, 2, 4 or 8 token rows and stages that many)
-constexpr int64_t gemv_rows(int64_t T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
-constexpr int64_t gemv_smem_bytes(int64_t T, int64_t in_f) { return gemv_rows(T) * ((in_f + 63) / 64) * 144; }
+// Decode GEMV (T = 1..8 token rows) over block-quantized or F16 weights:
+// one launch over n <= kMaxGroup projections of one type and one T, checked
+// by api.cu; row_bytes = qp_row_bytes(type, in_f).
+struct GemvArgs {
+    const void *W;
+    int64_t row_bytes, out_f, in_f, T;
+    const uint16_t *X;
+    float *Y;
+};
+cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int num_sms);
 
 }  // namespace qp

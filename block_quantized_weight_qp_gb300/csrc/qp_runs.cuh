@@ -19,13 +19,25 @@
 namespace qp {
 namespace runs {
 
-__device__ __forceinline__ uint32_t ldg16(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned short *>(p));
-}
-
-__device__ __forceinline__ uint32_t ldg32(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
-}
+// Where a run's bytes are read from: global memory through the read-only
+// path (the dequant kernels), or a copy staged in shared memory that keeps
+// the bytes' alignment modulo 16 (the decode GEMV).
+struct Gmem {
+    __device__ __forceinline__ static uint32_t u16(const uint8_t *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    __device__ __forceinline__ static uint32_t u32(const uint8_t *p) {
+        return __ldg(reinterpret_cast<const unsigned int *>(p));
+    }
+    __device__ __forceinline__ static uint4 u128(const uint8_t *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+};
+struct Smem {
+    __device__ __forceinline__ static uint32_t u16(const uint8_t *p) {
+        return *reinterpret_cast<const unsigned short *>(p);
+    }
+    __device__ __forceinline__ static uint32_t u32(const uint8_t *p) { return *reinterpret_cast<const unsigned int *>(p); }
+    __device__ __forceinline__ static uint4 u128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+};
 
 // Raw bytes of one lane's run, loaded one loop step ahead of their decode.
 // Two-byte aligned runs (Q6_K, Q8_0) are fetched as aligned words starting
@@ -35,12 +47,13 @@ __device__ __forceinline__ uint32_t ldg32(const uint8_t *p) {
 struct Span32 {
     uint32_t a[9];
     uint32_t sh;                                          // 0 or 16: realignment shift
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *p) {
         const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p) & 2u);
         const uint8_t *q = p - mis;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) a[k] = ldg32(q + 4 * k);
-        a[8] = mis ? ldg16(p + 30) : 0u;
+        for (int k = 0; k < 8; ++k) a[k] = M::u32(q + 4 * k);
+        a[8] = mis ? M::u16(p + 30) : 0u;
         sh = mis ? 16u : 0u;
     }
     __device__ __forceinline__ uint32_t word(int k) const { return __funnelshift_r(a[k], a[k + 1], sh); }
@@ -56,10 +69,11 @@ struct Span32 {
 // plus the top two bits of bytes t-4 and t).
 struct RawQ4K {
     uint4 hd, q0, q1;
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
-        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 16 + 32 * (t >> 1)));
-        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 32 + 32 * (t >> 1)));
+        hd = M::u128(b);    // d, dmin, scales[0..11]
+        q0 = M::u128(b + 16 + 32 * (t >> 1));
+        q1 = M::u128(b + 32 + 32 * (t >> 1));
     }
     __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
         const int sh = 8 * (t & 3);
@@ -81,12 +95,13 @@ struct RawQ4K {
 // qh[0..31].  q <= 31 still fits the exact byte-to-float step.
 struct RawQ5K {
     uint4 hd, h0, h1, q0, q1;
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        hd = __ldg(reinterpret_cast<const uint4 *>(b));    // d, dmin, scales[0..11]
-        h0 = __ldg(reinterpret_cast<const uint4 *>(b + 16));
-        h1 = __ldg(reinterpret_cast<const uint4 *>(b + 32));
-        q0 = __ldg(reinterpret_cast<const uint4 *>(b + 48 + 32 * (t >> 1)));
-        q1 = __ldg(reinterpret_cast<const uint4 *>(b + 64 + 32 * (t >> 1)));
+        hd = M::u128(b);    // d, dmin, scales[0..11]
+        h0 = M::u128(b + 16);
+        h1 = M::u128(b + 32);
+        q0 = M::u128(b + 48 + 32 * (t >> 1));
+        q1 = M::u128(b + 64 + 32 * (t >> 1));
     }
     __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
         const int sh = 8 * (t & 3);
@@ -111,11 +126,12 @@ struct RawQ5K {
 // scales[2t+1] (sc low nibble, m high nibble).
 struct RawQ2K {
     uint32_t w[8], sb, dd;
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int t) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = ldg32(b + 16 + 32 * (t >> 2) + 4 * k);
-        sb = ldg32(b + 4 * (t >> 1));
-        dd = ldg32(b + 80);                                // d | dmin << 16
+        for (int k = 0; k < 8; ++k) w[k] = M::u32(b + 16 + 32 * (t >> 2) + 4 * k);
+        sb = M::u32(b + 4 * (t >> 1));
+        dd = M::u32(b + 80);                                // d | dmin << 16
     }
     __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
         const uint32_t sbt = sb >> (16 * (t & 1));         // scales[2t] | scales[2t+1] << 8
@@ -143,11 +159,12 @@ struct RawQ2K {
 struct RawQ6K {
     Span32 ql, qh;
     uint32_t sb, db;
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int t) {
-        ql.load(b + 64 * (t >> 2) + 32 * (t & 1));
-        qh.load(b + 128 + 32 * (t >> 2));
-        sb = ldg16(b + 192 + 2 * t);                       // two int8 scales
-        db = ldg16(b + 208);
+        ql.template load<M>(b + 64 * (t >> 2) + 32 * (t & 1));
+        qh.template load<M>(b + 128 + 32 * (t >> 2));
+        sb = M::u16(b + 192 + 2 * t);                       // two int8 scales
+        db = M::u16(b + 208);
     }
     __device__ __forceinline__ void decode(int t, pair_t (&y)[16]) const {
         const int j = t & 3;
@@ -174,9 +191,10 @@ struct RawQ6K {
 struct RawQ80 {
     Span32 q;
     uint32_t db;
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int) {
-        q.load(b + 2);
-        db = ldg16(b);
+        q.template load<M>(b + 2);
+        db = M::u16(b);
     }
     __device__ __forceinline__ void decode(int, pair_t (&y)[16]) const {
         const float d = h2f(db);
@@ -191,9 +209,10 @@ struct RawQ80 {
 // time; the dequant kernels convert F16 with a flat kernel of their own.)
 struct RawF16 {
     uint4 a[4];
+    template <class M = Gmem>
     __device__ __forceinline__ void load(const uint8_t *b, int) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = __ldg(reinterpret_cast<const uint4 *>(b) + i);
+        for (int i = 0; i < 4; ++i) a[i] = M::u128(b + 16 * i);
     }
     __device__ __forceinline__ void decode(int, pair_t (&y)[16]) const {
 #pragma unroll

@@ -201,24 +201,36 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
  * Decode-side projection over the same weights (PR #4624 §What changes: the
  * serial prefill is one forward per prompt token; issue #4952 §Cause: the
  * decode GEMVs run over the same block types):
- *   Y[t, o] = sum_k X[t, k] * W[o, k]      0 <= t < T <= QP_GEMV_MAX_T
- * with the f32 weights qp_dequant_f32 gives (exact), f32 products and f32
- * accumulation, read once from W (bound by memory bandwidth).  Deterministic
- * run to run; within the GEMM tolerance of the fp64 reference (not bitwise
- * equal to qp_prefill_gemm, which multiplies f16-rounded weights).
+ *   Y[t, o] = sum_k X[t, k] * W16[o, k]      0 <= t < T <= QP_GEMV_MAX_T
+ * with W16 = the fp16 weights qp_dequant_f16 gives (the weights
+ * qp_prefill_gemm multiplies), exact products and f32 accumulation on the
+ * tensor cores, W read once.  Deterministic run to run; within the GEMM
+ * tolerance of the fp64 reference (not bitwise equal to qp_prefill_gemm,
+ * whose f32 sums run in another order).
  *   W   device, out_f * qp_row_bytes(type, in_f) bytes, 16-byte aligned
  *   X   device, [T x in_f] fp16 row-major, 16-byte aligned
  *   Y   device, [T x out_f] f32 row-major, 4-byte aligned
  * Any type of qp_type.  Requirements (else QP_ERR_UNSUPPORTED_SHAPE): whole
  * blocks (in_f a multiple of 256 for the K-quants, of 32 for Q8_0 and F16),
- * 1 <= T <= QP_GEMV_MAX_T, and R * ceil(in_f / 64) * 144 <= 232448 with R =
- * T rounded up to 1, 2, 4 or 8 (the token rows are staged in one CTA's
- * shared memory: in_f <= 12,864 for T > 4).
+ * 1 <= T <= QP_GEMV_MAX_T, out_f <= 2^30, in_f <= 2^24.
  * Errors also: QP_ERR_INVALID_PARAMETER (null pointer, non-positive size),
  * QP_ERR_UNSUPPORTED_TYPE, QP_ERR_MISALIGNED, QP_ERR_CUDA.
  */
 qp_status qp_decode_gemv(int type, const void *W, int64_t out_f, int64_t in_f, const uint16_t *X,
                          int64_t T, float *Y, void *stream);
+
+/*
+ * The decode GEMV of up to QP_MAX_GROUP projections of one type over the
+ * same T token rows in one launch (each desc: W blocks, out_f, in_f, its own
+ * X [T x in_f] and Y [T x out_f], as for qp_decode_gemv).  A layer's
+ * projections are microsecond GEMVs each; one launch streams their weights
+ * back to back instead of paying a pipeline fill and tail per projection.
+ * Every Y is bitwise the qp_decode_gemv result.  Requirements and errors are
+ * those of qp_decode_gemv for every desc, plus QP_ERR_INVALID_PARAMETER for a
+ * NULL descs or n outside 1..QP_MAX_GROUP, and QP_ERR_UNSUPPORTED_SHAPE when
+ * the descs hold more than 2^31 - 1 blocks of 8 weight rows in all.
+ */
+qp_status qp_decode_gemv_group(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream);
 
 /*
  * Prefill fit planner (PR #4624 §What changes: the FP16 batched prefill is

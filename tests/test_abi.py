@@ -131,9 +131,16 @@ def test_grouped_call_argument_checks(call, status):
     (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 256, 256, FAKE, 9, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
     (lambda l: l.qp_decode_gemv(qp.Q4_K, FAKE, 256, 288, FAKE, 1, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
     (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE, 256, 48, FAKE, 1, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
-    (lambda l: l.qp_decode_gemv(qp.F16, FAKE, 256, 13056, FAKE, 8, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv(qp.F16, FAKE, 256, (1 << 24) + 32, FAKE, 8, FAKE, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
     (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE + 8, 256, 64, FAKE, 1, FAKE, None), qp.QP_ERR_MISALIGNED),
     (lambda l: l.qp_decode_gemv(qp.Q8_0, FAKE, 256, 64, FAKE, 1, FAKE + 2, None), qp.QP_ERR_MISALIGNED),
+    (lambda l: l.qp_decode_gemv_group(qp.Q4_K, None, 1, 1, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv_group(qp.Q4_K, descs((256, 256)), 0, 1, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv_group(qp.Q4_K, descs(*[(256, 256)] * 9), 9, 1, None), qp.QP_ERR_INVALID_PARAMETER),
+    (lambda l: l.qp_decode_gemv_group(qp.Q4_K, descs((256, 256), (256, 288)), 2, 1, None),
+     qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv_group(qp.Q4_K, descs((256, 256)), 1, 9, None), qp.QP_ERR_UNSUPPORTED_SHAPE),
+    (lambda l: l.qp_decode_gemv_group(11, descs((256, 256)), 1, 1, None), qp.QP_ERR_UNSUPPORTED_TYPE),
 ])
 def test_decode_gemv_argument_checks(call, status):
     assert call(qp.load()) == status
@@ -148,3 +155,4 @@ def test_no_device_is_an_error_not_a_fallback():
     assert lib.qp_prefill_gemm(qp.Q4_K, FAKE, 256, 256, FAKE, 16, FAKE, None) == qp.QP_ERR_NO_DEVICE
     assert lib.qp_prefill_gemm_group(qp.Q4_K, descs((256, 256), (512, 512)), 2, 16, None) == qp.QP_ERR_NO_DEVICE
     assert lib.qp_decode_gemv(qp.Q4_K, FAKE, 256, 256, FAKE, 1, FAKE, None) == qp.QP_ERR_NO_DEVICE
+    assert lib.qp_decode_gemv_group(qp.Q4_K, descs((256, 256), (64, 512)), 2, 1, None) == qp.QP_ERR_NO_DEVICE

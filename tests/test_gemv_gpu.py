@@ -1,7 +1,8 @@
 """GPU parity of qp_decode_gemv (the decode-side projection over the same
 weight blocks, T = 1..8 token rows) against the CPU oracle's fp64
 reference: the GEMM tolerance of the workload definition, exact one-hot
-rows (the GEMV multiplies the exact f32 weights), determinism."""
+rows (the GEMV multiplies the fp16 weights of qp_dequant_f16, as the prefill
+GEMM does), determinism."""
 import numpy as np
 import pytest
 
@@ -16,13 +17,16 @@ CASES = [
     (qp.Q4_K, 384, 4096, 1),
     (qp.Q4_K, 37, 1024, 3),          # a partial warp of rows
     (qp.Q2_K, 256, 4096, 8),
-    (qp.Q6_K, 132, 12288, 8),        # T * in_f too large for f32 staging: f16 path
+    (qp.Q6_K, 132, 12288, 8),        # long rows: 384 runs over the CTA's warps
     (qp.Q6_K, 64, 2048, 1),
     (qp.Q5_K, 200, 2048, 5),
     (qp.Q8_0, 256, 512, 8),
     (qp.Q8_0, 9, 96, 2),             # three runs per row: most lanes idle
     (qp.F16, 260, 1024, 4),
     (qp.F16, 1, 32, 1),
+    (qp.Q2_K, 1029, 1024, 7),        # 65 row blocks of 16, the last with 5 rows
+    (qp.F16, 24, 13056, 8),          # 408 runs: a partial last step
+    (qp.Q8_0, 16, 4128, 6),          # 129 runs
 ]
 
 
@@ -45,10 +49,10 @@ def test_decode_gemv_vs_oracle(cuda_device, qtype, out_f, in_f, T):
 
 
 @pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
-def test_decode_gemv_one_hot_rows_give_the_f32_weights(cuda_device, qtype):
+def test_decode_gemv_one_hot_rows_give_the_f16_weights(cuda_device, qtype):
     out_f, in_f = 96, 2048
     w = synth.blocks(qtype, out_f, in_f, seed=13, tensor=qtype)
-    W = oracle.dequant_f32(qtype, w, out_f, in_f)
+    W = oracle.dequant_f16(qtype, w, out_f, in_f).view(np.float16).astype(np.float32)
     for ks in ([0, 31, 32, 255, 256, 1000, 2047, 1024], [7], [2046, 1]):
         X = np.zeros((len(ks), in_f), np.float16)
         for t, k in enumerate(ks):
@@ -69,3 +73,20 @@ def test_decode_gemv_is_deterministic(cuda_device):
     a = gemv(qtype, Wd, out_f, in_f, Xd, T)
     b = gemv(qtype, Wd, out_f, in_f, Xd, T)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
+def test_grouped_decode_gemv_equals_single_calls_bitwise(cuda_device, qtype):
+    """One launch over several projections (own X, own Y each, the long-K
+    one included) gives every Y bitwise as its own call does."""
+    import torch
+    shapes = [(37, 1024), (256, 4096), (8, 2048), (1029, 1024), (64, 12288)]
+    T = 5
+    ws = [dev(synth.blocks(qtype, o, i, seed=20 + k, tensor=qtype)) for k, (o, i) in enumerate(shapes)]
+    xs = [dev(synth.normal_f16((T, i), seed=30 + k, tensor=1)) for k, (o, i) in enumerate(shapes)]
+    singles = [gemv(qtype, w, o, i, x, T) for w, (o, i), x in zip(ws, shapes, xs)]
+    ys = [torch.full((T, o), float("nan"), dtype=torch.float32, device="cuda") for o, _ in shapes]
+    qp.qp_decode_gemv_group(qtype, [(w, o, i, x, y) for w, (o, i), x, y in zip(ws, shapes, xs, ys)], T)
+    qp.qp_check()
+    for k, (a, b) in enumerate(zip(singles, ys)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), shapes[k]
