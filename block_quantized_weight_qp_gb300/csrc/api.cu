@@ -215,8 +215,8 @@ qp_status qp_dequant_f32(int type, const void *blocks, int64_t rows, int64_t col
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    if (qp::launch_dequant_f32(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms) !=
-        cudaSuccess) {
+    if (qp::launch_dequant_f32(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms,
+                               g_encode) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
@@ -230,8 +230,8 @@ qp_status qp_dequant_f16(int type, const void *blocks, int64_t rows, int64_t col
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    if (qp::launch_dequant_f16(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms) !=
-        cudaSuccess) {
+    if (qp::launch_dequant_f16(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms,
+                               g_encode) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }

@@ -18,14 +18,24 @@
 // bits as the value formula evaluated with separately rounded f32 operations
 // (the CPU oracle).  f16 output is round-to-nearest-even of that f32.
 //
+// Stores: where the output is a whole number of 32-value runs per row (cols
+// a multiple of the block size), a warp step's 32 runs are one contiguous
+// stretch of the output; the warp writes them into a shared-memory tile in
+// the 128-byte (f32) / 64-byte (f16) swizzled layout of a TMA box of 32 runs
+// and one lane stores the tile with a single TMA tensor store.  Otherwise
+// the runs go through padded shared memory and leave as 16-byte stores.
+//
 // Tail guard: a lane writes only columns < cols; the padding values of a
 // partial last block are decoded but never stored.
 #include <cstdint>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "qp_decode.cuh"
 #include "qp_internal.h"
+#include "qp_ptx.cuh"
 #include "qp_runs.cuh"
 
 namespace qp {
@@ -69,6 +79,38 @@ template <typename OutT> struct Stage {
 template <typename OutT>
 __device__ __forceinline__ void put_run(uint8_t *stage, int lane, const pair_t (&y)[16]);
 
+// The lane's run as row `lane` of a swizzled TMA box tile: 16-byte chunk k
+// of the row at chunk position k ^ (lane % 8) (f32: 128-byte rows) or
+// k ^ ((lane / 2) % 4) (f16: 64-byte rows), so the 8 lanes of a store phase
+// hit 8 different bank groups.
+template <typename OutT>
+__device__ __forceinline__ void put_run_swz(uint32_t tile, int lane, const pair_t (&y)[16]);
+
+template <>
+__device__ __forceinline__ void put_run_swz<float>(uint32_t tile, int lane, const pair_t (&y)[16]) {
+    const uint32_t row = tile + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        float a, b, c, d;
+        unpk2(y[2 * k], a, b);
+        unpk2(y[2 * k + 1], c, d);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + static_cast<uint32_t>((k ^ (lane & 7)) << 4)),
+                     "f"(a), "f"(b), "f"(c), "f"(d)
+                     : "memory");
+    }
+}
+
+template <>
+__device__ __forceinline__ void put_run_swz<uint16_t>(uint32_t tile, int lane, const pair_t (&y)[16]) {
+    const uint32_t row = tile + static_cast<uint32_t>(lane * 64);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) << 4)),
+                     "r"(f2h2(y[4 * k])), "r"(f2h2(y[4 * k + 1])), "r"(f2h2(y[4 * k + 2])), "r"(f2h2(y[4 * k + 3]))
+                     : "memory");
+}
+
 template <>
 __device__ __forceinline__ void put_run<float>(uint8_t *stage, int lane, const pair_t (&y)[16]) {
     uint8_t *p = stage + lane * Stage<float>::PITCH;
@@ -90,10 +132,21 @@ __device__ __forceinline__ void put_run<uint16_t>(uint8_t *stage, int lane, cons
             make_uint4(f2h2(y[4 * k]), f2h2(y[4 * k + 1]), f2h2(y[4 * k + 2]), f2h2(y[4 * k + 3]));
 }
 
+// tmo: the output as [rows * cols / 32 runs x 32 values], box 32 x 32,
+// used when use_tma (every run of every row whole: cols a multiple of the
+// block size).
+// Three resident 256-thread CTAs per SM (80 registers a thread): measured
+// against two (the register use left alone) and four (heavy spills), three
+// keeps the most bytes in flight (Q4_K 4096^2 -> f32: 69% -> 73% of HBM).
+#ifndef QP_DQ_MINB
+#define QP_DQ_MINB 3
+#endif
+
 template <int TYPE, typename OutT>
-__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
+__global__ void __launch_bounds__(256, QP_DQ_MINB) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
                                                       int64_t nblocks, int64_t drow, int64_t dkb,
-                                                      OutT *__restrict__ out) {
+                                                      OutT *__restrict__ out, const __grid_constant__ CUtensorMap tmo,
+                                                      int use_tma) {
     using S = Stage<OutT>;
     using Raw = typename RawOf<TYPE>::T;
     constexpr int QK = TYPE == kQ8_0 ? 32 : 256;
@@ -101,9 +154,15 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         TYPE == kQ8_0 ? 34 : (TYPE == kQ4_K ? 144 : (TYPE == kQ5_K ? 176 : (TYPE == kQ2_K ? 84 : 210)));
     constexpr int BPW = blocks_per_warp<TYPE>();
     constexpr int RUNS_PER_BLOCK = 32 / BPW;                  // 8 (K-quants) or 1 (Q8_0)
-    __shared__ __align__(16) uint8_t stage_all[WARPS * 32 * S::PITCH];
+    // padded staging (32 runs x PITCH per warp), or two TMA box tiles per warp
+    constexpr int STAGE_BYTES = WARPS * 32 * S::PITCH > WARPS * 64 * S::RUN ? WARPS * 32 * S::PITCH : WARPS * 64 * S::RUN;
+    __shared__ __align__(16) uint8_t stage_all[STAGE_BYTES + 1024];
     const int lane = threadIdx.x & 31;
-    uint8_t *stage = stage_all + (threadIdx.x >> 5) * 32 * S::PITCH;
+    uint8_t *const base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(stage_all) + 1023) & ~uintptr_t(1023));
+    uint8_t *stage = base + (threadIdx.x >> 5) * 32 * S::PITCH;
+    // TMA box tiles of this warp: 2 x 32 runs x RUN bytes, aligned to the swizzle span
+    const uint32_t tiles = smem_u32(base) + static_cast<uint32_t>((threadIdx.x >> 5) * 64 * S::RUN);
+    uint32_t nst = 0;                                     // TMA stores this warp has issued
     const int64_t warps = static_cast<int64_t>(gridDim.x) * WARPS;
     const int64_t w0 = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
     const int t = TYPE == kQ8_0 ? 0 : (lane & 7);             // run within the superblock
@@ -133,7 +192,21 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
             const int64_t kb_first = __shfl_sync(0xffffffffu, c.kb, 0);
             whole = whole && (c.kb - lane == kb_first);
         }
-        if (__all_sync(0xffffffffu, whole)) {
+        if (use_tma && __all_sync(0xffffffffu, whole)) {
+            // the warp's 32 runs are runs first .. first + 31 of the output
+            const int64_t first = __shfl_sync(0xffffffffu, c.blk, 0) * RUNS_PER_BLOCK;
+            const uint32_t tile = tiles + (nst & 1u) * 32u * S::RUN;
+            if (lane == 0) bulk_wait_group_read<1>();     // the tile's previous store has read it
+            __syncwarp();
+            put_run_swz<OutT>(tile, lane, y);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(first));
+                bulk_commit_group();
+            }
+            ++nst;
+        } else if (__all_sync(0xffffffffu, whole)) {
             put_run<OutT>(stage, lane, y);
             __syncwarp();
             // piece k of the warp step: 32 chunks = 512 bytes, all from one block
@@ -175,10 +248,36 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         raw = next;
         c = n;
     }
+    if (use_tma && lane == 0) bulk_wait_all();            // the stores are complete before the CTA exits
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The output as [rows * cols / 32 runs x 32 values] for TMA stores of 32-run
+// boxes, when every row is a whole number of blocks (so that a warp step's
+// runs are contiguous) and the run index fits the 32-bit coordinate.
+template <int TYPE, typename OutT>
+bool encode_out(void *encode_fn, int64_t rows, int64_t cols, OutT *out, CUtensorMap *map) {
+    const int64_t qk = TYPE == kQ8_0 ? 32 : 256;
+    if (!encode_fn || cols % qk != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0) return false;
+    const int64_t runs = rows * cols / 32;
+    if (runs > INT32_MAX) return false;
+    const cuuint64_t dims[2] = {32, static_cast<cuuint64_t>(runs)};
+    const cuuint64_t strides[1] = {32 * sizeof(OutT)};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const bool f32 = sizeof(OutT) == 4;
+    return reinterpret_cast<EncodeFn>(encode_fn)(
+               map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int TYPE, typename OutT>
-cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream, int num_sms) {
+cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream, int num_sms,
+                   void *encode_fn) {
     const int64_t qk = TYPE == kQ8_0 ? 32 : 256;
     const int64_t nb = (cols + qk - 1) / qk;
     const int64_t nblocks = rows * nb;
@@ -196,8 +295,11 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
     const int64_t dblk = static_cast<int64_t>(grid) * WARPS * blocks_per_warp<TYPE>();
+    CUtensorMap tmo;
+    const bool use_tma = encode_out<TYPE, OutT>(encode_fn, rows, cols, out, &tmo);
+    if (!use_tma) memset(&tmo, 0, sizeof(tmo));
     dequant_kernel<TYPE, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), cols, nb, nblocks,
-                                                         dblk / nb, dblk % nb, out);
+                                                         dblk / nb, dblk % nb, out, tmo, use_tma ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -245,13 +347,13 @@ cudaError_t launch_f16(const uint16_t *in, int64_t n, OutT *out, cudaStream_t st
 
 template <typename OutT>
 cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream,
-                     int num_sms) {
+                     int num_sms, void *enc) {
     switch (type) {
-    case kQ8_0: return launch<kQ8_0>(blocks, rows, cols, out, stream, num_sms);
-    case kQ2_K: return launch<kQ2_K>(blocks, rows, cols, out, stream, num_sms);
-    case kQ4_K: return launch<kQ4_K>(blocks, rows, cols, out, stream, num_sms);
-    case kQ5_K: return launch<kQ5_K>(blocks, rows, cols, out, stream, num_sms);
-    case kQ6_K: return launch<kQ6_K>(blocks, rows, cols, out, stream, num_sms);
+    case kQ8_0: return launch<kQ8_0>(blocks, rows, cols, out, stream, num_sms, enc);
+    case kQ2_K: return launch<kQ2_K>(blocks, rows, cols, out, stream, num_sms, enc);
+    case kQ4_K: return launch<kQ4_K>(blocks, rows, cols, out, stream, num_sms, enc);
+    case kQ5_K: return launch<kQ5_K>(blocks, rows, cols, out, stream, num_sms, enc);
+    case kQ6_K: return launch<kQ6_K>(blocks, rows, cols, out, stream, num_sms, enc);
     case kF16: return launch_f16(static_cast<const uint16_t *>(blocks), rows * cols, out, stream, num_sms);
     default: return cudaErrorInvalidValue;
     }
@@ -260,13 +362,13 @@ cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, O
 }  // namespace
 
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
-                               cudaStream_t stream, int num_sms) {
-    return dispatch(type, blocks, rows, cols, out, stream, num_sms);
+                               cudaStream_t stream, int num_sms, void *encode_fn) {
+    return dispatch(type, blocks, rows, cols, out, stream, num_sms, encode_fn);
 }
 
 cudaError_t launch_dequant_f16(int type, const void *blocks, int64_t rows, int64_t cols, uint16_t *out,
-                               cudaStream_t stream, int num_sms) {
-    return dispatch(type, blocks, rows, cols, out, stream, num_sms);
+                               cudaStream_t stream, int num_sms, void *encode_fn) {
+    return dispatch(type, blocks, rows, cols, out, stream, num_sms, encode_fn);
 }
 
 }  // namespace qp

@@ -22,10 +22,12 @@ constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDequant = 1u << 3;
 constexpr uint32_t kErrPairAlloc = 1u << 4;  // the CTA pair got different TMEM addresses
 
+// `encode_fn` is cuTensorMapEncodeTiled (the output's tensor map for the
+// kernels' TMA stores).
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
-                               cudaStream_t stream, int num_sms);
+                               cudaStream_t stream, int num_sms, void *encode_fn);
 cudaError_t launch_dequant_f16(int type, const void *blocks, int64_t rows, int64_t cols, uint16_t *out,
-                               cudaStream_t stream, int num_sms);
+                               cudaStream_t stream, int num_sms, void *encode_fn);
 
 // Everything a GEMM launch needs, prepared on the host by api.cu.
 struct GemmArgs {
