@@ -135,15 +135,18 @@ __device__ __forceinline__ void put_run<uint16_t>(uint8_t *stage, int lane, cons
 // tmo: the output as [rows * cols / 32 runs x 32 values], box 32 x 32,
 // used when use_tma (every run of every row whole: cols a multiple of the
 // block size).
-// Three resident 256-thread CTAs per SM (80 registers a thread): measured
-// against two (the register use left alone) and four (heavy spills), three
-// keeps the most bytes in flight (Q4_K 4096^2 -> f32: 69% -> 73% of HBM).
-#ifndef QP_DQ_MINB
-#define QP_DQ_MINB 3
-#endif
+// Resident 256-thread CTAs per SM the register budget is cut for: three
+// (80 registers a thread) keeps the most bytes in flight -- measured against
+// two (the register use left alone) and four (heavy spills): Q4_K 4096^2 ->
+// f32 69% -> 73% of HBM.  Q5_K and Q6_K, whose runs carry the most raw
+// bytes, spill at 80 registers and keep two (Q6_K 4096 x 12288 -> f32: 84%
+// at two, 75% at three).
+template <int TYPE> struct MinBlocks { static constexpr int N = 3; };
+template <> struct MinBlocks<kQ5_K> { static constexpr int N = 2; };
+template <> struct MinBlocks<kQ6_K> { static constexpr int N = 2; };
 
 template <int TYPE, typename OutT>
-__global__ void __launch_bounds__(256, QP_DQ_MINB) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
+__global__ void __launch_bounds__(256, MinBlocks<TYPE>::N) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
                                                       int64_t nblocks, int64_t drow, int64_t dkb,
                                                       OutT *__restrict__ out, const __grid_constant__ CUtensorMap tmo,
                                                       int use_tma) {
