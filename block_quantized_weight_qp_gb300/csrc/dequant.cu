@@ -27,6 +27,7 @@
 //
 // Tail guard: a lane writes only columns < cols; the padding values of a
 // partial last block are decoded but never stored.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -286,13 +287,16 @@ cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cu
     const int64_t nblocks = rows * nb;
     const int64_t nwarps = (nblocks + blocks_per_warp<TYPE>() - 1) / blocks_per_warp<TYPE>();
     // one resident wave of 256-thread blocks at most
-    static int per_sm = 0;
+    static std::atomic<int> cached{0};                 // queried once per kernel, then cached
+    int per_sm = cached.load();
     if (per_sm == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dequant_kernel<TYPE, OutT>, 256, 0) != cudaSuccess ||
-            n < 1)
-            n = 1;
-        per_sm = n;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequant_kernel<TYPE, OutT>, 256, 0) !=
+                cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        cached.store(per_sm);
     }
     const int64_t want = (nwarps + WARPS - 1) / WARPS;
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;

@@ -45,6 +45,7 @@
 // latches an error bit in the device error word, makes every role stop,
 // lets copies in flight land, frees its TMEM and returns.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -1298,7 +1299,8 @@ cudaError_t launch_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t st
 
 // CTA-pair kernels: clusters of two, as many as the GPU holds at once.
 template <typename Kern, typename... Args>
-cudaError_t launch_clusters(Kern kern, int threads, int smem, const GroupParams &gp, int num_sms, int &max_clusters,
+cudaError_t launch_clusters(Kern kern, int threads, int smem, const GroupParams &gp, int num_sms,
+                            std::atomic<int> &max_clusters,
                             cudaStream_t stream, Args... args) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1313,16 +1315,18 @@ cudaError_t launch_clusters(Kern kern, int threads, int smem, const GroupParams 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_clusters == 0) {
+    int mc = max_clusters.load();                 // queried once per kernel, then cached
+    if (mc == 0) {
         cfg.gridDim = dim3(num_sms, 1, 1);
         int c = 0;
         if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess || c < 1) {
             cudaGetLastError();
             c = num_sms / 2;
         }
-        max_clusters = c;
+        mc = c;
+        max_clusters.store(c);
     }
-    const int clusters = gp.num_tiles < max_clusters ? gp.num_tiles : max_clusters;
+    const int clusters = gp.num_tiles < mc ? gp.num_tiles : mc;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, kern, gp, args...);
     if (e != cudaSuccess) return e;
@@ -1333,7 +1337,7 @@ template <int TYPE>
 cudaError_t launch_pair_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
     GroupParams gp;
     if (!build_group<TYPE>(a, n, enc, true, gp)) return cudaErrorInvalidValue;
-    static int max_clusters = 0;
+    static std::atomic<int> max_clusters{0};
     if constexpr (TYPE == 0) {
         using P = PairCfg<2>;
         return launch_clusters(pair_gemm_kernel<2>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, max_clusters,
