@@ -75,30 +75,19 @@ __device__ __forceinline__ void run_f16(const typename RawOf<TYPE>::T &raw, int 
 }
 
 // Q2_K straight to fp16: per 16-value sub-block, the four possible fp16
-// weights f16(dl * q - ml), q = 0..3 (the same one-rounding f32 arithmetic,
-// then the same fp16 rounding), held byte-planar in two words; each
-// value's 2-bit q then selects its two bytes with byte permutes.
+// weights (q2k_tables: the same one-rounding f32 arithmetic, then the same
+// fp16 rounding), held byte-planar in two words; each value's 2-bit q then
+// selects its two bytes with byte permutes.
 template <>
 __device__ __forceinline__ void run_f16<kQ2_K>(const RawQ2K &raw, int t, uint32_t (&h)[16]) {
-    const uint32_t sbt = raw.sb >> (16 * (t & 1));        // scales[2t] | scales[2t+1] << 8
-    const float d = h2f(raw.dd), dmin = h2f(raw.dd >> 16);
+    uint32_t plo[2], phi[2];
+    q2k_tables(raw.sb >> (16 * (t & 1)), h2f(raw.dd), h2f(raw.dd >> 16), plo, phi);   // scales[2t], scales[2t+1]
     const int sh = 2 * (t & 3);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const uint32_t sc = (sbt >> (8 * half)) & 0xffu;
-        const float dl = __fmul_rn(d, u2f_exact(sc & 15u));
-        const float nml = -__fmul_rn(dmin, u2f_exact(sc >> 4));
-        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-        const uint32_t h01 = f2h2(ffma2(dl2, pk2(0.0f, 1.0f), nml2));
-        const uint32_t h23 = f2h2(ffma2(dl2, pk2(2.0f, 3.0f), nml2));
-        const uint32_t plo = __byte_perm(h01, h23, 0x6420), phi = __byte_perm(h01, h23, 0x7531);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = 4 * half + k;
-            const uint32_t sel = ((raw.w[i] >> sh) & 0x03030303u) * 0x11u + 0x40404040u;   // q -> nibbles q, q + 4
-            h[2 * i] = __byte_perm(plo, phi, sel);
-            h[2 * i + 1] = __byte_perm(plo, phi, sel >> 16);
-        }
+    for (int i = 0; i < 8; ++i) {                        // values 4i .. 4i + 3, sub-block i / 4
+        const uint32_t sel = ((raw.w[i] >> sh) & 0x03030303u) * 0x11u + 0x40404040u;   // q -> nibbles q, q + 4
+        h[2 * i] = __byte_perm(plo[i >> 2], phi[i >> 2], sel);
+        h[2 * i + 1] = __byte_perm(plo[i >> 2], phi[i >> 2], sel >> 16);
     }
 }
 

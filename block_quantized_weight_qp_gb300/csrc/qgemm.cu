@@ -367,16 +367,6 @@ template <int WO> struct Dec<kQ2_K, WO> {
         row_words<4 * WO, 4, false>(row, 0, sc);
         row_words<16 + 4 * WO, 16, false>(row, 0, qs);
     }
-    // byte-planar lookup for the sub-block with scale byte b
-    __device__ __forceinline__ void lut(uint32_t b, uint32_t &plo, uint32_t &phi) const {
-        const float dl = __fmul_rn(d, static_cast<float>(b & 15u));
-        const float nml = -__fmul_rn(dmin, static_cast<float>(b >> 4));
-        const pair_t dl2 = pk2(dl, dl), nml2 = pk2(nml, nml);
-        const uint32_t h01 = f2h2(ffma2(dl2, pk2(0.0f, 1.0f), nml2));
-        const uint32_t h23 = f2h2(ffma2(dl2, pk2(2.0f, 3.0f), nml2));
-        plo = __byte_perm(h01, h23, 0x6420);
-        phi = __byte_perm(h01, h23, 0x7531);
-    }
     // 4 crumb values in the bytes of u -> 2 half2
     __device__ __forceinline__ static uint2 pick(uint32_t u, uint32_t plo, uint32_t phi) {
         const uint32_t sel = u * 0x11u + 0x40404040u;     // byte q -> nibbles (q, q + 4)
@@ -388,10 +378,11 @@ template <int WO> struct Dec<kQ2_K, WO> {
         constexpr int n = A / 2;
         const int sh = 2 * (2 * (A % 2) + h);            // 2j
         const uint32_t sw = sc[A] >> (16 * h);           // scale bytes of sub-blocks 4A+2h, 4A+2h+1
+        uint32_t plo_[2], phi_[2];                       // their value tables
+        q2k_tables(sw, d, dmin, plo_, phi_);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {           // two sub-blocks of 16 values
-            uint32_t plo, phi;
-            lut((sw >> (8 * half)) & 0xffu, plo, phi);
+            const uint32_t plo = plo_[half], phi = phi_[half];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * half + cc;

@@ -121,6 +121,37 @@ __device__ __forceinline__ uint2 word_scaled(uint32_t u, pair_t dl2, pair_t nbia
     return make_uint2(f2h2(a), f2h2(b));
 }
 
+// The fp16 value tables of two Q2_K sub-blocks whose scale bytes are the
+// low two bytes of sw (scale = low nibble, min = high nibble): entry q of
+// sub-block k is RN_f16(fma(d * sc_k, q, -(dmin * m_k))), q = 0..3 -- the
+// f32 operations of the value formula, each rounded once, then the fp16
+// rounding -- held byte-planar (plo[k]: the low bytes of entries 0..3,
+// phi[k]: the high bytes) so that byte permutes select entries.  Both
+// sub-blocks go through the same operations on f32 pairs.
+__device__ __forceinline__ uint32_t h2_of(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void q2k_tables(uint32_t sw, float d, float dmin, uint32_t (&plo)[2],
+                                           uint32_t (&phi)[2]) {
+    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+    const uint32_t scw = sw & 0x0F0Fu, mw = (sw >> 4) & 0x0F0Fu;
+    const pair_t sc2 = fadd2(pk2(bias_float<0>(scw), bias_float<1>(scw)), nbias);   // exact
+    const pair_t m2 = fadd2(pk2(bias_float<0>(mw), bias_float<1>(mw)), nbias);
+    const pair_t dl2 = fmul2(pk2(d, d), sc2);
+    const pair_t nml2 = fmul2(pk2(-dmin, -dmin), m2);      // = -(dmin * m): rounding is sign-symmetric
+    float x[4], y[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpk2(ffma2(dl2, pk2(static_cast<float>(q), static_cast<float>(q)), nml2), x[q], y[q]);
+    const uint32_t a01 = h2_of(x[0], x[1]), a23 = h2_of(x[2], x[3]);
+    const uint32_t b01 = h2_of(y[0], y[1]), b23 = h2_of(y[2], y[3]);
+    plo[0] = __byte_perm(a01, a23, 0x6420);
+    phi[0] = __byte_perm(a01, a23, 0x7531);
+    plo[1] = __byte_perm(b01, b23, 0x6420);
+    phi[1] = __byte_perm(b01, b23, 0x7531);
+}
+
 // Small integer (< 2^23) -> float, exactly.
 __device__ __forceinline__ float u2f_exact(uint32_t v) {
     return __fsub_rn(__uint_as_float(0x4B000000u | v), 8388608.0f);
