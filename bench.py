@@ -212,15 +212,10 @@ class Layer:
         """The step's launches as (block type, [projection indices]): with
         grouping, each run of consecutive projections of one type is one
         qp_prefill_gemm_group launch; without, one launch per projection."""
-        out = []
-        for i, (name, _, _, _, qt) in enumerate(self.wl["projections"]):
-            if self.only and name != self.only:
-                continue
-            if grouped and out and out[-1][0] == qt and len(out[-1][1]) < 8:
-                out[-1][1].append(i)
-            else:
-                out.append((qt, [i]))
-        return out
+        if grouped and not self.only:
+            return workloads.type_runs(self.wl["projections"])
+        return [(qt, [i]) for i, (name, _, _, _, qt) in enumerate(self.wl["projections"])
+                if not self.only or name == self.only]
 
 
 def run_layer(qp, layer, stream, events=None, mode="fused", chunk=None, X=None, Y=None, grouped=True):

@@ -66,6 +66,13 @@ def lib():
         l.qpo_dequant_f16.argtypes = [ctypes.c_int, u8p, i64, i64, u8p]
         l.qpo_gemm_f64.argtypes = [u8p, u8p, i64, i64, i64, u8p, i64, u8p, u8p]
         l.qpo_num_threads.restype = ctypes.c_int
+        l.qpo_set_num_threads.argtypes = [ctypes.c_int]
+        # one thread per core this process may run on (the affinity mask, which
+        # a container or a job scheduler may set below the machine's count)
+        try:
+            l.qpo_set_num_threads(len(os.sched_getaffinity(0)))
+        except (AttributeError, OSError):
+            pass
         _lib = l
     return _lib
 

@@ -78,6 +78,9 @@ void qpo_gemm_f64(const uint16_t *X, const float *W, int64_t T, int64_t out, int
 
 /* Number of threads an OpenMP region of this library runs with. */
 int qpo_num_threads(void);
+/* Sets that number (n >= 1); the results do not depend on it: every output
+ * value is computed by one thread in a fixed order. */
+void qpo_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

@@ -41,6 +41,7 @@ def lib():
         l.synth_key.argtypes = [u64, u64]
         l.synth_key.restype = u64
         l.synth_blocks.argtypes = [ctypes.c_int, u64, i64, vp]
+        l.synth_blocks_anybits.argtypes = [ctypes.c_int, u64, i64, vp]
         l.synth_normal_f16.argtypes = [u64, i64, vp]
         l.synth_bytes.argtypes = [u64, i64, vp]
         _lib = l
@@ -62,6 +63,17 @@ def blocks(qtype, rows, cols, seed, tensor=0):
     nb = -(-cols // qk)
     out = np.empty((rows, nb * bb), np.uint8)
     lib().synth_blocks(qtype, key(seed, tensor), rows * nb, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def blocks_anybits(qtype, rows, cols, seed, tensor=0):
+    """As ``blocks``, but every quant, scale and min byte is a uniform random
+    byte (all bit patterns of every field, int8 -128 included); the fp16 d and
+    dmin fields are drawn as in ``blocks``, so every weight stays finite."""
+    qk, bb = BLOCK[qtype]
+    nb = -(-cols // qk)
+    out = np.empty((rows, nb * bb), np.uint8)
+    lib().synth_blocks_anybits(qtype, key(seed, tensor), rows * nb, out.ctypes.data_as(ctypes.c_void_p))
     return out
 
 

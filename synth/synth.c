@@ -127,6 +127,42 @@ void synth_blocks(int type, uint64_t key, int64_t nblocks, uint8_t *out) {
     }
 }
 
+/* Blocks whose quant, scale and min bytes are all uniform random bytes, so
+ * every bit pattern of every field occurs (int8 q = -128 in Q8_0, int8 scale
+ * = -128 in Q6_K, 6-bit scales and mins with their top bits set, ...), while
+ * the fp16 d and dmin fields are drawn as in synth_blocks, which keeps every
+ * weight finite.  F16 blocks are drawn as in synth_blocks. */
+void synth_blocks_anybits(int type, uint64_t key, int64_t nblocks, uint8_t *out) {
+    if (type == 1) {
+        synth_blocks(type, key, nblocks, out);
+        return;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblocks; ++b) {
+        const uint64_t i0 = (uint64_t)b * STRIDE;
+        if (type == 8) {                         /* Q8_0: d | q[32] */
+            uint8_t *p = out + b * 34;
+            fill_bytes(key, i0 + 2, p + 2, 32);
+            put16(p, scale_sample(draw(key, i0)));
+        } else if (type == 12 || type == 13) {   /* Q4_K, Q5_K: d | dmin | ... */
+            const int bb = type == 12 ? 144 : 176;
+            uint8_t *p = out + b * bb;
+            fill_bytes(key, i0 + 2, p + 4, bb - 4);
+            put16(p + 0, scale_sample(draw(key, i0)));
+            put16(p + 2, scale_sample(draw(key, i0 + 1)));
+        } else if (type == 10) {                 /* Q2_K: ... | d | dmin */
+            uint8_t *p = out + b * 84;
+            fill_bytes(key, i0 + 2, p, 80);
+            put16(p + 80, scale_sample(draw(key, i0)));
+            put16(p + 82, scale_sample(draw(key, i0 + 1)));
+        } else if (type == 14) {                 /* Q6_K: ql | qh | scales | d */
+            uint8_t *p = out + b * 210;
+            fill_bytes(key, i0 + 2, p, 208);
+            put16(p + 208, scale_sample(draw(key, i0)));
+        }
+    }
+}
+
 /* n standard-normal fp16 values (Box-Muller, one value per draw: the upper 32
  * bits give u1 in (0,1], the lower 32 bits u2 in [0,1)). */
 void synth_normal_f16(uint64_t key, int64_t n, uint16_t *out) {

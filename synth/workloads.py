@@ -41,6 +41,20 @@ WORKLOADS = {
 DEQUANT_SWEEP = [("Q4_K", Q4_K, 4096, 4096), ("Q4_K", Q4_K, 37, 1000)]
 
 
+def type_runs(projections, max_group=8):
+    """How a layer is issued: each run of consecutive projections of one
+    block type (at most max_group) is one grouped launch.  Returns
+    [(type, [projection indices])]."""
+    out = []
+    for i, p in enumerate(projections):
+        qt = p[4]
+        if out and out[-1][0] == qt and len(out[-1][1]) < max_group:
+            out[-1][1].append(i)
+        else:
+            out.append((qt, [i]))
+    return out
+
+
 def input_dims(wl):
     d = wl["dims"]
     return {"h": d["hidden"], "o": d["hidden"], "f": d["ffn"]}

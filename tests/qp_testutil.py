@@ -49,3 +49,35 @@ def assert_gemm_within_tolerance(Y, Yref, A, what=""):
     assert rel <= 1e-3, "%s: relative Frobenius error %.3g > 1e-3" % (what, rel)
     assert ratio <= 1.0, "%s: elementwise error reaches %.3g of the 4e-3*sum|x||w| bound" % (what, ratio)
     return rel, ratio
+
+
+class GemmErrorTally:
+    """The projection's acceptance bar over an output checked piece by piece
+    (row blocks): the relative Frobenius error of the whole, and the worst
+    elementwise |y - y_ref| / (4e-3 * sum_k |x||w|)."""
+
+    def __init__(self, what=""):
+        self.what = what
+        self.se = 0.0
+        self.sr = 0.0
+        self.worst = 0.0
+        self.n = 0
+
+    def add(self, Y, Yref, A):
+        Y = np.asarray(Y, np.float64)
+        assert np.isfinite(Y).all(), "%s: non-finite output" % self.what
+        err = Y - Yref
+        self.se += float(np.sum(err * err))
+        self.sr += float(np.sum(Yref * Yref))
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(A > 0, np.abs(err) / (4e-3 * A), np.where(err == 0, 0.0, np.inf))
+        if ratio.size:
+            self.worst = max(self.worst, float(ratio.max()))
+        self.n += Y.size
+
+    def check(self):
+        rel = (self.se / self.sr) ** 0.5 if self.sr > 0 else (0.0 if self.se == 0 else float("inf"))
+        assert self.n > 0
+        assert rel <= 1e-3, "%s: relative Frobenius error %.3g > 1e-3" % (self.what, rel)
+        assert self.worst <= 1.0, "%s: elementwise error reaches %.3g of the bound" % (self.what, self.worst)
+        return rel, self.worst

@@ -54,3 +54,25 @@ def test_normal_moments():
     x = synth.normal_f16((1 << 20,), seed=3).astype(np.float64)
     assert abs(x.mean()) < 5e-3 and abs(x.std() - 1) < 5e-3
     assert np.all(np.isfinite(x))
+
+
+def test_anybits_blocks_cover_every_field_pattern():
+    """blocks_anybits: every quant/scale byte value occurs (int8 -128 included),
+    while d and dmin are drawn as for blocks (finite, U(1e-3, 1e-2) on the fp16
+    grid)."""
+    d_offsets = {synth.Q8_0: [0], synth.Q4_K: [0, 2], synth.Q5_K: [0, 2], synth.Q2_K: [80, 82],
+                 synth.Q6_K: [208]}
+    for qtype, offs in d_offsets.items():
+        bb = synth.BLOCK[qtype][1]
+        w = synth.blocks_anybits(qtype, 64, 2048, seed=11, tensor=qtype).reshape(-1, bb)
+        field = np.ones(bb, bool)
+        for o in offs:
+            field[o:o + 2] = False
+            d = w[:, o:o + 2].copy().view(np.float16).astype(np.float64).ravel()
+            assert d.min() >= 1e-3 * (1 - 2 ** -11) and d.max() <= 1e-2 * (1 + 2 ** -11)
+        counts = np.bincount(w[:, field].ravel(), minlength=256)
+        assert counts.min() > 0.5 * counts.mean(), qtype
+    s = synth.blocks_anybits(synth.Q6_K, 64, 2048, seed=11, tensor=14).reshape(-1, 210)[:, 192:208]
+    assert (s.view(np.int8) == -128).any()
+    f = synth.blocks_anybits(synth.F16, 8, 64, seed=1, tensor=1)
+    assert np.array_equal(f, synth.blocks(synth.F16, 8, 64, seed=1, tensor=1))
