@@ -258,14 +258,44 @@ def time_layer(qp, layer, stream, steps, warmup, mode="fused", chunk=None):
 
 def bench_dequant(qp, stream, device, launches=64, only=None):
     """Standalone dequant throughput: GB/s of quantized bytes read + output
-    bytes written.  Launches run back to back over rotating input/output
-    buffer sets whose total is at least 4x the L2 size, so every launch finds
-    its data in HBM; one CUDA-event pair brackets `launches` launches."""
+    bytes written.  `launches` launches run back to back over rotating
+    input/output buffer sets whose total is at least 4x the L2 size, so every
+    launch finds its data in HBM.  They are captured once in a CUDA graph and
+    the replay is timed with one CUDA-event pair (`gbs`, `us`: the device
+    time per launch without the host's launch overhead); the same launches
+    made eagerly from Python are timed beside it (`eager_gbs`).  Reference:
+    a device-to-device copy moving the same bytes (half read, half written)
+    over the same rotating buffers, also replayed from a graph."""
     import torch
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     cases = [("Q4_K", qp.Q4_K, 4096, 4096, 12), ("Q8_0", qp.Q8_0, 4096, 4096, 13),
              ("Q2_K", qp.Q2_K, 4096, 4096, 14), ("Q6_K", qp.Q6_K, 4096, 12288, 15),
              ("Q5_K", qp.Q5_K, 4096, 4096, 16), ("F16", qp.F16, 4096, 4096, 17)]
+    side = torch.cuda.Stream(device)
+
+    def timed(fn, graph):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if graph is None:
+            for i in range(launches):
+                fn(i, stream)
+        else:
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / launches
+
+    def captured(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(launches):
+                    fn(i, side)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
     out = {}
     for name, qt, rows, cols, tid in cases:
         if only and not any(o.startswith(name) for o in only):
@@ -280,32 +310,33 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
             ws = [w0.clone() for _ in range(nsets)]
             ys = [torch.empty((rows, cols), dtype=torch.float16 if f16 else torch.float32, device=device)
                   for _ in range(nsets)]
-            fn = qp.qp_dequant_f16 if f16 else qp.qp_dequant_f32
+            deq = qp.qp_dequant_f16 if f16 else qp.qp_dequant_f32
+
+            def fn(i, st):
+                deq(qt, ws[i % nsets], rows, cols, ys[i % nsets], st)
+
             for i in range(nsets):
-                fn(qt, ws[i], rows, cols, ys[i], stream)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for i in range(launches):
-                fn(qt, ws[i % nsets], rows, cols, ys[i % nsets], stream)
-            e1.record(stream)
-            e1.synchronize()
-            ms = e0.elapsed_time(e1) / launches
-            # reference: a device-to-device copy moving the same bytes (half read,
-            # half written) over the same rotating buffers
+                fn(i, stream)
+            ms_eager = timed(fn, None)
+            g = captured(fn)
+            ms = timed(fn, g)
+            del g
             srcs = [y.view(torch.uint8).view(-1)[: nbytes // 2] for y in ys]
             dsts = [torch.empty(nbytes // 2, dtype=torch.uint8, device=device) for _ in range(nsets)]
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+            def cp(i, st):
+                with torch.cuda.stream(st):
+                    dsts[i % nsets].copy_(srcs[(i + 1) % nsets])
+
             for i in range(nsets):
-                dsts[i][: nbytes // 2].copy_(srcs[(i + 1) % nsets])
-            c0.record(stream)
-            for i in range(launches):
-                dsts[i % nsets][: nbytes // 2].copy_(srcs[(i + 1) % nsets])
-            c1.record(stream)
-            c1.synchronize()
-            copy_gbs = round(nbytes / (c0.elapsed_time(c1) / launches / 1e3) / 1e9, 1)
+                cp(i, stream)
+            gc = captured(cp)
+            copy_ms = timed(cp, gc)
+            del gc
             out["%s_%dx%d_%s" % (name, rows, cols, "f16" if f16 else "f32")] = {
                 "gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2), "bytes": nbytes,
-                "buffer_sets": nsets, "same_bytes_copy_gbs": copy_gbs}
+                "eager_gbs": round(nbytes / (ms_eager / 1e3) / 1e9, 1), "buffer_sets": nsets,
+                "same_bytes_copy_gbs": round(nbytes / (copy_ms / 1e3) / 1e9, 1)}
             del ws, ys, srcs, dsts
     qp.qp_check(stream)
     return out

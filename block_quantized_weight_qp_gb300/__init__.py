@@ -24,6 +24,7 @@ QP_ERR_CUDA = 4
 QP_ERR_TIMEOUT = 5
 QP_ERR_MISALIGNED = 6
 QP_ERR_NO_DEVICE = 7
+QP_ERR_PAIR_ALLOC = 8
 
 # Every symbol include/qp.h declares.
 EXPORTS = ("qp_status_str", "qp_block_info", "qp_row_bytes", "qp_dequant_f32", "qp_dequant_f16",

@@ -20,10 +20,11 @@ namespace {
 // Latched device-side errors (bit flags, see qp_internal.h).
 __device__ uint32_t g_qp_error;
 
-constexpr int kMaxDevices = 64;
+using qp::kMaxDevices;
 
 struct DeviceInfo {
     bool ready = false;
+    int dev = 0;
     int num_sms = 0;
     uint32_t *err = nullptr;  // device address of g_qp_error on this device
 };
@@ -78,12 +79,17 @@ qp_status device_info(DeviceInfo **out) {
             }
             g_encode = fn;
         }
+        d.dev = dev;
         d.num_sms = sms;
         d.err = static_cast<uint32_t *>(addr);
         d.ready = true;
     }
     *out = &d;
     return QP_OK;
+}
+
+qp::LaunchEnv env_of(const DeviceInfo *d) {
+    return qp::LaunchEnv{d->dev, d->num_sms, d->err, g_wait_limit_ns.load(), g_encode};
 }
 
 int64_t qk_of(int t) { return t == qp::kF16 ? 1 : (t == qp::kQ8_0 ? 32 : 256); }
@@ -125,6 +131,7 @@ qp_status run_gemms(int type, const qp_gemm_desc *descs, int n, int64_t T, void 
         a[i].W = descs[i].W;
         a[i].X = descs[i].X;
         a[i].Y = descs[i].Y;
+        a[i].device = d->dev;
         a[i].num_sms = d->num_sms;
         a[i].err = d->err;
         a[i].wait_limit_ns = g_wait_limit_ns.load();
@@ -192,6 +199,7 @@ const char *qp_status_str(qp_status s) {
     case QP_ERR_TIMEOUT: return "device-side wait timed out";
     case QP_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case QP_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+    case QP_ERR_PAIR_ALLOC: return "the two CTAs of a pair got different tensor-memory allocations";
     default: return "unknown status";
     }
 }
@@ -215,8 +223,8 @@ qp_status qp_dequant_f32(int type, const void *blocks, int64_t rows, int64_t col
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    if (qp::launch_dequant_f32(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms,
-                               g_encode) != cudaSuccess) {
+    if (qp::launch_dequant_f32(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), env_of(d)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
@@ -230,8 +238,8 @@ qp_status qp_dequant_f16(int type, const void *blocks, int64_t rows, int64_t col
     DeviceInfo *d = nullptr;
     const qp_status s = device_info(&d);
     if (s != QP_OK) return s;
-    if (qp::launch_dequant_f16(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), d->num_sms,
-                               g_encode) != cudaSuccess) {
+    if (qp::launch_dequant_f16(type, blocks, rows, cols, out, static_cast<cudaStream_t>(stream), env_of(d)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
@@ -315,7 +323,7 @@ qp_status run_gemv(int type, const qp_gemm_desc *descs, int n, int64_t T, void *
     for (int i = 0; i < n; ++i)
         a[i] = qp::GemvArgs{descs[i].W, qp_row_bytes(type, descs[i].in_f), descs[i].out_f, descs[i].in_f, T,
                             descs[i].X, descs[i].Y};
-    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), d->num_sms) != cudaSuccess) {
+    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), d->dev, d->num_sms) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
@@ -394,7 +402,9 @@ qp_status qp_check(void *stream) {
     if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return QP_ERR_CUDA;
     if (word != 0) {
         if (cudaMemset(d->err, 0, sizeof(word)) != cudaSuccess) return QP_ERR_CUDA;
-        return QP_ERR_TIMEOUT;
+        // a pairing failure is the cause, not a consequence: the launch that
+        // met it ran none of its roles, so no wait of it could run out
+        return (word & qp::kErrPairAlloc) ? QP_ERR_PAIR_ALLOC : QP_ERR_TIMEOUT;
     }
     return QP_OK;
 }

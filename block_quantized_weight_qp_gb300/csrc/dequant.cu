@@ -2,31 +2,40 @@
 // dequantize-to-f32 step of "Qwen3.5 batched prefill has no f32 dequant for
 // IQ2_XXS, IQ3_S, IQ3_XXS, Q2_K", §Cause; the f16 copy built from it).
 //
-// HBM-bound.  Each lane decodes one run of 32 consecutive values per step of
-// a grid-stride loop: a whole 32-value sub-block of Q4_K, two 16-value
-// sub-blocks of Q2_K / Q6_K, or one Q8_0 block, so the per-run work (scale
-// unpacking, addresses, loop control) is paid once per 32 values.  A warp
-// covers four K-quant superblocks (or 32 Q8_0 blocks) per step and writes each
-// lane's run with 16-byte stores.  Block fields are read straight from
-// global memory with loads no wider than the block's alignment (Q4_K blocks
-// are 16-byte aligned, Q2_K 4-byte, Q6_K and Q8_0 2-byte; 2-byte aligned runs
-// are assembled from aligned words).  The (row, block) position of a lane's
-// run is divided out once and then stepped.
+// HBM-bound, and short: a 4096 x 4096 weight is read in a few microseconds,
+// so what limits it is how many bytes are in flight, not the decode.  One
+// persistent CTA per SM takes one contiguous stretch of the block array (the
+// stretches differ by at most one alignment unit of 1024 values, so the SMs
+// finish together).  A producer warp streams the stretch into a ring of
+// shared-memory stages with bulk copies (cp.async.bulk, completing on the
+// stage's mbarrier) as far ahead as the ring allows (90-160 KB of stages per
+// SM), so that HBM sees the whole stretch requested from the first
+// microsecond on.  Sixteen decode warps each take one
+// "warp step" of every stage: 32 runs of 32 consecutive values (four K-quant
+// superblocks, 32 Q8_0 blocks, or 1024 F16 values), one run per lane, decoded
+// from shared memory by the exact run decoders of qp_runs.cuh.
 //
 // Arithmetic (qp_decode.cuh): every field is widened exactly and each value
-// is one fma / mul with an exact product, i.e. one f32 rounding — the same
+// is one fma / mul with an exact product, i.e. one f32 rounding -- the same
 // bits as the value formula evaluated with separately rounded f32 operations
 // (the CPU oracle).  f16 output is round-to-nearest-even of that f32.
 //
-// Stores: where the output is a whole number of 32-value runs per row (cols
-// a multiple of the block size), a warp step's 32 runs are one contiguous
-// stretch of the output; the warp writes them into a shared-memory tile in
-// the 128-byte (f32) / 64-byte (f16) swizzled layout of a TMA box of 32 runs
-// and one lane stores the tile with a single TMA tensor store.  Otherwise
-// the runs go through padded shared memory and leave as 16-byte stores.
+// Stores: where every output row is a whole number of blocks, a warp step's
+// 32 runs are one contiguous stretch of the output; the warp writes them into
+// a shared-memory tile in the 128-byte (f32) / 64-byte (f16) swizzled layout
+// of a 32-run TMA box and one lane stores the tile with a TMA tensor store
+// (two tiles per warp, recycled once their store has read them).  Rows with a
+// partial last block take a guarded per-lane store path.
 //
 // Tail guard: a lane writes only columns < cols; the padding values of a
 // partial last block are decoded but never stored.
+//
+// Launched with programmatic stream serialization: the CTAs of a launch may
+// be scheduled while the previous kernel in the stream drains, and wait for
+// it (griddepcontrol.wait) before they touch global memory.
+//
+// Every wait is bounded; on expiry the kernel records an error bit, stops,
+// waits for the copies it issued, and returns.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -38,47 +47,67 @@
 #include "qp_internal.h"
 #include "qp_ptx.cuh"
 #include "qp_runs.cuh"
+#include "qp_sync.cuh"
 
 namespace qp {
 namespace {
 
 using namespace runs;
 
+// Per type: bytes per block (BB), 32-value runs per block (RPB), values per
+// block (QK) and warp steps per unit of the split between CTAs (ALIGN: the
+// smallest number of steps whose bytes are a multiple of 16, so that every
+// stretch and stage starts 16-byte aligned).  F16 weights are taken as
+// blocks of one run of 32 fp16 values.
+template <int TYPE> struct RFmt;
+template <> struct RFmt<kQ4_K> { static constexpr int BB = 144, RPB = 8, QK = 256, ALIGN = 1; };
+template <> struct RFmt<kQ5_K> { static constexpr int BB = 176, RPB = 8, QK = 256, ALIGN = 1; };
+template <> struct RFmt<kQ2_K> { static constexpr int BB = 84, RPB = 8, QK = 256, ALIGN = 1; };
+template <> struct RFmt<kQ6_K> { static constexpr int BB = 210, RPB = 8, QK = 256, ALIGN = 2; };
+template <> struct RFmt<kQ8_0> { static constexpr int BB = 34, RPB = 1, QK = 32, ALIGN = 1; };
+template <> struct RFmt<kF16> { static constexpr int BB = 64, RPB = 1, QK = 32, ALIGN = 1; };
 
-// ----------------------------------------------------------------- kernel --
+constexpr int RD_WARPS = 16;                        // decode warps per CTA
+constexpr int RD_THREADS = (RD_WARPS + 1) * 32;     // + the producer warp
+constexpr int SMEM_CAP = 232448;                    // shared memory a CTA may opt in to
 
-// Position of a lane's run: block index, its (row, block-in-row), stepped by
-// a grid stride whose (rows, blocks) split was divided out on the host.
-struct Cursor {
-    int64_t blk, row, kb;
-    __device__ __forceinline__ void step(int64_t dblk, int64_t drow, int64_t dkb, int64_t nb) {
-        blk += dblk;
-        row += drow;
-        kb += dkb;
-        if (kb >= nb) {
-            kb -= nb;
-            ++row;
-        }
-    }
+// Shared memory: the decode warps' output tiles (two 32-run boxes each,
+// 1024-byte aligned for the swizzle), the ring of ST stages of one chunk
+// (RD_WARPS warp steps) each, the stage barriers and two flags.  The ring
+// takes what the tiles leave (at most 16 stages): 90-100 KB per SM with f32
+// output, up to 160 KB with f16, so that a 4096 x 4096 weight's share of an
+// SM is in flight at once.
+template <int TYPE, typename OutT> struct RLayout {
+    using F = RFmt<TYPE>;
+    static constexpr int BPS = 32 / F::RPB;                     // blocks per warp step
+    static constexpr int STEP_BYTES = BPS * F::BB;
+    static constexpr int CHUNK_BYTES = RD_WARPS * STEP_BYTES;
+    static constexpr int RUN = 32 * static_cast<int>(sizeof(OutT));
+    static constexpr int TILE = 32 * RUN;
+    static constexpr int OFF_RING = RD_WARPS * 2 * TILE;
+    static constexpr int ST_FIT = (SMEM_CAP - 1024 - 16 - OFF_RING) / (CHUNK_BYTES + 16);
+    static constexpr int ST = ST_FIT < 16 ? ST_FIT : 16;
+    static constexpr int OFF_BAR = OFF_RING + ST * CHUNK_BYTES;
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * ST * 8;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+    static_assert(ST >= 2, "at least two ring stages");
+    static_assert((F::ALIGN * STEP_BYTES) % 16 == 0 && CHUNK_BYTES % 16 == 0, "stages start 16-byte aligned");
+    static_assert(SMEM <= SMEM_CAP, "shared memory per CTA");
 };
 
-// Blocks a warp covers per grid-stride step: four superblocks (8 runs each),
-// or 32 Q8_0 blocks (one run each) -- 1024 values either way.
-template <int TYPE> __host__ __device__ constexpr int blocks_per_warp() { return TYPE == kQ8_0 ? 32 : 4; }
-
-constexpr int WARPS = 8;                                       // per 256-thread block
-
-// Per-warp staging area: 32 runs, each run's bytes padded by 16 so that 16-byte
-// accesses of eight consecutive runs fall in eight different bank groups.
-template <typename OutT> struct Stage {
-    static constexpr int RUN = 32 * static_cast<int>(sizeof(OutT));   // bytes per run
-    static constexpr int PITCH = RUN + 16;
-    static constexpr int CHUNKS = 32 * RUN / 16;                      // 16-byte chunks per warp step
-    static constexpr int PER_RUN = RUN / 16;
+struct RingArgs {
+    const uint8_t *blocks;
+    int64_t nblocks;      // blocks of the tensor (F16: runs of 32 values, the last maybe partial)
+    int64_t in_bytes;     // bytes of the block array
+    int64_t steps;        // warp steps, ceil(nblocks / BPS)
+    int64_t units;        // split units, ceil(steps / ALIGN)
+    int64_t cols, nb;     // output row length, blocks per row (guarded path)
+    int64_t nvals;        // rows * cols
+    void *out;
+    uint32_t *err;
+    uint64_t limit_ns;
+    int use_tma;          // a warp step's 32 runs are one contiguous box of the output
 };
-
-template <typename OutT>
-__device__ __forceinline__ void put_run(uint8_t *stage, int lane, const pair_t (&y)[16]);
 
 // The lane's run as row `lane` of a swizzled TMA box tile: 16-byte chunk k
 // of the row at chunk position k ^ (lane % 8) (f32: 128-byte rows) or
@@ -112,162 +141,193 @@ __device__ __forceinline__ void put_run_swz<uint16_t>(uint32_t tile, int lane, c
                      : "memory");
 }
 
-template <>
-__device__ __forceinline__ void put_run<float>(uint8_t *stage, int lane, const pair_t (&y)[16]) {
-    uint8_t *p = stage + lane * Stage<float>::PITCH;
+// Values p0 .. p0 + n - 1 (n <= 32) of a decoded run to out[i0 ..].
+template <typename OutT>
+__device__ __forceinline__ void put_run_guarded(OutT *out, int64_t i0, int n, const pair_t (&y)[16]) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        float a, b, c, d;
-        unpk2(y[2 * k], a, b);
-        unpk2(y[2 * k + 1], c, d);
-        *reinterpret_cast<float4 *>(p + 16 * k) = make_float4(a, b, c, d);
+    for (int k = 0; k < 16; ++k) {
+        if constexpr (sizeof(OutT) == 4) {
+            float a, b;
+            unpk2(y[k], a, b);
+            if (2 * k < n) out[i0 + 2 * k] = a;
+            if (2 * k + 1 < n) out[i0 + 2 * k + 1] = b;
+        } else {
+            const uint32_t h = f2h2(y[k]);
+            if (2 * k < n) out[i0 + 2 * k] = static_cast<uint16_t>(h);
+            if (2 * k + 1 < n) out[i0 + 2 * k + 1] = static_cast<uint16_t>(h >> 16);
+        }
     }
 }
-
-template <>
-__device__ __forceinline__ void put_run<uint16_t>(uint8_t *stage, int lane, const pair_t (&y)[16]) {
-    uint8_t *p = stage + lane * Stage<uint16_t>::PITCH;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<uint4 *>(p + 16 * k) =
-            make_uint4(f2h2(y[4 * k]), f2h2(y[4 * k + 1]), f2h2(y[4 * k + 2]), f2h2(y[4 * k + 3]));
-}
-
-// tmo: the output as [rows * cols / 32 runs x 32 values], box 32 x 32,
-// used when use_tma (every run of every row whole: cols a multiple of the
-// block size).
-// Resident 256-thread CTAs per SM the register budget is cut for: three
-// (80 registers a thread) keeps the most bytes in flight -- measured against
-// two (the register use left alone) and four (heavy spills): Q4_K 4096^2 ->
-// f32 69% -> 73% of HBM.  Q5_K and Q6_K, whose runs carry the most raw
-// bytes, spill at 80 registers and keep two (Q6_K 4096 x 12288 -> f32: 84%
-// at two, 75% at three).
-template <int TYPE> struct MinBlocks { static constexpr int N = 3; };
-template <> struct MinBlocks<kQ5_K> { static constexpr int N = 2; };
-template <> struct MinBlocks<kQ6_K> { static constexpr int N = 2; };
 
 template <int TYPE, typename OutT>
-__global__ void __launch_bounds__(256, MinBlocks<TYPE>::N) dequant_kernel(const uint8_t *__restrict__ blocks, int64_t cols, int64_t nb,
-                                                      int64_t nblocks, int64_t drow, int64_t dkb,
-                                                      OutT *__restrict__ out, const __grid_constant__ CUtensorMap tmo,
-                                                      int use_tma) {
-    using S = Stage<OutT>;
+__global__ void __launch_bounds__(RD_THREADS, 1)
+    ring_dequant_kernel(const __grid_constant__ RingArgs a, const __grid_constant__ CUtensorMap tmo) {
+    using F = RFmt<TYPE>;
+    using L = RLayout<TYPE, OutT>;
     using Raw = typename RawOf<TYPE>::T;
-    constexpr int QK = TYPE == kQ8_0 ? 32 : 256;
-    constexpr int BB =
-        TYPE == kQ8_0 ? 34 : (TYPE == kQ4_K ? 144 : (TYPE == kQ5_K ? 176 : (TYPE == kQ2_K ? 84 : 210)));
-    constexpr int BPW = blocks_per_warp<TYPE>();
-    constexpr int RUNS_PER_BLOCK = 32 / BPW;                  // 8 (K-quants) or 1 (Q8_0)
-    // padded staging (32 runs x PITCH per warp), or two TMA box tiles per warp
-    constexpr int STAGE_BYTES = WARPS * 32 * S::PITCH > WARPS * 64 * S::RUN ? WARPS * 32 * S::PITCH : WARPS * 64 * S::RUN;
-    __shared__ __align__(16) uint8_t stage_all[STAGE_BYTES + 1024];
-    const int lane = threadIdx.x & 31;
-    uint8_t *const base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(stage_all) + 1023) & ~uintptr_t(1023));
-    uint8_t *stage = base + (threadIdx.x >> 5) * 32 * S::PITCH;
-    // TMA box tiles of this warp: 2 x 32 runs x RUN bytes, aligned to the swizzle span
-    const uint32_t tiles = smem_u32(base) + static_cast<uint32_t>((threadIdx.x >> 5) * 64 * S::RUN);
-    uint32_t nst = 0;                                     // TMA stores this warp has issued
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * WARPS;
-    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
-    const int t = TYPE == kQ8_0 ? 0 : (lane & 7);             // run within the superblock
-    Cursor c;
-    c.blk = w0 * BPW + lane / RUNS_PER_BLOCK;
-    c.row = c.blk / nb;
-    c.kb = c.blk - c.row * nb;
-    const int64_t dblk = warps * BPW;
-    const bool vec_ok = (cols & (16 / sizeof(OutT) - 1)) == 0;  // output rows keep 16-byte alignment
-    Raw raw;
-    if (c.blk < nblocks) raw.load(blocks + c.blk * BB, t);
-    while (__any_sync(0xffffffffu, c.blk < nblocks)) {
-        Cursor n = c;
-        n.step(dblk, drow, dkb, nb);
-        Raw next;
-        if (n.blk < nblocks) next.load(blocks + n.blk * BB, t);   // in flight while this step decodes
-        const bool valid = c.blk < nblocks;
-        pair_t y[16];
-        if (valid) raw.decode(t, y);
-        const int64_t col0 = c.kb * QK + 32 * t;
-        // Coalesced path: every run of the warp is whole and inside its row, and
-        // the runs of each 512-byte output piece are contiguous in memory.
-        bool whole = valid && vec_ok && col0 + 32 <= cols;
-        if constexpr (TYPE == kQ8_0) {
-            // every lane takes part in the shuffle (it must not sit behind a
-            // short-circuit): all 32 blocks in one row, consecutive
-            const int64_t kb_first = __shfl_sync(0xffffffffu, c.kb, 0);
-            whole = whole && (c.kb - lane == kb_first);
+    constexpr int BPS = L::BPS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR), *empty = full + L::ST;
+    const Stop stop{reinterpret_cast<volatile uint32_t *>(smem + L::OFF_FLAG), 0u};
+    volatile uint32_t *const drain_failed = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_FLAG + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::ST; ++s) {
+            mbar_init(&full[s], 1);           // the producer's arrive + the copy's bytes
+            mbar_init(&empty[s], RD_WARPS);   // every decode warp
         }
-        if (use_tma && __all_sync(0xffffffffu, whole)) {
-            // the warp's 32 runs are runs first .. first + 31 of the output
-            const int64_t first = __shfl_sync(0xffffffffu, c.blk, 0) * RUNS_PER_BLOCK;
-            const uint32_t tile = tiles + (nst & 1u) * 32u * S::RUN;
-            if (lane == 0) bulk_wait_group_read<1>();     // the tile's previous store has read it
-            __syncwarp();
-            put_run_swz<OutT>(tile, lane, y);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(first));
-                bulk_commit_group();
-            }
-            ++nst;
-        } else if (__all_sync(0xffffffffu, whole)) {
-            put_run<OutT>(stage, lane, y);
-            __syncwarp();
-            // piece k of the warp step: 32 chunks = 512 bytes, all from one block
-            // run group (K-quants: superblock (k*32)/(8*PER_RUN); Q8_0: one row)
-#pragma unroll
-            for (int k = 0; k < S::CHUNKS / 32; ++k) {
-                const int chunk = 32 * k + lane;
-                const int run = chunk / S::PER_RUN;
-                const int within = chunk % S::PER_RUN;
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + run * S::PITCH + 16 * within);
-                const int src = TYPE == kQ8_0 ? 0 : (run & ~7);    // a lane holding that run's block cursor
-                const int64_t row = __shfl_sync(0xffffffffu, c.row, src);
-                const int64_t kb0 = __shfl_sync(0xffffffffu, c.kb, src);
-                const int64_t col = kb0 * QK + (TYPE == kQ8_0 ? 32 * run : 32 * (run & 7));
-                __stcs(reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out + row * cols + col) + 16 * within),
-                       v);
-            }
-            __syncwarp();
-        } else if (valid && col0 < cols) {
-            // Guarded per-lane path (partial blocks, unaligned rows, row ends).
-            OutT *p = out + c.row * cols + col0;
-            if constexpr (sizeof(OutT) == 4) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float a, b;
-                    unpk2(y[k], a, b);
-                    if (col0 + 2 * k < cols) p[2 * k] = a;
-                    if (col0 + 2 * k + 1 < cols) p[2 * k + 1] = b;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint32_t h = f2h2(y[k]);
-                    if (col0 + 2 * k < cols) p[2 * k] = static_cast<uint16_t>(h);
-                    if (col0 + 2 * k + 1 < cols) p[2 * k + 1] = static_cast<uint16_t>(h >> 16);
-                }
-            }
-        }
-        raw = next;
-        c = n;
+        *stop.flag = 0u;
+        *drain_failed = 0u;
+        mbar_fence_init();
+        if (a.use_tma) prefetch_tensormap(&tmo);
     }
-    if (use_tma && lane == 0) bulk_wait_all();            // the stores are complete before the CTA exits
+    __syncthreads();
+    grid_dependency_wait();                   // the previous grid's memory operations are done
+
+    // this CTA's warp steps [s0, s1), in chunks of RD_WARPS steps
+    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.units / gridDim.x;
+    const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * a.units / gridDim.x;
+    const int64_t s0 = u0 * F::ALIGN;
+    const int64_t s1 = u1 * F::ALIGN < a.steps ? u1 * F::ALIGN : a.steps;
+    const int nchunks = s1 > s0 ? static_cast<int>((s1 - s0 + RD_WARPS - 1) / RD_WARPS) : 0;
+    uint8_t *const ring = smem + L::OFF_RING;
+
+    if (warp == RD_WARPS) {
+        // ------------------------------------------------------------ producer --
+        if (lane == 0) {
+            int stage = 0, armed = 0;
+            uint32_t phase = 0;
+            for (int i = 0; i < nchunks; ++i) {
+                if (!wait_phase_sleepy(&empty[stage], phase ^ 1u, 256, a.limit_ns, stop, a.err, kErrTimeoutRing))
+                    break;
+                const int64_t c0 = s0 + static_cast<int64_t>(i) * RD_WARPS;
+                const int64_t c1 = c0 + RD_WARPS < s1 ? c0 + RD_WARPS : s1;
+                const int64_t off = c0 * BPS * F::BB;
+                const int64_t end = c1 * BPS * F::BB < a.in_bytes ? c1 * BPS * F::BB : a.in_bytes;
+                const uint32_t bytes = static_cast<uint32_t>(end - off), b16 = bytes & ~15u;
+                uint8_t *dst = ring + stage * L::CHUNK_BYTES;
+                // the block array's last bytes past a multiple of 16 (only the
+                // tensor's last chunk has them): plain loads, published by the
+                // arrive below
+                for (uint32_t k = b16; k < bytes; ++k) dst[k] = a.blocks[off + k];
+                mbar_arrive_expect_tx(&full[stage], b16);
+                if (b16) bulk_load(dst, a.blocks + off, b16, &full[stage]);
+                ++armed;
+                advance(stage, phase, L::ST);
+            }
+            grid_launch_dependents();
+            if (!drain_ring(full, L::ST, armed, -1, a.limit_ns)) {
+                *drain_failed = 1u;
+                atomicOr(a.err, kErrTimeoutRing);
+            }
+        }
+    } else {
+        // -------------------------------------------------------------- decode --
+        OutT *const out = static_cast<OutT *>(a.out);
+        const uint32_t tiles = smem_u32(smem) + static_cast<uint32_t>(warp * 2 * L::TILE);
+        const int j = lane / F::RPB;                            // block of the warp step
+        const int t = F::RPB == 1 ? 0 : (lane % F::RPB);         // run within the block
+        int stage = 0;
+        uint32_t phase = 0, nst = 0;
+        for (int i = 0; i < nchunks; ++i) {
+            if (!wait_phase_warp(&full[stage], phase, a.limit_ns, stop, a.err, kErrTimeoutRing)) break;
+            const int64_t step = s0 + static_cast<int64_t>(i) * RD_WARPS + warp;
+            if (step < s1) {
+                const int64_t blk = step * BPS + j;
+                const bool valid = blk < a.nblocks;
+                const uint8_t *src = ring + stage * L::CHUNK_BYTES + (warp * BPS + j) * F::BB;
+                if constexpr (TYPE == kF16 && sizeof(OutT) == 2) {
+                    if (a.use_tma) {
+                        // fp16 weights to fp16: the run's 64 bytes move as they are
+                        const uint32_t tile = tiles + (nst & 1u) * static_cast<uint32_t>(L::TILE);
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        const uint32_t row = tile + static_cast<uint32_t>(lane * 64);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 v = valid ? Smem::u128(src + 16 * k) : make_uint4(0u, 0u, 0u, 0u);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             row + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) << 4)),
+                                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(step * 32));
+                            bulk_commit_group();
+                        }
+                        ++nst;
+                        if (valid && blk * 32 + 32 > a.nvals) {
+                            OutT *o = out + blk * 32;
+                            for (int64_t k = 0; k < a.nvals - blk * 32; ++k)
+                                o[k] = static_cast<OutT>(Smem::u16(src + 2 * k));
+                        }
+                        goto next_stage;
+                    }
+                }
+                pair_t y[16];
+                if (valid) {
+                    Raw raw;
+                    raw.template load<Smem>(src, t);
+                    raw.decode(t, y);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) y[k] = pk2(0.0f, 0.0f);
+                }
+                if (a.use_tma) {
+                    // box rows past the end of the output view are not written
+                    const uint32_t tile = tiles + (nst & 1u) * static_cast<uint32_t>(L::TILE);
+                    if (lane == 0) bulk_wait_group_read<1>();   // the tile's previous store has read it
+                    __syncwarp();
+                    put_run_swz<OutT>(tile, lane, y);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(step * 32));
+                        bulk_commit_group();
+                    }
+                    ++nst;
+                    if constexpr (TYPE == kF16) {
+                        // a last run of fewer than 32 values lies outside the view
+                        if (valid && blk * 32 + 32 > a.nvals)
+                            put_run_guarded<OutT>(out, blk * 32, static_cast<int>(a.nvals - blk * 32), y);
+                    }
+                } else if (valid) {
+                    if constexpr (TYPE == kF16) {
+                        const int64_t left = a.nvals - blk * 32;
+                        put_run_guarded<OutT>(out, blk * 32, left < 32 ? static_cast<int>(left) : 32, y);
+                    } else {
+                        const int64_t row = blk / a.nb;
+                        const int64_t col0 = (blk - row * a.nb) * F::QK + 32 * t;
+                        if (col0 < a.cols) {
+                            const int64_t left = a.cols - col0;
+                            put_run_guarded<OutT>(out, row * a.cols + col0, left < 32 ? static_cast<int>(left) : 32, y);
+                        }
+                    }
+                }
+            }
+        next_stage:
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            advance(stage, phase, L::ST);
+        }
+        if (lane == 0) bulk_wait_all();                       // the stores have completed
+    }
+    __syncthreads();
+    if (*drain_failed) pause_ns(200000ull);
 }
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The output as [rows * cols / 32 runs x 32 values] for TMA stores of 32-run
-// boxes, when every row is a whole number of blocks (so that a warp step's
-// runs are contiguous) and the run index fits the 32-bit coordinate.
-template <int TYPE, typename OutT>
-bool encode_out(void *encode_fn, int64_t rows, int64_t cols, OutT *out, CUtensorMap *map) {
-    const int64_t qk = TYPE == kQ8_0 ? 32 : 256;
-    if (!encode_fn || cols % qk != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0) return false;
-    const int64_t runs = rows * cols / 32;
-    if (runs > INT32_MAX) return false;
+// The output as [runs x 32 values] for TMA stores of 32-run boxes.
+template <typename OutT>
+bool encode_out(void *encode_fn, int64_t runs, OutT *out, CUtensorMap *map) {
+    if (!encode_fn || runs < 1 || runs > INT32_MAX || (reinterpret_cast<uintptr_t>(out) & 15u) != 0) return false;
     const cuuint64_t dims[2] = {32, static_cast<cuuint64_t>(runs)};
     const cuuint64_t strides[1] = {32 * sizeof(OutT)};
     const cuuint32_t box[2] = {32, 32};
@@ -280,88 +340,68 @@ bool encode_out(void *encode_fn, int64_t rows, int64_t cols, OutT *out, CUtensor
 }
 
 template <int TYPE, typename OutT>
-cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream, int num_sms,
-                   void *encode_fn) {
-    const int64_t qk = TYPE == kQ8_0 ? 32 : 256;
-    const int64_t nb = (cols + qk - 1) / qk;
-    const int64_t nblocks = rows * nb;
-    const int64_t nwarps = (nblocks + blocks_per_warp<TYPE>() - 1) / blocks_per_warp<TYPE>();
-    // one resident wave of 256-thread blocks at most
-    static std::atomic<int> cached{0};                 // queried once per kernel, then cached
-    int per_sm = cached.load();
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequant_kernel<TYPE, OutT>, 256, 0) !=
-                cudaSuccess ||
-            per_sm < 1) {
-            cudaGetLastError();
-            per_sm = 1;
-        }
-        cached.store(per_sm);
+cudaError_t launch(const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream,
+                   const LaunchEnv &env) {
+    using F = RFmt<TYPE>;
+    using L = RLayout<TYPE, OutT>;
+    RingArgs a;
+    a.blocks = static_cast<const uint8_t *>(blocks);
+    a.cols = cols;
+    a.nvals = rows * cols;
+    int64_t view_runs;                                    // whole runs the TMA view holds (0: no TMA)
+    if constexpr (TYPE == kF16) {
+        a.nb = cols;
+        a.nblocks = (a.nvals + 31) / 32;
+        a.in_bytes = 2 * a.nvals;
+        view_runs = a.nvals / 32;                         // a partial last run is stored by its lane
+    } else {
+        a.nb = (cols + F::QK - 1) / F::QK;
+        a.nblocks = rows * a.nb;
+        a.in_bytes = a.nblocks * F::BB;
+        view_runs = cols % F::QK == 0 ? a.nblocks * F::RPB : 0;
     }
-    const int64_t want = (nwarps + WARPS - 1) / WARPS;
-    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
-    const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    const int64_t dblk = static_cast<int64_t>(grid) * WARPS * blocks_per_warp<TYPE>();
+    a.steps = (a.nblocks + L::BPS - 1) / L::BPS;
+    a.units = (a.steps + F::ALIGN - 1) / F::ALIGN;
+    a.out = out;
+    a.err = env.err;
+    a.limit_ns = env.wait_limit_ns;
     CUtensorMap tmo;
-    const bool use_tma = encode_out<TYPE, OutT>(encode_fn, rows, cols, out, &tmo);
-    if (!use_tma) memset(&tmo, 0, sizeof(tmo));
-    dequant_kernel<TYPE, OutT><<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), cols, nb, nblocks,
-                                                         dblk / nb, dblk % nb, out, tmo, use_tma ? 1 : 0);
-    return cudaGetLastError();
-}
+    a.use_tma = view_runs > 0 && encode_out<OutT>(env.encode_fn, view_runs, out, &tmo) ? 1 : 0;
+    if (!a.use_tma) memset(&tmo, 0, sizeof(tmo));
 
-// F16 weights: each "block" is one fp16 value and rows carry no padding, so
-// the input and the output hold the same n values in the same order: a flat
-// conversion (exact widening to f32) or copy (f16), 8 values = one 16-byte
-// load per thread and step; a last partial group of 8 is done value by value.
-template <typename OutT>
-__global__ void __launch_bounds__(256) f16_weights_kernel(const uint16_t *__restrict__ in, int64_t n,
-                                                          OutT *__restrict__ out) {
-    const int64_t n8 = n / 8;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(in) + i);
-        if constexpr (sizeof(OutT) == 4) {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            float f[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                f[2 * k] = h2f(w[k]);
-                f[2 * k + 1] = h2f(w[k] >> 16);
-            }
-            float4 *o = reinterpret_cast<float4 *>(out) + 2 * i;
-            __stcs(o, make_float4(f[0], f[1], f[2], f[3]));
-            __stcs(o + 1, make_float4(f[4], f[5], f[6], f[7]));
-        } else {
-            __stcs(reinterpret_cast<uint4 *>(out) + i, v);
-        }
+    auto kern = ring_dequant_kernel<TYPE, OutT>;
+    static std::atomic<int> smem_set[kMaxDevices];        // the opt-in holds per device
+    if (!smem_set[env.device].load()) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+        if (e != cudaSuccess) return e;
+        smem_set[env.device].store(1);
     }
-    if (blockIdx.x == 0 && threadIdx.x < n - 8 * n8) {
-        const int64_t j = 8 * n8 + threadIdx.x;
-        if constexpr (sizeof(OutT) == 4) out[j] = h2f(in[j]);
-        else out[j] = in[j];
-    }
-}
-
-template <typename OutT>
-cudaError_t launch_f16(const uint16_t *in, int64_t n, OutT *out, cudaStream_t stream, int num_sms) {
-    const int64_t want = (n / 8 + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    f16_weights_kernel<OutT><<<grid, 256, 0, stream>>>(in, n, out);
+    const int64_t grid = a.units < env.num_sms ? a.units : env.num_sms;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(RD_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, tmo);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <typename OutT>
 cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, OutT *out, cudaStream_t stream,
-                     int num_sms, void *enc) {
+                     const LaunchEnv &env) {
     switch (type) {
-    case kQ8_0: return launch<kQ8_0>(blocks, rows, cols, out, stream, num_sms, enc);
-    case kQ2_K: return launch<kQ2_K>(blocks, rows, cols, out, stream, num_sms, enc);
-    case kQ4_K: return launch<kQ4_K>(blocks, rows, cols, out, stream, num_sms, enc);
-    case kQ5_K: return launch<kQ5_K>(blocks, rows, cols, out, stream, num_sms, enc);
-    case kQ6_K: return launch<kQ6_K>(blocks, rows, cols, out, stream, num_sms, enc);
-    case kF16: return launch_f16(static_cast<const uint16_t *>(blocks), rows * cols, out, stream, num_sms);
+    case kQ8_0: return launch<kQ8_0>(blocks, rows, cols, out, stream, env);
+    case kQ2_K: return launch<kQ2_K>(blocks, rows, cols, out, stream, env);
+    case kQ4_K: return launch<kQ4_K>(blocks, rows, cols, out, stream, env);
+    case kQ5_K: return launch<kQ5_K>(blocks, rows, cols, out, stream, env);
+    case kQ6_K: return launch<kQ6_K>(blocks, rows, cols, out, stream, env);
+    case kF16: return launch<kF16>(blocks, rows, cols, out, stream, env);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -369,13 +409,13 @@ cudaError_t dispatch(int type, const void *blocks, int64_t rows, int64_t cols, O
 }  // namespace
 
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
-                               cudaStream_t stream, int num_sms, void *encode_fn) {
-    return dispatch(type, blocks, rows, cols, out, stream, num_sms, encode_fn);
+                               cudaStream_t stream, const LaunchEnv &env) {
+    return dispatch(type, blocks, rows, cols, out, stream, env);
 }
 
 cudaError_t launch_dequant_f16(int type, const void *blocks, int64_t rows, int64_t cols, uint16_t *out,
-                               cudaStream_t stream, int num_sms, void *encode_fn) {
-    return dispatch(type, blocks, rows, cols, out, stream, num_sms, encode_fn);
+                               cudaStream_t stream, const LaunchEnv &env) {
+    return dispatch(type, blocks, rows, cols, out, stream, env);
 }
 
 }  // namespace qp

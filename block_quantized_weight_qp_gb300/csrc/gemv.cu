@@ -281,18 +281,20 @@ __global__ void __launch_bounds__(NW * 32, QP_GEMV_MINB) gemv_kernel(const __gri
 // 8-row block; each CTA's ring runs on from one block into its next, across
 // the projections of the launch.
 template <int TYPE, int NW>
-cudaError_t launch_nw(const GemvArgs *a, int n, cudaStream_t stream, int num_sms) {
+cudaError_t launch_nw(const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms) {
     auto kern = gemv_kernel<TYPE, NW>;
     constexpr int smem = gemv_smem<TYPE, NW>();
-    static std::atomic<int> per_sm{0};
-    int k = per_sm.load();
+    // the shared-memory opt-in and the occupancy query hold for one device:
+    // done once per device and instantiation
+    static std::atomic<int> per_sm[kMaxDevices];
+    int k = per_sm[device].load();
     if (k == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, NW * 32, smem) != cudaSuccess || k < 1) {
             cudaGetLastError();
             k = 1;
         }
-        per_sm.store(k);
+        per_sm[device].store(k);
     }
     GemvParams gp;
     int64_t blocks = 0;
@@ -311,15 +313,15 @@ cudaError_t launch_nw(const GemvArgs *a, int n, cudaStream_t stream, int num_sms
 
 }  // namespace
 
-cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int num_sms) {
+cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms) {
     if (n < 1 || n > kMaxGroup) return cudaErrorInvalidValue;
     switch (type) {
-    case kQ8_0: return launch_nw<kQ8_0, QP_GEMV_NW>(a, n, stream, num_sms);
-    case kQ2_K: return launch_nw<kQ2_K, QP_GEMV_NW>(a, n, stream, num_sms);
-    case kQ4_K: return launch_nw<kQ4_K, QP_GEMV_NW>(a, n, stream, num_sms);
-    case kQ5_K: return launch_nw<kQ5_K, QP_GEMV_NW>(a, n, stream, num_sms);
-    case kQ6_K: return launch_nw<kQ6_K, QP_GEMV_NW>(a, n, stream, num_sms);
-    case kF16: return launch_nw<kF16, QP_GEMV_NW>(a, n, stream, num_sms);
+    case kQ8_0: return launch_nw<kQ8_0, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kQ2_K: return launch_nw<kQ2_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kQ4_K: return launch_nw<kQ4_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kQ5_K: return launch_nw<kQ5_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kQ6_K: return launch_nw<kQ6_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kF16: return launch_nw<kF16, QP_GEMV_NW>(a, n, stream, device, num_sms);
     default: return cudaErrorInvalidValue;
     }
 }

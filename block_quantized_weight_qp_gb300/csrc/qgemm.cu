@@ -42,8 +42,12 @@
 // fused and cached modes give bitwise equal Y.
 //
 // Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
-// latches an error bit in the device error word, makes every role stop,
-// lets copies in flight land, frees its TMEM and returns.
+// latches an error bit in the device error word and makes every role stop (in
+// a CTA pair, the partner's roles too).  Before shared memory and TMEM are
+// released it waits, again with a bound, for what it issued itself: each
+// producer for the copies it started, the MMA thread for its MMAs.  Only if
+// one of those waits runs out, or where a copy's completion is signalled to
+// the other CTA of a pair, does the CTA fall back to a fixed pause.
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
@@ -55,6 +59,7 @@
 #include "qp_decode.cuh"
 #include "qp_internal.h"
 #include "qp_ptx.cuh"
+#include "qp_sync.cuh"
 
 namespace qp {
 namespace {
@@ -119,7 +124,8 @@ template <int TYPE> struct Cfg {
 struct Shared {
     uint64_t *fullx, *emptyx, *fullw, *emptyw, *qfull, *qempty, *accfull, *accempty, *done;
     uint32_t *tmem_base;
-    volatile uint32_t *abort_flag;
+    Stop stop;
+    volatile uint32_t *drain_failed;     // a wait for the CTA's own copies or MMAs ran out
 };
 
 // A launch runs up to MAX_GROUPS projections of one weight type over the
@@ -153,62 +159,6 @@ __device__ __forceinline__ TileLoc locate(const GroupParams &p, int tile) {
     }
     const int t = tile - base;
     return {g, (t % p.m_tiles[g]) * BM, (t / p.m_tiles[g]) * BN};
-}
-
-// Bounded wait on a barrier phase.  Returns false (and stops every role of
-// this CTA) when the limit passes or another role already gave up.
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
-                                           volatile uint32_t *abort_flag, uint32_t *err, uint32_t errbit) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                *abort_flag = 1u;
-                atomicOr(err, errbit);
-                return false;
-            }
-        }
-    }
-}
-
-// The same for waits that are not on the critical path (the epilogue waiting
-// for a whole tile's mainloop, the producer running ahead of the MMA): back
-// off with nanosleep between polls so the waiting warp does not take issue
-// slots from the decode warps sharing its SM sub-partition.
-__device__ __forceinline__ bool wait_phase_sleepy(uint64_t *bar, uint32_t parity, uint32_t max_sleep_ns,
-                                                  uint64_t limit_ns, volatile uint32_t *abort_flag, uint32_t *err,
-                                                  uint32_t errbit) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    uint32_t sleep_ns = 32;
-    for (;;) {
-        __nanosleep(sleep_ns);
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            *abort_flag = 1u;
-            atomicOr(err, errbit);
-            return false;
-        }
-        if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
-    }
-}
-
-// Warp-uniform form for roles whose every lane reads the guarded data.
-__device__ __forceinline__ bool wait_phase_warp(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
-                                                volatile uint32_t *abort_flag, uint32_t *err, uint32_t errbit) {
-    const bool ok = wait_phase(bar, parity, limit_ns, abort_flag, err, errbit);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void advance(int &stage, uint32_t &phase, int n) {
-    if (++stage == n) {
-        stage = 0;
-        phase ^= 1u;
-    }
 }
 
 // --------------------------------------------------------- fused decoding --
@@ -497,7 +447,7 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
     }
 #define QP_DEQUANT_ATOM(A)                                                                                     \
     {                                                                                                          \
-        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) \
+        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.stop, err, kErrTimeoutDequant)) \
             return false;                                                                                      \
         dec.template atom<A>(row, hs16, p, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
         fence_proxy_async_smem();                                                                              \
@@ -525,7 +475,7 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams
     for (int tile = first; tile < gp.num_tiles; tile += stride) {
         const int nk = gp.nk[locate(gp, tile).g];
         for (int kb = 0; kb < nk; ++kb) {
-            if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant)) return;
+            if (!wait_phase_warp(&sh.qfull[qs], qphase, limit_ns, sh.stop, err, kErrTimeoutDequant)) return;
             const uint8_t *row = qslots + qs * Q_SLOT_BYTES + r * QFmt<TYPE>::BOX;
             const int rem = (kb * QFmt<TYPE>::SB_BYTES) & 15;
             const uint32_t hs16 = (rem & 2) ? 16u : 0u;
@@ -571,7 +521,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     sh.accempty = sh.accfull + 2;
     sh.done = sh.accfull + 4;
     sh.tmem_base = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-    sh.abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4);
+    sh.stop = Stop{reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4), 0u};
+    sh.drain_failed = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -595,7 +546,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
             mbar_init(&sh.accempty[a], 4);
         }
         mbar_init(sh.done, 1);
-        *sh.abort_flag = 0u;
+        *sh.stop.flag = 0u;
+        *sh.drain_failed = 0u;
         mbar_fence_init();
         for (int g = 0; g < gp.n_groups; ++g) {
             prefetch_tensormap(&gp.tmX[g]);
@@ -618,7 +570,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
-            int stage = 0, qs = 0, loads = 0;
+            int stage = 0, qs = 0, loads = 0, qloads = 0;
             uint32_t phase = 0, qphase = 0;
             for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
                 const TileLoc L = locate(gp, tile);
@@ -626,12 +578,13 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                 const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
                 for (int kb = 0; kb < nk; ++kb) {
                     if constexpr (C::FUSED) {
-                        if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
+                        if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.stop, err,
                                                kErrTimeoutProducer))
                             goto producer_done;
                         const int start = kb * QFmt<TYPE>::SB_BYTES;
                         mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
                         tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
+                        ++qloads;
                         advance(qs, qphase, C::QST);
                     }
 #pragma unroll 1
@@ -639,8 +592,8 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                         // fused: the decode warps share this sub-partition, so poll gently;
                         // cached: the producer feeds the MMA directly, so poll hot
                         if (!(C::FUSED ? wait_phase_sleepy(&sh.emptyx[stage], phase ^ 1u, 256, limit_ns,
-                                                           sh.abort_flag, err, kErrTimeoutProducer)
-                                       : wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,
+                                                           sh.stop, err, kErrTimeoutProducer)
+                                       : wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.stop, err,
                                                     kErrTimeoutProducer)))
                             goto producer_done;
                         const int k0 = kb * SB + a * BK;
@@ -656,7 +609,14 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            // every copy issued has landed before shared memory can be released
+            bool drained = drain_ring(sh.fullx, XS, loads, inject_stall, limit_ns);
+            if constexpr (C::FUSED) drained = drain_ring(sh.qfull, C::QST, qloads, -1, limit_ns) && drained;
+            if (!drained) {
+                *sh.drain_failed = 1u;
+                atomicOr(err, kErrTimeoutProducer);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -666,17 +626,17 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
             uint32_t phase = 0, wphase = 0, acc_phase = 0;
             for (int tile = blockIdx.x; tile < gp.num_tiles; tile += gridDim.x) {
                 const int nk = gp.nk[locate(gp, tile).g];
-                if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.stop, err, kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
-                        if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                        if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.stop, err, kErrTimeoutMma))
                             goto mma_done;
                         if constexpr (C::FUSED) {
-                            if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                            if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma))
                                 goto mma_done;
                         }
                         tc_fence_after();
@@ -700,7 +660,10 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         mma_done:
             // Everything issued has completed before TMEM is released.
             mma_commit(sh.done);
-            wait_phase(sh.done, 0, limit_ns, sh.abort_flag, err, kErrTimeoutMma);
+            if (!wait_drain(sh.done, 0, limit_ns)) {
+                *sh.drain_failed = 1u;
+                atomicOr(err, kErrTimeoutMma);
+            }
         }
         __syncwarp();
     } else if (warp < 6) {
@@ -714,7 +677,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
             const int m0 = L.m0, n0 = L.n0, out_f = gp.out_f[L.g];
             float *const Y = gp.Y[L.g];
             if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
-                                                           sh.abort_flag, err, kErrTimeoutEpilogue)))
+                                                           sh.stop, err, kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const int o = m0 + quarter * 32 + lane;
@@ -749,13 +712,7 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
     }
 
     __syncthreads();
-    if (*sh.abort_flag) {
-        // A role gave up: give TMA copies already issued time to land before
-        // this CTA's shared memory is released.
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
-        }
-    }
+    if (*sh.drain_failed) pause_ns(200000ull);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -839,7 +796,9 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
     uint64_t *full = bars, *empty = bars + P::ST, *accfull = bars + 2 * P::ST, *accempty = accfull + 2,
              *done = accfull + 4;
     uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + P::OFF_MISC);
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + P::OFF_MISC + 4);
+    volatile uint32_t *const flag = reinterpret_cast<volatile uint32_t *>(smem + P::OFF_MISC + 4);
+    volatile uint32_t *const drain_failed = reinterpret_cast<volatile uint32_t *>(smem + P::OFF_MISC + 8);
+    const Stop stop{flag, mapa_shared(smem_u32(const_cast<uint32_t *>(flag)), rank ^ 1u)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -852,7 +811,8 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
             mbar_init(&accempty[a], 8);     // leader: four epilogue warps of each CTA
         }
         mbar_init(done, 1);
-        *abort_flag = 0u;
+        *flag = 0u;
+        *drain_failed = 0u;
         mbar_fence_init();
         for (int g = 0; g < gp.n_groups; ++g) {
             prefetch_tensormap(&gp.tmX[g]);
@@ -881,7 +841,7 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
                 const int m0 = 2 * L.m0 + 128 * static_cast<int>(rank), n0 = L.n0 + 128 * static_cast<int>(rank);
                 const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
                 for (int k = 0; k < gp.nk[L.g] * (SB / BK); ++k) {
-                    if (!wait_phase(&empty[stage], phase ^ 1u, limit_ns, abort_flag, err, kErrTimeoutProducer))
+                    if (!wait_phase(&empty[stage], phase ^ 1u, limit_ns, stop, err, kErrTimeoutProducer))
                         goto producer_done;
                     const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0u);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P::STAGE_BYTES);
@@ -893,7 +853,13 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
                     advance(stage, phase, P::ST);
                 }
             }
-        producer_done:;
+        producer_done:
+            // The leader's stage barriers count both CTAs' bytes: once every
+            // phase it armed has completed, every copy of both has landed.
+            if (rank == 0 && !drain_ring(full, P::ST, loads, inject_stall, limit_ns)) {
+                *drain_failed = 1u;
+                atomicOr(err, kErrTimeoutProducer);
+            }
         }
         __syncwarp();
     } else if (alloc_ok && warp == 1) {
@@ -903,12 +869,12 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
             uint32_t phase = 0, acc_phase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
-                if (!wait_phase(&accempty[acc], acc_phase ^ 1u, limit_ns, abort_flag, err, kErrTimeoutMma))
+                if (!wait_phase(&accempty[acc], acc_phase ^ 1u, limit_ns, stop, err, kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int k = 0; k < nks; ++k) {
-                    if (!wait_phase(&full[stage], phase, limit_ns, abort_flag, err, kErrTimeoutMma)) goto mma_done;
+                    if (!wait_phase(&full[stage], phase, limit_ns, stop, err, kErrTimeoutMma)) goto mma_done;
                     tc_fence_after();
                     uint8_t *st = stages + stage * P::STAGE_BYTES;
                     const uint64_t adesc = desc_sw128_kmajor(smem_u32(st));
@@ -923,8 +889,13 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
                 advance(acc, acc_phase, ACC);
             }
         mma_done:
+            // both CTAs' TMEM is written by these MMAs: they complete before
+            // the cluster barrier that precedes the deallocation
             mma_commit_pair_multicast(done, 0x1);
-            wait_phase(done, 0, limit_ns, abort_flag, err, kErrTimeoutMma);
+            if (!wait_drain(done, 0, limit_ns)) {
+                *drain_failed = 1u;
+                atomicOr(err, kErrTimeoutMma);
+            }
         }
         __syncwarp();
     } else if (alloc_ok && warp < 6) {
@@ -936,7 +907,7 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
         uint32_t acc_phase = 0, nst = 0;
         for (int tile = first; tile < gp.num_tiles; tile += stride) {
             const TileLoc L = locate(gp, tile);
-            if (!__all_sync(0xffffffffu, wait_phase(&accfull[acc], acc_phase, limit_ns, abort_flag, err,
+            if (!__all_sync(0xffffffffu, wait_phase(&accfull[acc], acc_phase, limit_ns, stop, err,
                                                       kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
@@ -953,11 +924,9 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
     }
 
     __syncthreads();
-    if (*abort_flag) {
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
-        }
-    }
+    // The second CTA's copies complete on the leader's barriers, which it
+    // cannot poll: after a stop it pauses instead.
+    if (*drain_failed || (rank == 1 && stop.raised())) pause_ns(200000ull);
     cluster_sync();                         // nothing of either CTA still in flight
     if (warp == 1) {
         tc_fence_after();
@@ -1024,7 +993,11 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
     sh.accempty = sh.accfull + 2;
     sh.done = sh.accfull + 4;
     sh.tmem_base = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-    sh.abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4);
+    {
+        volatile uint32_t *const flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4);
+        sh.stop = Stop{flag, mapa_shared(smem_u32(const_cast<uint32_t *>(flag)), rank ^ 1u)};
+    }
+    sh.drain_failed = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -1046,7 +1019,8 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             mbar_init(&sh.accempty[a], 8);         // leader: four epilogue warps of each CTA
         }
         mbar_init(sh.done, 1);
-        *sh.abort_flag = 0u;
+        *sh.stop.flag = 0u;
+        *sh.drain_failed = 0u;
         mbar_fence_init();
         for (int g = 0; g < gp.n_groups; ++g) {
             prefetch_tensormap(&gp.tmX[g]);
@@ -1071,7 +1045,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
     if (alloc_ok && warp == 0) {
         // --------------------------------------------------------- producer --
         if (lane == 0) {
-            int stage = 0, qs = 0, loads = 0;
+            int stage = 0, qs = 0, loads = 0, qloads = 0;
             uint32_t phase = 0, qphase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const TileLoc L = locate(gp, tile);
@@ -1079,16 +1053,17 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                 const int nk = gp.nk[L.g];
                 const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.abort_flag, err,
+                    if (!wait_phase_sleepy(&sh.qempty[qs], qphase ^ 1u, 256, limit_ns, sh.stop, err,
                                            kErrTimeoutProducer))
                         goto producer_done;
                     const int start = kb * QFmt<TYPE>::SB_BYTES;
                     mbar_arrive_expect_tx(&sh.qfull[qs], C::Q_SLOT_BYTES);
                     tma_load_2d(qslots + qs * C::Q_SLOT_BYTES, tmW, &sh.qfull[qs], (start & ~15) >> 2, m0);
+                    ++qloads;
                     advance(qs, qphase, QS);
 #pragma unroll 1
                     for (int a = 0; a < SB / BK; ++a) {
-                        if (!wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.abort_flag, err,
+                        if (!wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.stop, err,
                                         kErrTimeoutProducer))
                             goto producer_done;
                         if (rank == 0) mbar_arrive_expect_tx(&sh.fullx[stage], 2 * C::X_HALF);
@@ -1100,7 +1075,15 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            // Each CTA's slice copies complete on its own barriers; the token
+            // halves of both CTAs on the leader's.
+            bool drained = drain_ring(sh.qfull, QS, qloads, -1, limit_ns);
+            if (rank == 0) drained = drain_ring(sh.fullx, XS, loads, inject_stall, limit_ns) && drained;
+            if (!drained) {
+                *sh.drain_failed = 1u;
+                atomicOr(err, kErrTimeoutProducer);
+            }
         }
         __syncwarp();
     } else if (alloc_ok && warp == 1) {
@@ -1110,15 +1093,15 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             uint32_t phase = 0, wphase = 0, acc_phase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
-                if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.abort_flag, err,
+                if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.stop, err,
                                       kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int k = 0; k < nks; ++k) {
-                    if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.abort_flag, err, kErrTimeoutMma) ||
-                        !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma) ||
-                        !wait_phase(&peerw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutMma))
+                    if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.stop, err, kErrTimeoutMma) ||
+                        !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma) ||
+                        !wait_phase(&peerw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma))
                         goto mma_done;
                     tc_fence_after();
                     const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wstage * W_STAGE_BYTES));
@@ -1135,8 +1118,13 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                 advance(acc, acc_phase, 2);
             }
         mma_done:
+            // both CTAs' TMEM is written by these MMAs: they complete before
+            // the cluster barrier that precedes the deallocation
             mma_commit_pair_multicast(sh.done, 0x1);
-            wait_phase(sh.done, 0, limit_ns, sh.abort_flag, err, kErrTimeoutMma);
+            if (!wait_drain(sh.done, 0, limit_ns)) {
+                *sh.drain_failed = 1u;
+                atomicOr(err, kErrTimeoutMma);
+            }
         } else if (lane == 0) {
             // ----------------------------------- forwarding thread (peer) --
             // one arrival on the leader's peerw per stage this CTA's decode
@@ -1148,7 +1136,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
                 for (int k = 0; k < nks; ++k) {
-                    if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.abort_flag, err, kErrTimeoutDequant))
+                    if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutDequant))
                         goto fwd_done;
                     mbar_arrive_remote(peerw_leader + static_cast<uint32_t>(wstage * 8));
                     advance(wstage, wphase, WS);
@@ -1167,7 +1155,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
         for (int tile = first; tile < gp.num_tiles; tile += stride) {
             const TileLoc L = locate(gp, tile);
             if (!__all_sync(0xffffffffu, wait_phase_sleepy(&sh.accfull[acc], acc_phase, 512, limit_ns,
-                                                                 sh.abort_flag, err, kErrTimeoutEpilogue)))
+                                                                 sh.stop, err, kErrTimeoutEpilogue)))
                 break;
             tc_fence_after();
             const uint32_t taddr =
@@ -1191,11 +1179,9 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
     }
 
     __syncthreads();
-    if (*sh.abort_flag) {
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
-        }
-    }
+    // The second CTA's token copies complete on the leader's barriers, which
+    // it cannot poll: after a stop it pauses instead.
+    if (*sh.drain_failed || (rank == 1 && sh.stop.raised())) pause_ns(200000ull);
     cluster_sync();
     if (warp == 1) {
         tc_fence_after();
@@ -1306,7 +1292,7 @@ cudaError_t launch_clusters(Kern kern, int threads, int smem, const GroupParams 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int mc = max_clusters.load();                 // queried once per kernel, then cached
+    int mc = max_clusters.load();                 // queried once per kernel and device, then cached
     if (mc == 0) {
         cfg.gridDim = dim3(num_sms, 1, 1);
         int c = 0;
@@ -1328,14 +1314,15 @@ template <int TYPE>
 cudaError_t launch_pair_typed(const GemmArgs *a, int n, EncodeFn enc, cudaStream_t stream) {
     GroupParams gp;
     if (!build_group<TYPE>(a, n, enc, true, gp)) return cudaErrorInvalidValue;
-    static std::atomic<int> max_clusters{0};
+    static std::atomic<int> max_clusters[kMaxDevices];
+    std::atomic<int> &mc = max_clusters[a[0].device];
     if constexpr (TYPE == 0) {
         using P = PairCfg<2>;
-        return launch_clusters(pair_gemm_kernel<2>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, max_clusters,
+        return launch_clusters(pair_gemm_kernel<2>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, mc,
                                stream, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
     } else {
         using P = PairFCfg<TYPE>;
-        return launch_clusters(pair_fused_kernel<TYPE>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, max_clusters,
+        return launch_clusters(pair_fused_kernel<TYPE>, P::THREADS, P::SMEM_BYTES, gp, a[0].num_sms, mc,
                                stream, a[0].err, a[0].wait_limit_ns, a[0].inject_stall);
     }
 }

@@ -21,13 +21,27 @@ constexpr uint32_t kErrTimeoutMma = 1u << 1;
 constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDequant = 1u << 3;
 constexpr uint32_t kErrPairAlloc = 1u << 4;  // the CTA pair got different TMEM addresses
+constexpr uint32_t kErrTimeoutRing = 1u << 5;    // standalone dequant: a wait on its copy ring
+
+// Devices a process may drive; launchers keep per-device caches of their
+// occupancy queries, indexed by the device ordinal (0 <= device < this).
+constexpr int kMaxDevices = 64;
 
 // `encode_fn` is cuTensorMapEncodeTiled (the output's tensor map for the
 // kernels' TMA stores).
+// Per-device facts and settings a launch needs, prepared by api.cu.
+struct LaunchEnv {
+    int device;            // the current device's ordinal
+    int num_sms;
+    uint32_t *err;         // device error word
+    uint64_t wait_limit_ns;
+    void *encode_fn;       // cuTensorMapEncodeTiled
+};
+
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,
-                               cudaStream_t stream, int num_sms, void *encode_fn);
+                               cudaStream_t stream, const LaunchEnv &env);
 cudaError_t launch_dequant_f16(int type, const void *blocks, int64_t rows, int64_t cols, uint16_t *out,
-                               cudaStream_t stream, int num_sms, void *encode_fn);
+                               cudaStream_t stream, const LaunchEnv &env);
 
 // Everything a GEMM launch needs, prepared on the host by api.cu.
 struct GemmArgs {
@@ -36,6 +50,7 @@ struct GemmArgs {
     const void *W;         // quantized blocks or fp16 weight
     const uint16_t *X;
     float *Y;
+    int device;            // the current device's ordinal
     int num_sms;
     uint32_t *err;         // device error word
     uint64_t wait_limit_ns;
@@ -59,6 +74,6 @@ struct GemvArgs {
     const uint16_t *X;
     float *Y;
 };
-cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int num_sms);
+cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms);
 
 }  // namespace qp

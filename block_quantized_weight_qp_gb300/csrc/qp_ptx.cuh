@@ -81,6 +81,10 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -108,6 +112,28 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// Plain (untiled) bulk copy of `bytes` bytes from global memory into this
+// CTA's shared memory, completing on `bar` (byte count).  Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory operations are visible (a no-op for a
+// launch made without the programmatic-serialization attribute) ...
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and let the next grid in the stream begin launching once every CTA of
+// this one has called this (or exited); that grid still waits for this one
+// to complete before it touches memory.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Tile store: the box at shared address `src` (row-major, no swizzle) to

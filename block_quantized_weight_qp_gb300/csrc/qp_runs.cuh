@@ -31,12 +31,28 @@ struct Gmem {
     }
     __device__ __forceinline__ static uint4 u128(const uint8_t *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 };
+// Shared-memory loads are issued as ld.shared on the 32-bit shared address:
+// the callers' pointers are generic (derived through aligned integer
+// arithmetic), and a generic load would take the slower global-memory path.
 struct Smem {
-    __device__ __forceinline__ static uint32_t u16(const uint8_t *p) {
-        return *reinterpret_cast<const unsigned short *>(p);
+    __device__ __forceinline__ static uint32_t a32(const uint8_t *p) {
+        return static_cast<uint32_t>(__cvta_generic_to_shared(p));
     }
-    __device__ __forceinline__ static uint32_t u32(const uint8_t *p) { return *reinterpret_cast<const unsigned int *>(p); }
-    __device__ __forceinline__ static uint4 u128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ static uint32_t u16(const uint8_t *p) {
+        unsigned short v;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a32(p)));
+        return v;
+    }
+    __device__ __forceinline__ static uint32_t u32(const uint8_t *p) {
+        uint32_t v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a32(p)));
+        return v;
+    }
+    __device__ __forceinline__ static uint4 u128(const uint8_t *p) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a32(p)));
+        return v;
+    }
 };
 
 // Raw bytes of one lane's run, loaded one loop step ahead of their decode.

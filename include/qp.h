@@ -78,7 +78,9 @@ typedef enum {
     QP_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
     QP_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out (from qp_check) */
     QP_ERR_MISALIGNED = 6,        /* a pointer is not aligned as required */
-    QP_ERR_NO_DEVICE = 7          /* no usable sm_103 CUDA device */
+    QP_ERR_NO_DEVICE = 7,         /* no usable sm_103 CUDA device */
+    QP_ERR_PAIR_ALLOC = 8         /* the two CTAs of a GEMM pair got different tensor-memory
+                                     allocations; that launch computed nothing (from qp_check) */
 } qp_status;
 
 /* Static description of the status code. */
@@ -276,6 +278,8 @@ qp_status qp_plan_prefill(const qp_proj_shape *proj, int n, int64_t T, int64_t f
 /*
  * Synchronize `stream`, then read and clear the device error word.
  * Returns QP_OK, QP_ERR_TIMEOUT (a bounded wait inside a GEMM ran out; its
+ * output is incomplete), QP_ERR_PAIR_ALLOC (a CTA pair of a GEMM launch was
+ * given two different tensor-memory allocations and skipped its tiles; its
  * output is incomplete) or QP_ERR_CUDA (the stream reported an error).
  */
 qp_status qp_check(void *stream);

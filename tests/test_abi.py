@@ -57,9 +57,14 @@ def test_block_info_and_row_bytes():
 
 def test_status_strings():
     lib = qp.load()
-    for s in range(8):
+    names = set()
+    for s in range(9):
         assert lib.qp_status_str(s)
+        names.add(lib.qp_status_str(s))
+    assert len(names) == 9                       # every status has its own description
+    assert lib.qp_status_str(9) == b"unknown status"
     assert qp.status_str(qp.QP_ERR_TIMEOUT) == "device-side wait timed out"
+    assert "tensor-memory" in qp.status_str(qp.QP_ERR_PAIR_ALLOC)
 
 
 FAKE = 1 << 40  # 16-byte aligned, never dereferenced: every call below fails its host check
