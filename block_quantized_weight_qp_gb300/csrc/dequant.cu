@@ -65,7 +65,7 @@ template <> struct RFmt<kQ5_K> { static constexpr int BB = 176, RPB = 8, QK = 25
 template <> struct RFmt<kQ2_K> { static constexpr int BB = 84, RPB = 8, QK = 256, ALIGN = 1; };
 template <> struct RFmt<kQ6_K> { static constexpr int BB = 210, RPB = 8, QK = 256, ALIGN = 2; };
 template <> struct RFmt<kQ8_0> { static constexpr int BB = 34, RPB = 1, QK = 32, ALIGN = 1; };
-template <> struct RFmt<kF16> { static constexpr int BB = 64, RPB = 1, QK = 32, ALIGN = 1; };
+template <> struct RFmt<kF16> { static constexpr int BB = 64, RPB = 1, ALIGN = 1; };
 
 constexpr int RD_WARPS = 16;                        // decode warps per CTA
 constexpr int RD_THREADS = (RD_WARPS + 1) * 32;     // + the producer warp
@@ -238,51 +238,21 @@ __global__ void __launch_bounds__(RD_THREADS, 1)
                 const int64_t blk = step * BPS + j;
                 const bool valid = blk < a.nblocks;
                 const uint8_t *src = ring + stage * L::CHUNK_BYTES + (warp * BPS + j) * F::BB;
-                if constexpr (TYPE == kF16 && sizeof(OutT) == 2) {
-                    if (a.use_tma) {
-                        // fp16 weights to fp16: the run's 64 bytes move as they are
-                        const uint32_t tile = tiles + (nst & 1u) * static_cast<uint32_t>(L::TILE);
-                        if (lane == 0) bulk_wait_group_read<1>();
-                        __syncwarp();
-                        const uint32_t row = tile + static_cast<uint32_t>(lane * 64);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint4 v = valid ? Smem::u128(src + 16 * k) : make_uint4(0u, 0u, 0u, 0u);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                             row + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) << 4)),
-                                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                         : "memory");
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(step * 32));
-                            bulk_commit_group();
-                        }
-                        ++nst;
-                        if (valid && blk * 32 + 32 > a.nvals) {
-                            OutT *o = out + blk * 32;
-                            for (int64_t k = 0; k < a.nvals - blk * 32; ++k)
-                                o[k] = static_cast<OutT>(Smem::u16(src + 2 * k));
-                        }
-                        goto next_stage;
-                    }
-                }
-                pair_t y[16];
-                if (valid) {
-                    Raw raw;
-                    raw.template load<Smem>(src, t);
-                    raw.decode(t, y);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) y[k] = pk2(0.0f, 0.0f);
-                }
-                if (a.use_tma) {
-                    // box rows past the end of the output view are not written
+                constexpr bool kRawCopy = TYPE == kF16 && sizeof(OutT) == 2;
+                if (kRawCopy && a.use_tma) {
+                    // fp16 weights to fp16: the run's 64 bytes move as they are
                     const uint32_t tile = tiles + (nst & 1u) * static_cast<uint32_t>(L::TILE);
                     if (lane == 0) bulk_wait_group_read<1>();   // the tile's previous store has read it
                     __syncwarp();
-                    put_run_swz<OutT>(tile, lane, y);
+                    const uint32_t row = tile + static_cast<uint32_t>(lane * 64);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = valid ? Smem::u128(src + 16 * k) : make_uint4(0u, 0u, 0u, 0u);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         row + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) << 4)),
+                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                     : "memory");
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -290,26 +260,55 @@ __global__ void __launch_bounds__(RD_THREADS, 1)
                         bulk_commit_group();
                     }
                     ++nst;
-                    if constexpr (TYPE == kF16) {
-                        // a last run of fewer than 32 values lies outside the view
-                        if (valid && blk * 32 + 32 > a.nvals)
-                            put_run_guarded<OutT>(out, blk * 32, static_cast<int>(a.nvals - blk * 32), y);
+                    if (valid && blk * 32 + 32 > a.nvals) {      // a last run of fewer than 32 values
+                        OutT *o = out + blk * 32;
+                        for (int64_t k = 0; k < a.nvals - blk * 32; ++k)
+                            o[k] = static_cast<OutT>(Smem::u16(src + 2 * k));
                     }
-                } else if (valid) {
-                    if constexpr (TYPE == kF16) {
-                        const int64_t left = a.nvals - blk * 32;
-                        put_run_guarded<OutT>(out, blk * 32, left < 32 ? static_cast<int>(left) : 32, y);
+                } else {
+                    pair_t y[16];
+                    if (valid) {
+                        Raw raw;
+                        raw.template load<Smem>(src, t);
+                        raw.decode(t, y);
                     } else {
-                        const int64_t row = blk / a.nb;
-                        const int64_t col0 = (blk - row * a.nb) * F::QK + 32 * t;
-                        if (col0 < a.cols) {
-                            const int64_t left = a.cols - col0;
-                            put_run_guarded<OutT>(out, row * a.cols + col0, left < 32 ? static_cast<int>(left) : 32, y);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) y[k] = pk2(0.0f, 0.0f);
+                    }
+                    if (a.use_tma) {
+                        // box rows past the end of the output view are not written
+                        const uint32_t tile = tiles + (nst & 1u) * static_cast<uint32_t>(L::TILE);
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        put_run_swz<OutT>(tile, lane, y);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmo, tile, 0, static_cast<int32_t>(step * 32));
+                            bulk_commit_group();
+                        }
+                        ++nst;
+                        if constexpr (TYPE == kF16) {
+                            // a last run of fewer than 32 values lies outside the view
+                            if (valid && blk * 32 + 32 > a.nvals)
+                                put_run_guarded<OutT>(out, blk * 32, static_cast<int>(a.nvals - blk * 32), y);
+                        }
+                    } else if (valid) {
+                        if constexpr (TYPE == kF16) {
+                            const int64_t left = a.nvals - blk * 32;
+                            put_run_guarded<OutT>(out, blk * 32, left < 32 ? static_cast<int>(left) : 32, y);
+                        } else {
+                            const int64_t row = blk / a.nb;
+                            const int64_t col0 = (blk - row * a.nb) * F::QK + 32 * t;
+                            if (col0 < a.cols) {
+                                const int64_t left = a.cols - col0;
+                                put_run_guarded<OutT>(out, row * a.cols + col0,
+                                                      left < 32 ? static_cast<int>(left) : 32, y);
+                            }
                         }
                     }
                 }
             }
-        next_stage:
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             advance(stage, phase, L::ST);

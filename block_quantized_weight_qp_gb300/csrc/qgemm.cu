@@ -171,6 +171,17 @@ __device__ __forceinline__ TileLoc locate(const GroupParams &p, int tile) {
 // eight different bank groups); misaligned fields are realigned in registers
 // with compile-time word offsets (and, for Q6_K, a run-time half-word shift).
 
+// 16-byte shared load through the 32-bit shared address: the staged slices
+// are reached through generic pointers derived by integer alignment
+// arithmetic, which the compiler would otherwise read with generic loads.
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -187,7 +198,7 @@ __device__ __forceinline__ void row_words(const uint8_t *row, uint32_t hs16, uin
     uint32_t c[4 * NC];
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(row + LO + 16 * i);
+        const uint4 v = lds128(row + LO + 16 * i);
         c[4 * i] = v.x;
         c[4 * i + 1] = v.y;
         c[4 * i + 2] = v.z;
@@ -256,7 +267,7 @@ template <int WO> struct Dec<kQ4_K, WO> {
         row_words<16, 32, false>(row, 0, w);       // qs[0 .. 127]
 #pragma unroll
         for (int k = 0; k < 32; ++k) qn[k] = (w[k] >> (4 * h)) & 0x0F0F0F0Fu;
-        k4_scales(*reinterpret_cast<const uint4 *>(row), h, dl2, nml2);
+        k4_scales(lds128(row), h, dl2, nml2);
     }
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int, uint32_t tile,
@@ -284,7 +295,7 @@ template <int WO> struct Dec<kQ5_K, WO> {
 #pragma unroll
         for (int k = 0; k < 32; ++k)
             qn[k] = ((w[k] >> (4 * h)) & 0x0F0F0F0Fu) | (((qh[k & 7] >> (2 * (k >> 3) + h)) & 0x01010101u) << 4);
-        k4_scales(*reinterpret_cast<const uint4 *>(row), h, dl2, nml2);
+        k4_scales(lds128(row), h, dl2, nml2);
     }
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int, uint32_t tile,
@@ -1170,8 +1181,20 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
         if (lane == 0) bulk_wait_all();         // Y stores complete before the CTA's shared memory goes
     } else if (alloc_ok) {
         // ------------------------------------------------------------ decode --
-        const int u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
-        if (warp != 9 && warp != 13) {
+        // Unit u = 0..7 decodes rows 32(u%4)..+31, half u/4 of each K step.  In
+        // the leader the units sit on warps 6, 7, 8, 10, 11, 12, 14, 15, off the
+        // MMA thread's sub-partition 1 (3/3/2 on sub-partitions 2, 3, 0); the
+        // peer issues no MMAs, so its units take warps 6..13, two on each
+        // sub-partition.  Measured on the 8B-shaped layer: decode warps on
+        // sub-partition 1 in both CTAs 1190 TFLOP/s; in neither 1451; in the
+        // peer only 1471.
+        int u = -1;
+        if (rank == 1) {
+            if (warp >= 6 && warp < 14) u = warp - 6;
+        } else if (warp != 9 && warp != 13) {
+            u = warp < 9 ? warp - 6 : (warp < 13 ? warp - 7 : warp - 8);
+        }
+        if (u >= 0) {
             const int r = (u & 3) * 32 + lane;                 // this CTA's weight row
             dequant_role<TYPE, WS, QS>(sh, gp, first, stride, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns,
                                          err);
