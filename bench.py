@@ -351,10 +351,21 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
     weights (88 MB here) would fit in L2, so before every timed step a 256 MB
     buffer is written (outside the timed region: events bracket the GEMV
     launches of each step only).  GB/s counts the weight bytes plus the X and
-    Y bytes of a step."""
+    Y bytes of a step.
+
+    L2 flush: the 256 MB write evicts the weights, and the following read of
+    another 256 MB buffer leaves the L2 holding only clean lines, as it does
+    when a decode step streams a layer's weights after the previous layer's
+    (a flush left dirty would make the timed GEMV pay for writing 129 MB of
+    someone else's data back to HBM)."""
     import torch
     wl = layer.wl
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 << 20, dtype=torch.int32, device=device)
+
+    def flush_l2():
+        flush.fill_(1)
+        flush_rd.sum()
     wbytes = sum(w.numel() for w in layer.W)
     out = {}
     for T in (1, 8):
@@ -388,7 +399,7 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
         for how in ("grouped", "single", "eager"):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
             for e0, e1 in ev:
-                flush.fill_(1)
+                flush_l2()
                 e0.record(stream)
                 if how == "eager":
                     grouped(stream)
@@ -406,7 +417,7 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
                           "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 1),
                           "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4),
                           "one_launch_per_projection_ms": round(res["single"], 4)}
-    del flush
+    del flush, flush_rd
     return out
 
 

@@ -323,7 +323,7 @@ qp_status run_gemv(int type, const qp_gemm_desc *descs, int n, int64_t T, void *
     for (int i = 0; i < n; ++i)
         a[i] = qp::GemvArgs{descs[i].W, qp_row_bytes(type, descs[i].in_f), descs[i].out_f, descs[i].in_f, T,
                             descs[i].X, descs[i].Y};
-    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), d->dev, d->num_sms) != cudaSuccess) {
+    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), env_of(d)) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }
@@ -345,7 +345,7 @@ qp_status qp_decode_gemv_group(int type, const qp_gemm_desc *descs, int n, int64
         if (s != QP_OK) return s;
     }
     int64_t blocks = 0;
-    for (int i = 0; i < n; ++i) blocks += (descs[i].out_f + 7) / 8;
+    for (int i = 0; i < n; ++i) blocks += (descs[i].out_f + 15) / 16;
     if (blocks > INT32_MAX) return QP_ERR_UNSUPPORTED_SHAPE;
     return run_gemv(type, descs, n, T, stream);
 }

@@ -10,36 +10,51 @@
 // the prefill GEMM on T <= 8 rows.
 //
 // Meant to be bound by HBM on W (every weight byte is read once), which puts
-// the ALUs on a budget of a few instructions per weight value: they only
-// decode, and the dot products run on the tensor cores with the warp-level
-// mma.sync m16n8k16, whose cost per value does not depend on T.  The MMA's
-// A operand is the token rows (16 rows, of which rows >= T and all of rows
-// 8..15 are zeros), B is 8 weight rows x 16 K values in fp16, D = f32.
+// the integer pipe on a budget of about one to two instructions per weight
+// value: the lanes only decode, and the dot products run on the tensor cores
+// with the warp-level mma.sync m16n8k16, whose cost per value does not depend
+// on T.  The MMA's A operand is 16 weight rows x 16 K values in fp16, B is
+// the K values of the T token rows (columns >= T zero), D = f32.
 //
-// A CTA owns 8 weight rows at a time; its NW warps split the rows' steps of
-// 8 runs (one K-quant superblock, or 8 Q8_0 / F16 blocks).  Each warp stages
-// its steps' bytes -- 8 rows x one step, copied as the 16-byte aligned span
-// that covers it, so that every byte keeps its alignment modulo 16 -- into a
-// private ring of NST shared-memory slots with coalesced 16-byte cp.async
-// copies issued NST - 1 steps ahead; the ring runs on from one 8-row block
-// into the CTA's next.  In a step, lane (g, c) (g = lane / 4, c = lane % 4)
-// decodes runs 2c and 2c + 1 of the step in weight row g from the slot with
-// the exact run decoders (qp_runs.cuh), rounds them to fp16 and feeds each
-// run's 32 values to eight MMAs, four per MMA.  The MMA's K order is
-// permuted: K slots 2c, 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3 of
-// lane c's run in MMA i, for A and B alike, so the sum over K is unchanged,
-// each lane's B fragment is its own decoded values and its A fragment is 4
-// consecutive values of token row g of X.  Runs past the row's end
-// contribute zeros.  The warps' 8 x 8 partial tiles are summed through
-// shared memory in warp order, so results are deterministic.
+// Two persistent CTAs per SM take 16-row blocks b, b + gridDim.x, ... of the
+// launch.  A producer warp streams each block's rows through a ring of
+// shared-memory tiles with 2-D TMA copies: a tile is the 16 rows x S steps
+// (S x 256 values) of one K range, as the 16-byte aligned cover of that range
+// in every row (up to 2 KB per row, so that the copies are long).  Eight
+// consumer warps split the tiles: warp w takes step w % S of every tile its
+// team w / S is given (the teams take a block's tiles in turn).  Measured on
+// the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
+// faster than one with twice the warps and ring.  In a step,
+// lane (g, c) (g = lane / 4, c = lane % 4) decodes runs 2c and 2c + 1 of
+// the step in weight rows g and g + 8 from the tile with the exact run
+// decoders (qp_runs.cuh), rounds them to fp16 and feeds each run's 32 values
+// to eight MMAs, four per MMA.  The MMA's K order is permuted: K slots 2c,
+// 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3 of lane c's run in MMA i,
+// for A and B alike, so the sum over K is unchanged, each lane's A fragment
+// is its own decoded values and its B fragment is 4 consecutive values of
+// token row g of X.  Steps past the row's end contribute zeros.  At a
+// block's end the consumer warps' 16 x 8 partial tiles are summed through
+// shared memory in warp order (a named barrier over the consumers only), so
+// results are deterministic.
+//
+// Weights whose row pitch is not a multiple of 16 bytes (which a TMA tensor
+// cannot describe) are staged instead by 16 bulk copies a tile, one per row.
+//
+// Every wait is bounded; on expiry the kernel records an error bit and stops
+// (the consumers still meet at every block's barrier), and the producer
+// waits for its copies in flight before the CTA exits.
 #include <atomic>
 #include <cstdint>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "qp_decode.cuh"
 #include "qp_internal.h"
+#include "qp_ptx.cuh"
 #include "qp_runs.cuh"
+#include "qp_sync.cuh"
 
 namespace qp {
 namespace {
@@ -100,33 +115,29 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-#ifndef QP_GEMV_MINB
-#define QP_GEMV_MINB 3        // resident CTAs per SM the register budget is cut for
-#endif
+constexpr int ROWS = 16;                      // weight rows per block (the MMA's M)
+constexpr int STEP_VALUES = 256;              // values of a row per step (8 runs)
+constexpr int NC = 8;                         // consumer warps per CTA
+constexpr int GEMV_THREADS = (NC + 1) * 32;   // + the producer warp
 
-// A step's bytes per row (STEP), the staged row pitch (an odd multiple of 16
-// bytes, at least the widest 16-byte aligned cover of a step, so that the
-// eight rows' 16-byte loads of a load phase hit eight bank groups) and the
-// ring depth (steps in flight, scaled to keep a few KB per warp in flight).
+// A step's bytes per row (STEP), steps per tile (S), the staged row pitch
+// (PITCH: the TMA box width, an odd multiple of 16 bytes at least the
+// 16-byte aligned cover of S steps wherever they start, so that 16-byte
+// loads of the rows of a load phase hit different bank groups) and the ring
+// depth NST (tiles, 80-95 KB in all: two CTAs share an SM).
 template <int TYPE> struct Stage;
-template <> struct Stage<kQ4_K> { static constexpr int STEP = 144, PITCH = 144, NST = 4; };
-template <> struct Stage<kQ5_K> { static constexpr int STEP = 176, PITCH = 176, NST = 4; };
-template <> struct Stage<kQ2_K> { static constexpr int STEP = 84, PITCH = 112, NST = 5; };
-template <> struct Stage<kQ6_K> { static constexpr int STEP = 210, PITCH = 240, NST = 3; };
-template <> struct Stage<kQ8_0> { static constexpr int STEP = 272, PITCH = 304, NST = 3; };
-template <> struct Stage<kF16> { static constexpr int STEP = 512, PITCH = 528, NST = 2; };
+template <> struct Stage<kQ4_K> { static constexpr int STEP = 144, S = 8, PITCH = 1168, NST = 5; };
+template <> struct Stage<kQ5_K> { static constexpr int STEP = 176, S = 8, PITCH = 1424, NST = 4; };
+template <> struct Stage<kQ2_K> { static constexpr int STEP = 84, S = 8, PITCH = 688, NST = 8; };
+template <> struct Stage<kQ6_K> { static constexpr int STEP = 210, S = 8, PITCH = 1712, NST = 3; };
+template <> struct Stage<kQ8_0> { static constexpr int STEP = 272, S = 4, PITCH = 1104, NST = 5; };
+template <> struct Stage<kF16> { static constexpr int STEP = 512, S = 2, PITCH = 1040, NST = 5; };
 
-template <int TYPE, int NW> constexpr int gemv_smem() { return NW * Stage<TYPE>::NST * 8 * Stage<TYPE>::PITCH; }
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+template <int TYPE> __host__ __device__ constexpr int tile_bytes() { return ROWS * Stage<TYPE>::PITCH; }
+template <int TYPE> __host__ __device__ constexpr int gemv_smem() { return Stage<TYPE>::NST * tile_bytes<TYPE>(); }
 
 // A launch runs up to kMaxGroup projections of one type over the same T
-// token rows.  Their 8-row blocks are numbered projection after projection;
+// token rows.  Their 16-row blocks are numbered projection after projection;
 // CTA b takes blocks b, b + gridDim.x, ...  A block's sums do not depend on
 // which CTA computes it or what shares the launch.
 struct GemvGroup {
@@ -135,193 +146,288 @@ struct GemvGroup {
     float *Y;
     int64_t row_bytes;
     int out_f, in_f, blk_end;      // blk_end: one past the projection's last block
+    int use_tma;                   // tmW describes W (its row pitch is a multiple of 16 bytes)
 };
 struct GemvParams {
+    CUtensorMap tmW[kMaxGroup];    // W as [out_f rows x row_bytes / 8] 64-bit words, box PITCH / 8 x 16
     GemvGroup g[kMaxGroup];
     int n, T;
+    uint32_t *err;
+    uint64_t limit_ns;
 };
 
-template <int TYPE, int NW>
-__global__ void __launch_bounds__(NW * 32, QP_GEMV_MINB) gemv_kernel(const __grid_constant__ GemvParams gp) {
+// Block b of the launch: its projection, first weight row, steps per row
+// and tiles.
+struct BlockLoc {
+    int grp, m0, nsteps, ntiles;
+};
+
+template <int TYPE>
+__device__ __forceinline__ BlockLoc block_loc(const GemvParams &gp, int b) {
+    int k = 0;
+    while (k < gp.n - 1 && b >= gp.g[k].blk_end) ++k;
+    const int nsteps = (gp.g[k].in_f + STEP_VALUES - 1) / STEP_VALUES;
+    return {k, (b - (k ? gp.g[k - 1].blk_end : 0)) * ROWS, nsteps, (nsteps + Stage<TYPE>::S - 1) / Stage<TYPE>::S};
+}
+
+template <int TYPE>
+__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_constant__ GemvParams gp) {
     using G = Geom<TYPE>;
     using S = Stage<TYPE>;
     using Raw = typename RawOf<TYPE>::T;
-    extern __shared__ __align__(16) uint8_t ring_all[];
-    __shared__ float part[NW][8][8];                      // each warp's 8 weight rows x 8 tokens
+    constexpr int TILE = tile_bytes<TYPE>();
+    constexpr int TEAMS = NC / S::S;                      // tiles in work at once
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ float part[NC][ROWS][8];                   // each consumer warp's 16 weight rows x 8 tokens
+    __shared__ __align__(8) uint64_t full[S::NST], empty[S::NST];
+    __shared__ uint32_t stop_word, drain_failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-    uint8_t *ring = ring_all + warp * (S::NST * 8 * S::PITCH);
-    const int T = gp.T, nblk = gp.g[gp.n - 1].blk_end;
-    const bool tok = g < T;                               // this lane's A row is a token row
-    // A cursor over this warp's items (block, step): the warp takes steps
-    // warp, warp + NW, ... of each block's rows, spw of them for every warp
-    // (spw = the projection's steps per row / NW, rounded up), in block order.
-    struct Cur {
-        int b, i;                                         // block, item within the block
-        int grp, m0, nsteps, spw;
-    };
-    auto locate = [&](Cur &u) {
-        int k = 0;
-        while (k < gp.n - 1 && u.b >= gp.g[k].blk_end) ++k;
-        u.grp = k;
-        u.m0 = (u.b - (k ? gp.g[k - 1].blk_end : 0)) * 8;
-        u.nsteps = (gp.g[k].in_f / 32 + 7) / 8;
-        u.spw = (u.nsteps + NW - 1) / NW;
-    };
-    auto advance = [&](Cur &u) {
-        if (++u.i == u.spw) {
-            u.i = 0;
-            u.b += gridDim.x;
-            if (u.b < nblk) locate(u);
+    const Stop stop{&stop_word, 0u};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::NST; ++s) {
+            mbar_init(&full[s], 1);                       // the producer's arrive + the bytes
+            mbar_init(&empty[s], S::S);                   // the team that reads the tile
         }
-    };
-    // Stage the producer cursor's item into slot `slot_i`: lane (g, c)
-    // copies 16-byte vectors c, c + 4, ... of row g's cover [start & ~15,
-    // end) of the step (a copy that would pass the end of W -- only the
-    // last row's last step can -- is done 2 bytes at a time instead).
-    auto stage = [&](const Cur &u, int slot_i) {
-        const int q = u.i * NW + warp;
-        if (u.b < nblk && q < u.nsteps) {
-            const GemvGroup &P = gp.g[u.grp];
-            const int row = min(u.m0 + g, P.out_f - 1);   // rows past out_f: a copy of the last row
-            const uint8_t *start = P.W + static_cast<int64_t>(row) * P.row_bytes + static_cast<int64_t>(q) * S::STEP;
-            const uint8_t *a0 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(start) & ~uintptr_t(15));
-            const int64_t left = P.row_bytes - static_cast<int64_t>(q) * S::STEP;   // bytes of the row from start
-            const int nbytes = static_cast<int>((left < S::STEP ? left : S::STEP) + (start - a0));
-            const uint32_t dst0 = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) +
-                                  static_cast<uint32_t>((slot_i * 8 + g) * S::PITCH);
-            const bool last_row = row == P.out_f - 1;
-#pragma unroll
-            for (int k = c; k < S::PITCH / 16; k += 4) {
-                if (16 * k >= nbytes) break;
-                const uint8_t *src = a0 + 16 * k;
-                const uint32_t dst = dst0 + static_cast<uint32_t>(16 * k);
-                if (!last_row || 16 * (k + 1) <= nbytes) {
-                    cp_async16(dst, src);
-                } else {                                  // the tail of W: whole 2-byte units only
-                    for (int o = 0; 16 * k + o < nbytes; o += 2)
-                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst + static_cast<uint32_t>(o)),
-                                     "h"(__ldg(reinterpret_cast<const unsigned short *>(src + o))));
-                }
-            }
-        }
-        cp_async_commit();
-    };
-    Cur cons{static_cast<int>(blockIdx.x), 0, 0, 0, 0, 0};
-    if (cons.b >= nblk) return;
-    locate(cons);
-    Cur prod = cons;
-#pragma unroll 1
-    for (int p = 0; p < S::NST - 1; ++p) {
-        stage(prod, p);
-        advance(prod);
+        stop_word = 0u;
+        drain_failed = 0u;
+        for (int k = 0; k < gp.n; ++k)
+            if (gp.g[k].use_tma) prefetch_tensormap(&gp.tmW[k]);
+        mbar_fence_init();
     }
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int n = 0; cons.b < nblk; ++n) {
-        stage(prod, (n + S::NST - 1) % S::NST);           // refills the slot read in the previous item
-        advance(prod);
-        cp_async_wait<S::NST - 1>();                      // this lane's copies of item n have landed
-        __syncwarp();                                     // ... and every lane's
-        const GemvGroup &P = gp.g[cons.grp];
-        const int q = cons.i * NW + warp;
-        const int nruns = P.in_f / 32;
-        const int row = min(cons.m0 + g, P.out_f - 1);
-        const uint8_t *start = P.W + static_cast<int64_t>(row) * P.row_bytes + static_cast<int64_t>(q) * S::STEP;
-        const uint8_t *srow = ring + (n % S::NST) * 8 * S::PITCH + g * S::PITCH +
-                              (reinterpret_cast<uintptr_t>(start) & 15);
-        const uint16_t *xrow = P.X + static_cast<int64_t>(tok ? g : 0) * P.in_f;
-#pragma unroll
-        for (int rho = 0; rho < 2; ++rho) {
-            const int j = 8 * q + 2 * c + rho;            // this lane's run of the row
-            const bool valid = q < cons.nsteps && j < nruns;
-            uint32_t h[16];
-            if (valid) {
-                Raw raw;
-                raw.template load<Smem>(srow + ((2 * c + rho) / G::RPB) * G::BB, j % G::RPB);
-                run_f16<TYPE>(raw, j % G::RPB, h);
-            } else {
-#pragma unroll
-                for (int p = 0; p < 16; ++p) h[p] = 0u;
-            }
-            const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * j);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {                 // 8 values of X per 16-byte load: two MMAs
-                const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
-                mma_16816(d, x.x, 0u, x.y, 0u, h[4 * u], h[4 * u + 1]);
-                mma_16816(d, x.z, 0u, x.w, 0u, h[4 * u + 2], h[4 * u + 3]);
+    __syncthreads();
+    grid_dependency_wait();                               // the previous grid's memory operations are done
+    const int nblk = gp.g[gp.n - 1].blk_end;
+
+    if (warp == NC) {
+        // ------------------------------------------------------------ producer --
+        // The CTA's tiles in order: block after block, each block's tiles
+        // 0 .. ntiles - 1; tile n goes to slot n % NST.
+        int n = 0;
+        bool ok = true;
+        for (int b = blockIdx.x; ok && b < nblk; b += gridDim.x) {
+            const BlockLoc L = block_loc<TYPE>(gp, b);
+            const GemvGroup &P = gp.g[L.grp];
+            for (int j = 0; j < L.ntiles; ++j, ++n) {
+                const int s = n % S::NST;
+                if (!wait_phase_warp(&empty[s], ((n / S::NST) & 1) ^ 1u, gp.limit_ns, stop, gp.err,
+                                     kErrTimeoutGemv)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *const slot = ring + s * TILE;
+                const int64_t off = static_cast<int64_t>(j) * S::S * S::STEP;   // the tile's first byte in a row
+                if (P.use_tma) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[s], TILE);
+                        tma_load_2d(slot, &gp.tmW[L.grp], &full[s], static_cast<int32_t>((off & ~int64_t(15)) >> 3),
+                                    L.m0);
+                    }
+                } else if (lane < ROWS) {
+                    // row m0 + lane: the 16-byte aligned cover of its S steps
+                    uint32_t bytes = 0;
+                    const uint8_t *a0 = nullptr;
+                    uint8_t *dst = slot + lane * S::PITCH;
+                    if (L.m0 + lane < P.out_f) {
+                        const uint8_t *row = P.W + static_cast<int64_t>(L.m0 + lane) * P.row_bytes;
+                        const uint8_t *start = row + off;
+                        const int64_t left = P.row_bytes - off;
+                        const uint8_t *end = start + (left < int64_t(S::S) * S::STEP ? left : int64_t(S::S) * S::STEP);
+                        const uint8_t *w_end = P.W + static_cast<int64_t>(P.out_f) * P.row_bytes;
+                        a0 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(start) & ~uintptr_t(15));
+                        const uint8_t *a1 = reinterpret_cast<const uint8_t *>(
+                            (reinterpret_cast<uintptr_t>(end) + 15) & ~uintptr_t(15));
+                        if (a1 > w_end) {   // only the last row's last tile: its last bytes by plain loads
+                            a1 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(w_end) & ~uintptr_t(15));
+                            if (a1 < a0) a1 = a0;
+                            for (const uint8_t *p = a1; p < end; ++p) dst[p - a0] = *p;
+                        }
+                        bytes = static_cast<uint32_t>(a1 - a0);
+                    }
+                    const uint32_t total = __reduce_add_sync(0x0000ffffu, bytes);
+                    __syncwarp(0x0000ffffu);              // the plain stores above precede the arrive
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+                    if (bytes) bulk_load(dst, a0, bytes, &full[s]);
+                }
+                __syncwarp();
             }
         }
-        __syncwarp();                                     // the slot is read before it is refilled
-        if (cons.i == cons.spw - 1) {                     // the block's last item (the same n in every warp)
-            // D rows 0..7 = tokens g, columns 2c, 2c + 1 = weight rows; rows 8..15 are zero
-            part[warp][2 * c][g] = d[0];
-            part[warp][2 * c + 1][g] = d[1];
-            d[0] = d[1] = d[2] = d[3] = 0.0f;
-            __syncthreads();
-            for (int o = threadIdx.x; o < 64; o += NW * 32) {
-                const int t = o >> 3, r = o & 7;          // consecutive threads: consecutive rows of Y
+        // the copies issued land before the CTA's shared memory goes
+        if (lane == 0) {
+            bool drained = true;
+            for (int m = n - S::NST < 0 ? 0 : n - S::NST; m < n; ++m)
+                drained = wait_drain(&full[m % S::NST], static_cast<uint32_t>((m / S::NST) & 1), gp.limit_ns) &&
+                          drained;
+            if (!drained) {
+                drain_failed = 1u;
+                atomicOr(gp.err, kErrTimeoutGemv);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers --
+        const int g = lane >> 2, c = lane & 3;
+        const int team = warp / S::S, sl = warp % S::S;   // this warp's team and step within a tile
+        const int T = gp.T;
+        const bool tok = g < T;                           // this lane's B column is a token row
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        bool live = true;
+        int n0 = 0;                                       // the block's first tile in the CTA's sequence
+        for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
+            const BlockLoc L = block_loc<TYPE>(gp, b);
+            const GemvGroup &P = gp.g[L.grp];
+            const int nruns = (P.in_f + 31) / 32;
+            const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
+            // rows g, g + 8: the row's start modulo 16 (0 when staged by TMA)
+            const int base0 = P.use_tma ? 0
+                                        : static_cast<int>((reinterpret_cast<uintptr_t>(P.W) +
+                                                            static_cast<uint64_t>(L.m0 + g) * P.row_bytes) & 15);
+            const int base1 = P.use_tma ? 0
+                                        : static_cast<int>((reinterpret_cast<uintptr_t>(P.W) +
+                                                            static_cast<uint64_t>(L.m0 + g + 8) * P.row_bytes) & 15);
+            const uint16_t *xrow = P.X + static_cast<int64_t>(tok ? g : 0) * P.in_f;
+            for (int j = team; j < L.ntiles; j += TEAMS) {
+                const int n = n0 + j, s = n % S::NST;
+                live = live && wait_phase_warp(&full[s], static_cast<uint32_t>((n / S::NST) & 1), gp.limit_ns, stop,
+                                               gp.err, kErrTimeoutGemv);
+                if (!live) continue;
+                const int q = j * S::S + sl;              // this warp's step of the row
+                if (q < L.nsteps) {
+                    const int off = j * S::S * S::STEP;
+                    const uint8_t *slot = ring + s * TILE;
+                    const uint8_t *src0 = slot + g * S::PITCH + ((base0 + off) & 15) + sl * S::STEP;
+                    const uint8_t *src1 = slot + (g + 8) * S::PITCH + ((base1 + off) & 15) + sl * S::STEP;
+#pragma unroll
+                    for (int rho = 0; rho < 2; ++rho) {
+                        const int t = 2 * c + rho;        // this lane's run of the step
+                        const int jr = 8 * q + t;         // ... and of the row
+                        const bool valid = jr < nruns;
+                        uint32_t h0[16], h1[16];
+                        if (valid && row0) {
+                            Raw raw;
+                            raw.template load<Smem>(src0 + (t / G::RPB) * G::BB, t % G::RPB);
+                            run_f16<TYPE>(raw, t % G::RPB, h0);
+                        } else {
+#pragma unroll
+                            for (int p = 0; p < 16; ++p) h0[p] = 0u;
+                        }
+                        if (valid && row1) {
+                            Raw raw;
+                            raw.template load<Smem>(src1 + (t / G::RPB) * G::BB, t % G::RPB);
+                            run_f16<TYPE>(raw, t % G::RPB, h1);
+                        } else {
+#pragma unroll
+                            for (int p = 0; p < 16; ++p) h1[p] = 0u;
+                        }
+                        const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * jr);
+                        float (&acc)[4] = rho ? e : d;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {     // 8 values of X per 16-byte load: two MMAs
+                            const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
+                            mma_16816(acc, h0[4 * u], h1[4 * u], h0[4 * u + 1], h1[4 * u + 1], x.x, x.y);
+                            mma_16816(acc, h0[4 * u + 2], h1[4 * u + 2], h0[4 * u + 3], h1[4 * u + 3], x.z, x.w);
+                        }
+                    }
+                }
+                __syncwarp();                             // the tile is read before it is released
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            n0 += L.ntiles;
+            // block end: D rows g, g + 8 (weight rows), columns 2c, 2c + 1 (tokens)
+            part[warp][g][2 * c] = d[0] + e[0];
+            part[warp][g][2 * c + 1] = d[1] + e[1];
+            part[warp][g + 8][2 * c] = d[2] + e[2];
+            part[warp][g + 8][2 * c + 1] = d[3] + e[3];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) d[k] = e[k] = 0.0f;
+            named_barrier_sync(1, NC * 32);
+            for (int o = threadIdx.x; o < ROWS * 8; o += NC * 32) {
+                const int tt = o / ROWS, r = o % ROWS;    // consecutive threads: consecutive rows of Y
                 float v = 0.0f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) v += part[w][r][t];
-                if (t < T && cons.m0 + r < P.out_f) P.Y[static_cast<int64_t>(t) * P.out_f + cons.m0 + r] = v;
+                for (int w = 0; w < NC; ++w) v += part[w][r][tt];
+                if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = v;
             }
-            __syncthreads();
+            named_barrier_sync(1, NC * 32);
         }
-        advance(cons);
     }
-    cp_async_wait<0>();                                   // no copy outlives the kernel
+    __syncthreads();
+    if (drain_failed) pause_ns(200000ull);
 }
 
-#ifndef QP_GEMV_NW
-#define QP_GEMV_NW 8          // warps per CTA (split of each 8-row block's steps)
-#endif
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Persistent grid: as many CTAs as fit at once (queried once per
-// instantiation: the decode GEMVs are microsecond kernels), at most one per
-// 8-row block; each CTA's ring runs on from one block into its next, across
-// the projections of the launch.
-template <int TYPE, int NW>
-cudaError_t launch_nw(const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms) {
-    auto kern = gemv_kernel<TYPE, NW>;
-    constexpr int smem = gemv_smem<TYPE, NW>();
-    // the shared-memory opt-in and the occupancy query hold for one device:
-    // done once per device and instantiation
-    static std::atomic<int> per_sm[kMaxDevices];
-    int k = per_sm[device].load();
-    if (k == 0) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, NW * 32, smem) != cudaSuccess || k < 1) {
-            cudaGetLastError();
-            k = 1;
-        }
-        per_sm[device].store(k);
+// W as a 2-D tensor of 64-bit words [out_f rows x row_bytes / 8], box
+// pitch / 8 words x 16 rows, no swizzle; reads outside it are zero-filled.
+bool encode_w(void *encode_fn, const void *W, int64_t row_bytes, int64_t out_f, int pitch, CUtensorMap *map) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 8), static_cast<cuuint64_t>(out_f)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pitch / 8), static_cast<cuuint32_t>(ROWS)};
+    const cuuint32_t estr[2] = {1, 1};
+    return reinterpret_cast<EncodeFn>(encode_fn)(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims,
+                                                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Persistent grid: two CTAs per SM, at most one per 16-row block; each CTA's
+// ring runs on from one block into its next, across the projections of the
+// launch.  Launched with programmatic stream serialization (the kernel waits
+// for the previous grid before it reads or writes).
+template <int TYPE>
+cudaError_t launch_typed(const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env) {
+    auto kern = gemv_kernel<TYPE>;
+    constexpr int smem = gemv_smem<TYPE>();
+    static std::atomic<int> smem_set[kMaxDevices];        // the opt-in holds per device
+    if (!smem_set[env.device].load()) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set[env.device].store(1);
     }
     GemvParams gp;
+    memset(&gp, 0, sizeof(gp));
     int64_t blocks = 0;
     for (int i = 0; i < n; ++i) {
-        blocks += (a[i].out_f + 7) / 8;
+        blocks += (a[i].out_f + ROWS - 1) / ROWS;
         if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+        // TMA tiles need a row pitch that is a multiple of 16 bytes (and a
+        // 16-byte aligned base, which the C ABI already requires)
+        const bool tma = a[i].row_bytes % 16 == 0 && env.encode_fn &&
+                         encode_w(env.encode_fn, a[i].W, a[i].row_bytes, a[i].out_f, Stage<TYPE>::PITCH, &gp.tmW[i]);
         gp.g[i] = GemvGroup{static_cast<const uint8_t *>(a[i].W), a[i].X, a[i].Y, a[i].row_bytes,
-                            static_cast<int>(a[i].out_f), static_cast<int>(a[i].in_f), static_cast<int>(blocks)};
+                            static_cast<int>(a[i].out_f), static_cast<int>(a[i].in_f), static_cast<int>(blocks),
+                            tma ? 1 : 0};
     }
     gp.n = n;
     gp.T = static_cast<int>(a[0].T);
-    const int64_t cap = static_cast<int64_t>(num_sms) * k;
-    kern<<<static_cast<unsigned>(blocks < cap ? blocks : cap), NW * 32, smem, stream>>>(gp);
+    gp.err = env.err;
+    gp.limit_ns = env.wait_limit_ns;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < 2 * env.num_sms ? blocks : 2 * env.num_sms), 1, 1);
+    cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, gp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms) {
+cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env) {
     if (n < 1 || n > kMaxGroup) return cudaErrorInvalidValue;
     switch (type) {
-    case kQ8_0: return launch_nw<kQ8_0, QP_GEMV_NW>(a, n, stream, device, num_sms);
-    case kQ2_K: return launch_nw<kQ2_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
-    case kQ4_K: return launch_nw<kQ4_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
-    case kQ5_K: return launch_nw<kQ5_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
-    case kQ6_K: return launch_nw<kQ6_K, QP_GEMV_NW>(a, n, stream, device, num_sms);
-    case kF16: return launch_nw<kF16, QP_GEMV_NW>(a, n, stream, device, num_sms);
+    case kQ8_0: return launch_typed<kQ8_0>(a, n, stream, env);
+    case kQ2_K: return launch_typed<kQ2_K>(a, n, stream, env);
+    case kQ4_K: return launch_typed<kQ4_K>(a, n, stream, env);
+    case kQ5_K: return launch_typed<kQ5_K>(a, n, stream, env);
+    case kQ6_K: return launch_typed<kQ6_K>(a, n, stream, env);
+    case kF16: return launch_typed<kF16>(a, n, stream, env);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -22,6 +22,7 @@ constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDequant = 1u << 3;
 constexpr uint32_t kErrPairAlloc = 1u << 4;  // the CTA pair got different TMEM addresses
 constexpr uint32_t kErrTimeoutRing = 1u << 5;    // standalone dequant: a wait on its copy ring
+constexpr uint32_t kErrTimeoutGemv = 1u << 6;    // decode GEMV: a wait on a warp's copy ring
 
 // Devices a process may drive; launchers keep per-device caches of their
 // occupancy queries, indexed by the device ordinal (0 <= device < this).
@@ -74,6 +75,6 @@ struct GemvArgs {
     const uint16_t *X;
     float *Y;
 };
-cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, int device, int num_sms);
+cudaError_t launch_decode_gemv(int type, const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env);
 
 }  // namespace qp

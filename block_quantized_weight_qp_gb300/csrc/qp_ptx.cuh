@@ -48,6 +48,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of
+// this CTA: warps that do not take part are not held.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------- cluster ---
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

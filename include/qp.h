@@ -230,7 +230,7 @@ qp_status qp_decode_gemv(int type, const void *W, int64_t out_f, int64_t in_f, c
  * Every Y is bitwise the qp_decode_gemv result.  Requirements and errors are
  * those of qp_decode_gemv for every desc, plus QP_ERR_INVALID_PARAMETER for a
  * NULL descs or n outside 1..QP_MAX_GROUP, and QP_ERR_UNSUPPORTED_SHAPE when
- * the descs hold more than 2^31 - 1 blocks of 8 weight rows in all.
+ * the descs hold more than 2^31 - 1 blocks of 16 weight rows in all.
  */
 qp_status qp_decode_gemv_group(int type, const qp_gemm_desc *descs, int n, int64_t T, void *stream);
 
