@@ -395,6 +395,25 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
                 with torch.cuda.graph(graphs[name], stream=cap):
                     fn(cap)
         torch.cuda.synchronize()
+        # each grouped launch on its own (eager, L2 flushed before each step)
+        per_launch = {}
+        nl = len(layer.launches(True))
+        evl = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+               for _ in range(steps)]
+        for s_ev in evl:
+            flush_l2()
+            for k, (qt, idx) in enumerate(layer.launches(True)):
+                descs = [(layer.W[i], wl["projections"][i][1], wl["projections"][i][2],
+                          X[wl["projections"][i][3]], Y[i]) for i in idx]
+                s_ev[k][0].record(stream)
+                qp.qp_decode_gemv_group(qt, descs, T, stream)
+                s_ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        for k, (qt, idx) in enumerate(layer.launches(True)):
+            wb = sum(layer.W[i].numel() for i in idx)
+            us = statistics.mean(e[k][0].elapsed_time(e[k][1]) for e in evl) * 1e3
+            per_launch["%s:%s" % (synth.NAMES[qt], ",".join(wl["projections"][i][0] for i in idx))] = {
+                "us": round(us, 2), "weight_bytes": wb, "weight_gbs": round(wb / (us / 1e6) / 1e9, 1)}
         res = {}
         for how in ("grouped", "single", "eager"):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -416,7 +435,7 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
         out["T%d" % T] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1),
                           "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 1),
                           "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4),
-                          "one_launch_per_projection_ms": round(res["single"], 4)}
+                          "one_launch_per_projection_ms": round(res["single"], 4), "per_launch_eager": per_launch}
     del flush, flush_rd
     return out
 
@@ -454,6 +473,63 @@ def cpu_oracle_sample(wl, seconds=10.0, rows_max=4096):
             "kind": "oracle",
             "sample": "scalar-C oracle: f32 dequant of all 7 weights (%.2f s) + fp64 GEMM of %d token rows "
                       "(%.2f s), extrapolated linearly to T=%d" % (t_deq, n, t_rows, T)}
+
+
+def cpu_dequant_rows(seconds_per_case=0.2):
+    """The CPU oracle's dequant throughput per block type (the same weights as
+    the GPU dequant rows), on one core and on every core of the process's
+    affinity mask: GB/s of quantized bytes read + output bytes written."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    cases = [("Q4_K", synth.Q4_K, 4096, 4096, 12), ("Q8_0", synth.Q8_0, 4096, 4096, 13),
+             ("Q2_K", synth.Q2_K, 4096, 4096, 14), ("Q6_K", synth.Q6_K, 4096, 12288, 15),
+             ("Q5_K", synth.Q5_K, 4096, 4096, 16), ("F16", synth.F16, 4096, 4096, 17)]
+    out = {"cores": cores}
+    try:
+        for name, qt, rows, cols, tid in cases:
+            w = synth.blocks(qt, rows, cols, seed=1, tensor=tid)
+            for f16 in (False, True):
+                fn = oracle.dequant_f16 if f16 else oracle.dequant_f32
+                nbytes = w.size + rows * cols * (2 if f16 else 4)
+                res = {}
+                for label, n in (("one_core", 1), ("all_cores", cores)):
+                    oracle.set_num_threads(n)
+                    reps, t0 = 0, time.perf_counter()
+                    while True:
+                        fn(qt, w, rows, cols)
+                        reps += 1
+                        dt = time.perf_counter() - t0
+                        if dt >= seconds_per_case:
+                            break
+                    res[label + "_gbs"] = round(nbytes * reps / dt / 1e9, 3)
+                out["%s_%dx%d_%s" % (name, rows, cols, "f16" if f16 else "f32")] = res
+    finally:
+        oracle.set_num_threads(cores)
+    return out
+
+
+def measure_matmul_peaks(device, n=8192, reps=10):
+    """Dense tensor-core reference: torch.matmul of two n x n matrices in fp16
+    and in bf16, best of `reps` (burst), 2 n^3 flops."""
+    import torch
+    out = {}
+    for name, dt in (("fp16", torch.float16), ("bf16", torch.bfloat16)):
+        a = torch.randn((n, n), device=device).to(dt)
+        b = torch.randn((n, n), device=device).to(dt)
+        for _ in range(3):
+            torch.matmul(a, b)
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b)
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name + "_tflops"] = round(2.0 * n ** 3 / (best / 1e3) / 1e12, 1)
+        del a, b
+    return out
 
 
 def main_dequant_only(args):
@@ -667,8 +743,11 @@ def main_qp(args):
                                "tflops": round(l5.flops() / ms_c / 1e9, 1),
                                "note": "excludes the one-time f16 weight build"}}
             del l5
+            rows["matmul_peaks_8192"] = measure_matmul_peaks(device)
         if not args.no_cpu_baseline:
             cpu = cpu_oracle_sample(wl, seconds=args.cpu_seconds)
+            if rows is not None:
+                rows["cpu_oracle_dequant"] = cpu_dequant_rows()
 
     if rank == 0:
         line = {

@@ -85,6 +85,12 @@ def num_threads():
     return int(lib().qpo_num_threads())
 
 
+def set_num_threads(n):
+    """Threads of the oracle's OpenMP regions (parallelism only: every output
+    value is computed by one thread in a fixed order)."""
+    lib().qpo_set_num_threads(int(n))
+
+
 def f16_to_f32(h):
     h = np.ascontiguousarray(h, dtype=np.uint16)
     out = np.empty(h.shape, np.float32)
