@@ -378,12 +378,16 @@ template <int WO> struct Dec<kQ6_K, WO> {
 #pragma unroll
         for (int k = 0; k < 8; ++k) ql[8 + k] = t[k];
         row_words<128 + 4 * WO, 16, true>(row, hs16, qh);           // qh[0 .. 63]
+        // this half only ever needs crumbs j = h and j = 2 + h of each qh byte:
+        // keep them at bits 0..1 and 4..5 and clear the rest, so that each
+        // K step merges a word of 6-bit q with one shift and one select
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qh[k] = (qh[k] >> (2 * h)) & 0x33333333u;
     }
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
                                          const ChunkAddr &ca) const {
         constexpr int n = A / 2;
-        constexpr int nsh = (A % 2) ? 4 : 0;             // j >= 2: high nibble
         const pair_t nbias2 = pk2(-8388640.0f, -8388640.0f);     // -(2^23 + 32)
         const uint32_t sw = sc[A] >> (16 * h);
 #pragma unroll
@@ -397,10 +401,13 @@ template <int WO> struct Dec<kQ6_K, WO> {
                 uint32_t u[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const uint32_t qhw = qh[8 * n + 2 * c + k];
-                    // bits 2j..2j+1 of each qh byte moved to bits 4..5: j = 2(A%2) + h
-                    const uint32_t hb = ((A % 2) ? (qhw >> (2 * h)) : (qhw << (4 - 2 * h))) & 0x30303030u;
-                    u[k] = ((ql[8 * n + 2 * c + k] >> nsh) & 0x0F0F0F0Fu) | hb;
+                    // low four bits: the low (j < 2) or high nibble of the ql byte;
+                    // bits 4..5: crumb j = 2(A%2) + h of the qh byte (bits 0..1 of the
+                    // masked word for A even, bits 4..5 for A odd); bits 6..7 clear
+                    const uint32_t qhw = qh[8 * n + 2 * c + k], qlw = ql[8 * n + 2 * c + k];
+                    const uint32_t a = (A % 2) ? (qlw >> 4) : qlw;
+                    const uint32_t b = (A % 2) ? qhw : (qhw << 4);
+                    u[k] = (a & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
                 }
                 const uint2 lo = word_scaled(u[0], dl2, nbias2);
                 const uint2 hi = word_scaled(u[1], dl2, nbias2);
