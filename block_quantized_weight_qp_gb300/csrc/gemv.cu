@@ -26,9 +26,10 @@
 // the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
 // faster than one with twice the warps and ring.  In a step,
 // lane (g, c) (g = lane / 4, c = lane % 4) decodes runs 2c and 2c + 1 of
-// the step in weight rows g and g + 8 from the tile with the exact run
-// decoders (qp_runs.cuh), rounds them to fp16 and feeds each run's 32 values
-// to eight MMAs, four per MMA.  The MMA's K order is permuted: K slots 2c,
+// the step in weight rows g and g + 8 from the tile (Q2_K and Q6_K with
+// steps written out per type, the others with the exact run decoders of
+// qp_runs.cuh), rounds them to fp16 and feeds each run's 32 values to eight
+// MMAs, four per MMA.  The MMA's K order is permuted: K slots 2c,
 // 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3 of lane c's run in MMA i,
 // for A and B alike, so the sum over K is unchanged, each lane's A fragment
 // is its own decoded values and its B fragment is 4 consecutive values of
@@ -61,12 +62,11 @@ namespace {
 
 using namespace runs;
 
-// Bytes per block and 32-value runs per block (F16: a "block" of 32 values).
+// Bytes per block and 32-value runs per block (F16: a "block" of 32 values)
+// for the types decoded through the generic run decoders.
 template <int TYPE> struct Geom;
 template <> struct Geom<kQ4_K> { static constexpr int BB = 144, RPB = 8; };
 template <> struct Geom<kQ5_K> { static constexpr int BB = 176, RPB = 8; };
-template <> struct Geom<kQ2_K> { static constexpr int BB = 84, RPB = 8; };
-template <> struct Geom<kQ6_K> { static constexpr int BB = 210, RPB = 8; };
 template <> struct Geom<kQ8_0> { static constexpr int BB = 34, RPB = 1; };
 template <> struct Geom<kF16> { static constexpr int BB = 64, RPB = 1; };
 
@@ -89,23 +89,6 @@ __device__ __forceinline__ void run_f16(const typename RawOf<TYPE>::T &raw, int 
     }
 }
 
-// Q2_K straight to fp16: per 16-value sub-block, the four possible fp16
-// weights (q2k_tables: the same one-rounding f32 arithmetic, then the same
-// fp16 rounding), held byte-planar in two words; each value's 2-bit q then
-// selects its two bytes with byte permutes.
-template <>
-__device__ __forceinline__ void run_f16<kQ2_K>(const RawQ2K &raw, int t, uint32_t (&h)[16]) {
-    uint32_t plo[2], phi[2];
-    q2k_tables(raw.sb >> (16 * (t & 1)), h2f(raw.dd), h2f(raw.dd >> 16), plo, phi);   // scales[2t], scales[2t+1]
-    const int sh = 2 * (t & 3);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {                        // values 4i .. 4i + 3, sub-block i / 4
-        const uint32_t sel = ((raw.w[i] >> sh) & 0x03030303u) * 0x11u + 0x40404040u;   // q -> nibbles q, q + 4
-        h[2 * i] = __byte_perm(plo[i >> 2], phi[i >> 2], sel);
-        h[2 * i + 1] = __byte_perm(plo[i >> 2], phi[i >> 2], sel >> 16);
-    }
-}
-
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -113,6 +96,216 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// hi32(a * b) + c: one integer multiply-add.
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ----------------------------------------------------- Q2_K and Q6_K steps --
+// A consumer lane (g, c) decodes, in each step of 256 values, runs 2c and
+// 2c + 1 of weight rows g and g + 8.  For the two K-quants that dominate the
+// decode workloads the step is written out per type: a row's fields are read
+// from shared memory once for both runs, and each word of quants feeds the
+// MMAs of both runs as soon as it is decoded.  The MMA order is the one
+// described above: MMA k of run rho takes values 4k .. 4k + 3 of the run.
+
+// Q2_K tables of four sub-blocks whose scale bytes are the bytes of sw:
+// t01[s] = entries 0, 1 of sub-block s as a half2, t23[s] = entries 2, 3;
+// entry q = RN_f16(fma(d * sc, q, -(dmin * m))), each f32 operation rounded
+// once (the value formula of the K-quant page, "Q2_K" section), then fp16.
+// A byte-permute selector nibble 2q (2q + 1) then picks entry q's low (high)
+// byte from {t01, t23}.
+template <int P>
+__device__ __forceinline__ void q2k_pair_tables(uint32_t scw, uint32_t mw, pair_t d2, pair_t nd2, uint32_t (&t01)[4],
+                                                uint32_t (&t23)[4]) {
+    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+    const pair_t sc = fadd2(pk2(bias_float<2 * P>(scw), bias_float<2 * P + 1>(scw)), nbias);   // exact
+    const pair_t m = fadd2(pk2(bias_float<2 * P>(mw), bias_float<2 * P + 1>(mw)), nbias);
+    const pair_t dl = fmul2(d2, sc), nml = fmul2(nd2, m);
+    float x[4], y[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpk2(ffma2(dl, pk2(static_cast<float>(q), static_cast<float>(q)), nml), x[q], y[q]);
+    t01[2 * P] = h2_of(x[0], x[1]);
+    t23[2 * P] = h2_of(x[2], x[3]);
+    t01[2 * P + 1] = h2_of(y[0], y[1]);
+    t23[2 * P + 1] = h2_of(y[2], y[3]);
+}
+
+__device__ __forceinline__ void q2k_tables4(uint32_t sw, uint32_t dd, uint32_t (&t01)[4], uint32_t (&t23)[4]) {
+    const float d = h2f(dd), dmin = h2f(dd >> 16);
+    const pair_t d2 = pk2(d, d), nd2 = pk2(-dmin, -dmin);   // -(dmin * m) = (-dmin) * m: rounding is sign-symmetric
+    const uint32_t scw = sw & 0x0F0F0F0Fu, mw = (sw >> 4) & 0x0F0F0F0Fu;
+    q2k_pair_tables<0>(scw, mw, d2, nd2, t01, t23);
+    q2k_pair_tables<1>(scw, mw, d2, nd2, t01, t23);
+}
+
+// Four 2-bit quants (bits 0-1 of each byte of v) -> four fp16 weights of
+// sub-block s: the selectors 2q | (2q + 1) << 4 per value, for the low and
+// the high two bytes of v.
+__device__ __forceinline__ void q2k_pick(uint32_t v, uint32_t t01, uint32_t t23, uint32_t &h01, uint32_t &h23) {
+    h01 = __byte_perm(t01, t23, v * 0x22u + 0x10101010u);
+    h23 = __byte_perm(t01, t23, mad_hi(v, 0x00220000u, 0x1010u));   // (v * 0x22) >> 16, + 0x1010
+}
+
+// Q2_K (84-byte superblocks, 4-byte aligned in the stage): run t = 2c + rho
+// takes bits 2(t & 3) of qs[32(t >> 2) + l] and scale bytes 2t, 2t + 1; the
+// lane's two runs share the quant words and the scale word of bytes 4c .. 4c + 3.
+__device__ __forceinline__ void step_q2k(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
+                                         float (&d)[4], float (&e)[4]) {
+    uint32_t ta0[4], tb0[4], ta1[4], tb1[4];
+    q2k_tables4(Smem::u32(b0 + 4 * c), Smem::u32(b0 + 80), ta0, tb0);
+    q2k_tables4(Smem::u32(b1 + 4 * c), Smem::u32(b1 + 80), ta1, tb1);
+    const uint8_t *q0 = b0 + 16 + 32 * (c >> 1), *q1 = b1 + 16 + 32 * (c >> 1);
+    const int sh = 4 * (c & 1);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);       // run 2c, values 8u .. 8u + 7
+        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);   // run 2c + 1
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int k = 2 * u + hh, s = k >> 2;
+            const uint32_t w0 = Smem::u32(q0 + 4 * k) >> sh, w1 = Smem::u32(q1 + 4 * k) >> sh;
+            uint32_t a0, a1, a2, a3;
+            q2k_pick(w0 & 0x03030303u, ta0[s], tb0[s], a0, a2);
+            q2k_pick(w1 & 0x03030303u, ta1[s], tb1[s], a1, a3);
+            mma_16816(d, a0, a1, a2, a3, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
+            q2k_pick((w0 >> 2) & 0x03030303u, ta0[s + 2], tb0[s + 2], a0, a2);
+            q2k_pick((w1 >> 2) & 0x03030303u, ta1[s + 2], tb1[s + 2], a1, a3);
+            mma_16816(e, a0, a1, a2, a3, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
+        }
+    }
+}
+
+// Q6_K (210-byte superblocks, 2-byte aligned in the stage): run t = 2c + rho
+// takes the low (c even) or high (c odd) nibbles of ql[64(t >> 2) + 32 rho + l]
+// and bits 2(t & 3) of qh[32(t >> 2) + l], int8 scales 2t, 2t + 1; the two
+// runs share the qh words and the scale bytes 4c .. 4c + 3.
+// MIS: the superblock starts 2 bytes past a 4-byte boundary.  Its fields are
+// then read as the aligned words starting 2 bytes early, so assembled word
+// k holds values 4k - 2 .. 4k + 1 and a value's byte is taken from word k or
+// k + 1 (all reads stay inside the superblock).
+template <bool MIS>
+struct Q6Row {
+    static constexpr int NW = MIS ? 9 : 8;
+    uint32_t u0[NW], u1[NW];   // 6-bit quants of runs 2c, 2c + 1, one per byte
+    pair_t dl[4];              // d * scale of sub-blocks 4c .. 4c + 3, as pairs
+
+    __device__ __forceinline__ void load(const uint8_t *b, int c) {
+        const int o = MIS ? -2 : 0;
+        const uint8_t *ql = b + 64 * (c >> 1) + o, *qh = b + 128 + 32 * (c >> 1) + o;
+        const int hs = 4 * (c & 1);
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const uint32_t h = Smem::u32(qh + 4 * k) >> hs;
+            u0[k] = ((Smem::u32(ql + 4 * k) >> hs) & 0x0F0F0F0Fu) + ((h & 0x03030303u) << 4);
+            u1[k] = ((Smem::u32(ql + 32 + 4 * k) >> hs) & 0x0F0F0F0Fu) + ((h & 0x0C0C0C0Cu) << 2);
+        }
+        const uint32_t sw = MIS ? (Smem::u16(b + 192 + 4 * c) | (Smem::u16(b + 194 + 4 * c) << 16))
+                                : Smem::u32(b + 192 + 4 * c);
+        const float dd = h2f(Smem::u16(b + 208));
+        const pair_t nb = pk2(-8388736.0f, -8388736.0f);   // -(2^23 + 128): int8 = (byte ^ 0x80) - 128
+        const uint32_t sx = sw ^ 0x80808080u;
+        const pair_t s01 = fadd2(pk2(bias_float<0>(sx), bias_float<1>(sx)), nb);
+        const pair_t s23 = fadd2(pk2(bias_float<2>(sx), bias_float<3>(sx)), nb);
+        float s[4];
+        unpk2(s01, s[0], s[1]);
+        unpk2(s23, s[2], s[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float v = __fmul_rn(dd, s[i]);   // exact: 11 x 8 significant bits
+            dl[i] = pk2(v, v);
+        }
+    }
+};
+
+// A row read in the 2-byte offset form, brought to the aligned form (word k
+// = values 4k .. 4k + 3), for warps whose lanes' rows start differently.
+__device__ __forceinline__ void q6k_realign(const Q6Row<true> &a, Q6Row<false> &r) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        r.u0[k] = __funnelshift_r(a.u0[k], a.u0[k + 1], 16);
+        r.u1[k] = __funnelshift_r(a.u1[k], a.u1[k + 1], 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.dl[i] = a.dl[i];
+}
+
+// Values 4k .. 4k + 3 of a run's quant words -> two half2 words.
+template <bool MIS>
+__device__ __forceinline__ void q6k_word(const uint32_t *u, int k, pair_t dl, uint32_t &h01, uint32_t &h23) {
+    const pair_t nb = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
+    pair_t q01, q23;
+    if (MIS) {
+        q01 = pk2(bias_float<2>(u[k]), bias_float<3>(u[k]));
+        q23 = pk2(bias_float<0>(u[k + 1]), bias_float<1>(u[k + 1]));
+    } else {
+        q01 = pk2(bias_float<0>(u[k]), bias_float<1>(u[k]));
+        q23 = pk2(bias_float<2>(u[k]), bias_float<3>(u[k]));
+    }
+    h01 = f2h2(fmul2(dl, fadd2(q01, nb)));   // d * s * (q - 32): exact product, one rounding to fp16
+    h23 = f2h2(fmul2(dl, fadd2(q23, nb)));
+}
+
+// The MMAs of a step over two rows already read.  mma.sync needs the whole
+// warp: callers reach this with all 32 lanes.
+template <bool MIS>
+__device__ __forceinline__ void q6k_mma(const Q6Row<MIS> &r0, const Q6Row<MIS> &r1, const uint4 *xv, bool tok,
+                                        float (&d)[4], float (&e)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int k = 2 * u + hh, s = k >> 2;
+            uint32_t a0, a1, a2, a3;
+            q6k_word<MIS>(r0.u0, k, r0.dl[s], a0, a2);
+            q6k_word<MIS>(r1.u0, k, r1.dl[s], a1, a3);
+            mma_16816(d, a0, a1, a2, a3, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
+            q6k_word<MIS>(r0.u1, k, r0.dl[s + 2], a0, a2);
+            q6k_word<MIS>(r1.u1, k, r1.dl[s + 2], a1, a3);
+            mma_16816(e, a0, a1, a2, a3, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
+        }
+    }
+}
+
+// One Q6_K step.  Rows g and g + 8 start alike modulo 4 (8 row pitches
+// apart); with TMA tiles every row of a step starts alike too, so a warp's
+// lanes agree and the warp takes the form of its rows' offset.  Rows staged
+// by one copy each can disagree from lane to lane: then each lane reads its
+// rows in its own form, brings them to the aligned one, and the warp's MMAs
+// run together afterwards.
+__device__ __forceinline__ void step_q6k(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
+                                         float (&d)[4], float (&e)[4]) {
+    const bool mis = (smem_u32(b0) & 2u) != 0u;
+    if (__all_sync(0xffffffffu, mis)) {
+        Q6Row<true> r0, r1;
+        r0.load(b0, c);
+        r1.load(b1, c);
+        q6k_mma<true>(r0, r1, xv, tok, d, e);
+    } else if (!__any_sync(0xffffffffu, mis)) {
+        Q6Row<false> r0, r1;
+        r0.load(b0, c);
+        r1.load(b1, c);
+        q6k_mma<false>(r0, r1, xv, tok, d, e);
+    } else {
+        Q6Row<false> r0, r1;
+        if (mis) {
+            Q6Row<true> a;
+            a.load(b0, c);
+            q6k_realign(a, r0);
+            a.load(b1, c);
+            q6k_realign(a, r1);
+        } else {
+            r0.load(b0, c);
+            r1.load(b1, c);
+        }
+        q6k_mma<false>(r0, r1, xv, tok, d, e);
+    }
 }
 
 constexpr int ROWS = 16;                      // weight rows per block (the MMA's M)
@@ -274,8 +467,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
             const BlockLoc L = block_loc<TYPE>(gp, b);
             const GemvGroup &P = gp.g[L.grp];
-            const int nruns = (P.in_f + 31) / 32;
-            const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
             // rows g, g + 8: the row's start modulo 16 (0 when staged by TMA)
             const int base0 = P.use_tma ? 0
                                         : static_cast<int>((reinterpret_cast<uintptr_t>(P.W) +
@@ -295,35 +486,43 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                     const uint8_t *slot = ring + s * TILE;
                     const uint8_t *src0 = slot + g * S::PITCH + ((base0 + off) & 15) + sl * S::STEP;
                     const uint8_t *src1 = slot + (g + 8) * S::PITCH + ((base1 + off) & 15) + sl * S::STEP;
+                    if constexpr (TYPE == kQ2_K) {
+                        step_q2k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
+                    } else if constexpr (TYPE == kQ6_K) {
+                        step_q6k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
+                    } else {
+                        const int nruns = (P.in_f + 31) / 32;
+                        const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
 #pragma unroll
-                    for (int rho = 0; rho < 2; ++rho) {
-                        const int t = 2 * c + rho;        // this lane's run of the step
-                        const int jr = 8 * q + t;         // ... and of the row
-                        const bool valid = jr < nruns;
-                        uint32_t h0[16], h1[16];
-                        if (valid && row0) {
-                            Raw raw;
-                            raw.template load<Smem>(src0 + (t / G::RPB) * G::BB, t % G::RPB);
-                            run_f16<TYPE>(raw, t % G::RPB, h0);
-                        } else {
+                        for (int rho = 0; rho < 2; ++rho) {
+                            const int t = 2 * c + rho;        // this lane's run of the step
+                            const int jr = 8 * q + t;         // ... and of the row
+                            const bool valid = jr < nruns;
+                            uint32_t h0[16], h1[16];
+                            if (valid && row0) {
+                                Raw raw;
+                                raw.template load<Smem>(src0 + (t / G::RPB) * G::BB, t % G::RPB);
+                                run_f16<TYPE>(raw, t % G::RPB, h0);
+                            } else {
 #pragma unroll
-                            for (int p = 0; p < 16; ++p) h0[p] = 0u;
-                        }
-                        if (valid && row1) {
-                            Raw raw;
-                            raw.template load<Smem>(src1 + (t / G::RPB) * G::BB, t % G::RPB);
-                            run_f16<TYPE>(raw, t % G::RPB, h1);
-                        } else {
+                                for (int p = 0; p < 16; ++p) h0[p] = 0u;
+                            }
+                            if (valid && row1) {
+                                Raw raw;
+                                raw.template load<Smem>(src1 + (t / G::RPB) * G::BB, t % G::RPB);
+                                run_f16<TYPE>(raw, t % G::RPB, h1);
+                            } else {
 #pragma unroll
-                            for (int p = 0; p < 16; ++p) h1[p] = 0u;
-                        }
-                        const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * jr);
-                        float (&acc)[4] = rho ? e : d;
+                                for (int p = 0; p < 16; ++p) h1[p] = 0u;
+                            }
+                            const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * jr);
+                            float (&acc)[4] = rho ? e : d;
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {     // 8 values of X per 16-byte load: two MMAs
-                            const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
-                            mma_16816(acc, h0[4 * u], h1[4 * u], h0[4 * u + 1], h1[4 * u + 1], x.x, x.y);
-                            mma_16816(acc, h0[4 * u + 2], h1[4 * u + 2], h0[4 * u + 3], h1[4 * u + 3], x.z, x.w);
+                            for (int u = 0; u < 4; ++u) {     // 8 values of X per 16-byte load: two MMAs
+                                const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
+                                mma_16816(acc, h0[4 * u], h1[4 * u], h0[4 * u + 1], h1[4 * u + 1], x.x, x.y);
+                                mma_16816(acc, h0[4 * u + 2], h1[4 * u + 2], h0[4 * u + 3], h1[4 * u + 3], x.z, x.w);
+                            }
                         }
                     }
                 }

@@ -79,10 +79,14 @@ def test_gemm_random_fields_vs_oracle(cuda_device, tiling, qtype):
     assert_gemm_within_tolerance(Y.cpu().numpy(), Yref, A, "random fields %s" % ID[qtype])
 
 
+@pytest.mark.parametrize("in_f", [2048, 1280], ids=["tma_tiles", "row_copies"])
 @pytest.mark.parametrize("qtype", QUANT_TYPES, ids=lambda q: ID[q])
-def test_gemv_one_hot_over_every_column(cuda_device, qtype):
+def test_gemv_one_hot_over_every_column(cuda_device, qtype, in_f):
+    """Every weight of every row, exactly.  With 1280 values a Q2_K or Q6_K
+    row is not a whole number of 16-byte words, so the rows are staged by one
+    copy each and (Q6_K) every other row starts 2 bytes past a word."""
     t = torch()
-    out_f, in_f, T = 72, 2048, 8
+    out_f, T = 72, 8
     w, W16 = weights(qtype, out_f, in_f, seed=43)
     Wd = dev(w)
     n = in_f // T

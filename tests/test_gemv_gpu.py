@@ -27,6 +27,8 @@ CASES = [
     (qp.Q2_K, 1029, 1024, 7),        # 65 row blocks of 16, the last with 5 rows
     (qp.F16, 24, 13056, 8),          # 408 runs: a partial last step
     (qp.Q8_0, 16, 4128, 6),          # 129 runs
+    (qp.Q2_K, 48, 768, 3),           # rows of 252 bytes: staged by one copy per row
+    (qp.Q6_K, 40, 1280, 2),          # rows of 1050 bytes: odd rows start 2 bytes past a word
 ]
 
 
