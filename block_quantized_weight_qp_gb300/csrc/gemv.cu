@@ -22,7 +22,8 @@
 // (S x 256 values) of one K range, as the 16-byte aligned cover of that range
 // in every row (up to 2 KB per row, so that the copies are long).  Eight
 // consumer warps split the tiles: warp w takes step w % S of every tile its
-// team w / S is given (the teams take a block's tiles in turn).  Measured on
+// team w / S is given (the teams take a block's tiles in turn); every
+// consumer warp still waits for and releases every tile.  Measured on
 // the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
 // faster than one with twice the warps and ring.  In a step,
 // lane (g, c) (g = lane / 4, c = lane % 4) decodes runs 2c and 2c + 1 of
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::NST; ++s) {
             mbar_init(&full[s], 1);                       // the producer's arrive + the bytes
-            mbar_init(&empty[s], S::S);                   // the team that reads the tile
+            mbar_init(&empty[s], NC);                     // every consumer warp, whichever team reads it
         }
         stop_word = 0u;
         drain_failed = 0u;
@@ -475,13 +476,17 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                                         : static_cast<int>((reinterpret_cast<uintptr_t>(P.W) +
                                                             static_cast<uint64_t>(L.m0 + g + 8) * P.row_bytes) & 15);
             const uint16_t *xrow = P.X + static_cast<int64_t>(tok ? g : 0) * P.in_f;
-            for (int j = team; j < L.ntiles; j += TEAMS) {
+            for (int j = 0; j < L.ntiles; ++j) {
+                // Every consumer warp waits for every tile and releases it, also
+                // the tiles another team reads: a warp that skipped ring rounds
+                // could meet a slot's barrier two phases on, where a parity wait
+                // no longer tells the phases apart.
                 const int n = n0 + j, s = n % S::NST;
                 live = live && wait_phase_warp(&full[s], static_cast<uint32_t>((n / S::NST) & 1), gp.limit_ns, stop,
                                                gp.err, kErrTimeoutGemv);
                 if (!live) continue;
                 const int q = j * S::S + sl;              // this warp's step of the row
-                if (q < L.nsteps) {
+                if (j % TEAMS == team && q < L.nsteps) {
                     const int off = j * S::S * S::STEP;
                     const uint8_t *slot = ring + s * TILE;
                     const uint8_t *src0 = slot + g * S::PITCH + ((base0 + off) & 15) + sl * S::STEP;
