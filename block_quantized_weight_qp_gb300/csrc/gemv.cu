@@ -99,13 +99,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// hi32(a * b) + c: one integer multiply-add.
-__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // ----------------------------------------------------- Q2_K and Q6_K steps --
 // A consumer lane (g, c) decodes, in each step of 256 values, runs 2c and
 // 2c + 1 of weight rows g and g + 8.  For the two K-quants that dominate the
@@ -148,8 +141,8 @@ __device__ __forceinline__ void q2k_tables4(uint32_t sw, uint32_t dd, uint32_t (
 // sub-block s: the selectors 2q | (2q + 1) << 4 per value, for the low and
 // the high two bytes of v.
 __device__ __forceinline__ void q2k_pick(uint32_t v, uint32_t t01, uint32_t t23, uint32_t &h01, uint32_t &h23) {
-    h01 = __byte_perm(t01, t23, v * 0x22u + 0x10101010u);
-    h23 = __byte_perm(t01, t23, mad_hi(v, 0x00220000u, 0x1010u));   // (v * 0x22) >> 16, + 0x1010
+    h01 = prmt_sel(t01, t23, v * 0x22u + 0x10101010u);
+    h23 = prmt_sel(t01, t23, mad_hi(v, 0x00220000u, 0x1010u));   // (v * 0x22) >> 16, + 0x1010
 }
 
 // Q2_K (84-byte superblocks, 4-byte aligned in the stage): run t = 2c + rho

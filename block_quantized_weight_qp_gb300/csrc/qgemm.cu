@@ -330,8 +330,9 @@ template <int WO> struct Dec<kQ2_K, WO> {
     }
     // 4 crumb values in the bytes of u -> 2 half2
     __device__ __forceinline__ static uint2 pick(uint32_t u, uint32_t plo, uint32_t phi) {
-        const uint32_t sel = u * 0x11u + 0x40404040u;     // byte q -> nibbles (q, q + 4)
-        return make_uint2(__byte_perm(plo, phi, sel), __byte_perm(plo, phi, sel >> 16));
+        // byte q -> nibbles (q, q + 4); the high half's selector (u * 0x11) >> 16
+        // + 0x4040 comes from the multiply's high word
+        return make_uint2(prmt_sel(plo, phi, u * 0x11u + 0x40404040u), prmt_sel(plo, phi, mad_hi(u, 0x110000u, 0x4040u)));
     }
     template <int A>
     __device__ __forceinline__ void atom(const uint8_t *, uint32_t, int h, uint32_t tile,
@@ -463,21 +464,33 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty);
     }
-#define QP_DEQUANT_ATOM(A)                                                                                     \
+    // The atoms go in pairs: both stages are written, then one proxy fence
+    // makes the pair's stores visible to the tensor cores before either
+    // stage's arrive (one fence per atom measured 1.2% slower on the Q6_K
+    // down projection).  The second stage's wait needs no arrive of the first:
+    // the ring is at least two stages deep.
+#define QP_DEQUANT_PAIR(A)                                                                                     \
     {                                                                                                          \
+        const int s0 = stage;                                                                                  \
         if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.stop, err, kErrTimeoutDequant)) \
             return false;                                                                                      \
         dec.template atom<A>(row, hs16, p, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);         \
+        advance(stage, phase, S);                                                                              \
+        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.stop, err, kErrTimeoutDequant)) \
+            return false;                                                                                      \
+        dec.template atom<A + 1>(row, hs16, p, ws_addr + static_cast<uint32_t>(stage * W_STAGE_BYTES), ca);     \
         fence_proxy_async_smem();                                                                              \
         __syncwarp();                                                                                          \
-        if (lane == 0) mbar_arrive(&sh.fullw[stage]);                                                          \
+        if (lane == 0) {                                                                                       \
+            mbar_arrive(&sh.fullw[s0]);                                                                        \
+            mbar_arrive(&sh.fullw[stage]);                                                                     \
+        }                                                                                                      \
         advance(stage, phase, S);                                                                              \
     }
-    QP_DEQUANT_ATOM(0)
-    QP_DEQUANT_ATOM(1)
-    QP_DEQUANT_ATOM(2)
-    QP_DEQUANT_ATOM(3)
-#undef QP_DEQUANT_ATOM
+    static_assert(S >= 2, "a pair of atoms needs two W stages");
+    QP_DEQUANT_PAIR(0)
+    QP_DEQUANT_PAIR(2)
+#undef QP_DEQUANT_PAIR
     return true;
 }
 

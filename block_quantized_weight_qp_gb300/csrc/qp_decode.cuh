@@ -80,6 +80,24 @@ __device__ __forceinline__ float bias_float(uint32_t u) {
     return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440 + I));
 }
 
+// Byte permute with a selector computed at run time.  __byte_perm ignores
+// bit 3 of each selector nibble, so for a run-time selector the compiler
+// clears those bits first, an extra instruction per permute; the selectors
+// used here never set them (nibbles 0..7), so the PTX permute takes them as
+// they are.
+__device__ __forceinline__ uint32_t prmt_sel(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// hi32(a * b) + c: one integer multiply-add.
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Unpack a pair into two floats.
 #ifndef QP_SCALAR_PAIRS
 __device__ __forceinline__ void unpk2(pair_t v, float &lo, float &hi) {
