@@ -126,6 +126,7 @@ struct Shared {
     uint32_t *tmem_base;
     Stop stop;
     volatile uint32_t *drain_failed;     // a wait for the CTA's own copies or MMAs ran out
+    uint32_t fullw_remote = 0;           // second CTA of a pair: shared::cluster address of the first CTA's fullw
 };
 
 // A launch runs up to MAX_GROUPS projections of one weight type over the
@@ -482,8 +483,13 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
         fence_proxy_async_smem();                                                                              \
         __syncwarp();                                                                                          \
         if (lane == 0) {                                                                                       \
-            mbar_arrive(&sh.fullw[s0]);                                                                        \
-            mbar_arrive(&sh.fullw[stage]);                                                                     \
+            if (sh.fullw_remote) {                                                                             \
+                mbar_arrive_remote(sh.fullw_remote + static_cast<uint32_t>(s0 * 8));                           \
+                mbar_arrive_remote(sh.fullw_remote + static_cast<uint32_t>(stage * 8));                        \
+            } else {                                                                                           \
+                mbar_arrive(&sh.fullw[s0]);                                                                    \
+                mbar_arrive(&sh.fullw[stage]);                                                                 \
+            }                                                                                                  \
         }                                                                                                      \
         advance(stage, phase, S);                                                                              \
     }
@@ -971,11 +977,14 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
 // weight rows x 256 tokens; CTA r decodes weight rows m0 + 128r (its half of
 // A) into its own shared memory exactly as the single-CTA kernel does, and
 // stages tokens n0 + 128r (its half of B) with the pair form of TMA.  The
-// leader's MMA thread waits for the token halves (TMA bytes on its fullx),
-// its own decode warps (fullw) and the peer's (peerw: one arrival per stage
-// from the peer's forwarding thread, which waits on the peer's own fullw),
-// issues the M = 256 MMAs and multicasts its commits: the stages' emptyx /
-// emptyw and the accumulators' accfull in both CTAs.
+// leader's MMA thread waits for the token halves (TMA bytes on its fullx)
+// and for the decoded stage of both CTAs (its fullw counts the leader's eight
+// decode warps and the peer's eight, which arrive remotely, each after its
+// stores were made visible to the tensor cores), issues the M = 256 MMAs and
+// multicasts its commits: the stages' emptyx / emptyw and the accumulators'
+// accfull in both CTAs.  (A forwarding thread in the peer that waited on the
+// peer's own barrier and passed one arrival on measured 2% slower on the
+// Q2_K launch.)
 // Ring depths and epilogue staging buffers per warp.  The token ring (16 KiB
 // stages) is the one that pays for depth (measured on the Q2_K / Q6_K layer:
 // 4 -> 6 -> 8 stages, +5% then +0.5%); more fp16 W stages or a second slice
@@ -995,8 +1004,8 @@ template <int TYPE> struct PairFCfg {
     static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
     static constexpr int OFF_EPI = OFF_Q + QST * Q_SLOT_BYTES;   // 4 epilogue warps x EPI x 4 KiB
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI * 4096;
-    // fullx, emptyx, fullw, emptyw, peerw, qfull, qempty, accfull[2], accempty[2], done
-    static constexpr int NBAR = 2 * XST + 3 * WST + 2 * QST + 5;
+    // fullx, emptyx, fullw, emptyw, qfull, qempty, accfull[2], accempty[2], done
+    static constexpr int NBAR = 2 * XST + 2 * WST + 2 * QST + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(OFF_Q % 1024 == 0 && OFF_EPI % 128 == 0 && SMEM_BYTES <= 232448, "shared memory layout");
@@ -1017,8 +1026,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
     sh.emptyx = bars + XS;
     sh.fullw = bars + 2 * XS;
     sh.emptyw = sh.fullw + WS;
-    uint64_t *peerw = sh.emptyw + WS;
-    sh.qfull = peerw + WS;
+    sh.qfull = sh.emptyw + WS;
     sh.qempty = sh.qfull + QS;
     sh.accfull = sh.qempty + QS;
     sh.accempty = sh.accfull + 2;
@@ -1029,6 +1037,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
         sh.stop = Stop{flag, mapa_shared(smem_u32(const_cast<uint32_t *>(flag)), rank ^ 1u)};
     }
     sh.drain_failed = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 8);
+    if (rank == 1) sh.fullw_remote = mapa_shared(smem_u32(sh.fullw), 0u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -1037,9 +1046,8 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             mbar_init(&sh.emptyx[s], 1);           // the leader's multicast commit
         }
         for (int s = 0; s < WS; ++s) {
-            mbar_init(&sh.fullw[s], C::DQ_WARPS);  // this CTA's decode warps
+            mbar_init(&sh.fullw[s], 2 * C::DQ_WARPS);  // leader: both CTAs' decode warps (the peer's: unused)
             mbar_init(&sh.emptyw[s], 1);           // the leader's multicast commit
-            mbar_init(&peerw[s], 1);               // leader: the peer's forwarding thread
         }
         for (int s = 0; s < QS; ++s) {
             mbar_init(&sh.qfull[s], 1);
@@ -1131,8 +1139,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int k = 0; k < nks; ++k) {
                     if (!wait_phase(&sh.fullx[stage], phase, limit_ns, sh.stop, err, kErrTimeoutMma) ||
-                        !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma) ||
-                        !wait_phase(&peerw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma))
+                        !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma))
                         goto mma_done;
                     tc_fence_after();
                     const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wstage * W_STAGE_BYTES));
@@ -1156,24 +1163,6 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                 *sh.drain_failed = 1u;
                 atomicOr(err, kErrTimeoutMma);
             }
-        } else if (lane == 0) {
-            // ----------------------------------- forwarding thread (peer) --
-            // one arrival on the leader's peerw per stage this CTA's decode
-            // warps complete (their stores were made visible to the tensor
-            // cores before they arrived; the release carries them on)
-            const uint32_t peerw_leader = mapa_shared(smem_u32(peerw), 0u);
-            int wstage = 0;
-            uint32_t wphase = 0;
-            for (int tile = first; tile < gp.num_tiles; tile += stride) {
-                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
-                for (int k = 0; k < nks; ++k) {
-                    if (!wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutDequant))
-                        goto fwd_done;
-                    mbar_arrive_remote(peerw_leader + static_cast<uint32_t>(wstage * 8));
-                    advance(wstage, wphase, WS);
-                }
-            }
-        fwd_done:;
         }
         __syncwarp();
     } else if (alloc_ok && warp < 6) {
