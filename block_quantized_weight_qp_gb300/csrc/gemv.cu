@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
     }
     __syncthreads();
     grid_dependency_wait();                               // the previous grid's memory operations are done
+    grid_launch_dependents();                             // the next grid may launch; it still waits for this one
     const int nblk = gp.g[gp.n - 1].blk_end;
 
     if (warp == NC) {
