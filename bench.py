@@ -346,11 +346,12 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
 
 def bench_gemv(qp, layer, stream, device, peaks, steps=20):
     """The decode GEMV over the layer's seven weights for T = 1 and 8 token
-    rows, as one grouped launch per block type (qp_decode_gemv_group: the six
-    Q2_K projections, then the Q6_K down projection), captured in a CUDA
-    graph as a decode loop would run it.  Also timed: the same launches made
-    eagerly, and the seven projections launched one at a time (graph).  The
-    weights (88 MB here) would fit in L2, so before every timed step a 256 MB
+    rows, as one grouped launch per block type (qp_decode_gemv_group; for the
+    Q2_K layer the six Q2_K projections, then the Q6_K down projection),
+    captured in a CUDA graph as a decode loop would run it.  Also timed: the
+    same launches made eagerly, and the seven projections launched one at a
+    time (graph).  The weights (88 MB for the Q2_K layer, 155-189 MB for the
+    Q4_K and Q5_K ones) fit in L2 or nearly, so before every timed step a 256 MB
     buffer is written (outside the timed region: events bracket the GEMV
     launches of each step only).  GB/s counts the weight bytes plus the X and
     Y bytes of a step.
@@ -760,6 +761,7 @@ def main_qp(args):
             ms5k = time_layer(qp, l5k, stream, max(5, args.steps // 2), 3)
             rows["qwen3_8b_q5k_t8192"] = {"ms": round(ms5k, 4), "tflops": round(l5k.flops() / ms5k / 1e9, 1),
                                           "tok_per_s": round(l5k.T / ms5k * 1e3, 1)}
+            rows["decode_gemv_qwen3_8b_q5k"] = bench_gemv(qp, l5k, stream, device, peaks)
             del l5k
             rows["decode_gemv_" + args.workload] = bench_gemv(qp, layer, stream, device, peaks)
             wl5 = workloads.WORKLOADS["qwen3_8b_q4k_t31258_chunk4864"]
@@ -772,6 +774,7 @@ def main_qp(args):
                 "cached_f16": {"ms": round(ms_c, 3), "tok_per_s": round(l5.T / ms_c * 1e3, 1),
                                "tflops": round(l5.flops() / ms_c / 1e9, 1),
                                "note": "excludes the one-time f16 weight build"}}
+            rows["decode_gemv_qwen3_8b_q4k"] = bench_gemv(qp, l5, stream, device, peaks)
             del l5
             rows["matmul_peaks_8192"] = measure_matmul_peaks(device)
         if not args.no_cpu_baseline:

@@ -27,8 +27,8 @@
 // the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
 // faster than one with twice the warps and ring.  In a step,
 // lane (g, c) (g = lane / 4, c = lane % 4) decodes runs 2c and 2c + 1 of
-// the step in weight rows g and g + 8 from the tile (Q2_K and Q6_K with
-// steps written out per type, the others with the exact run decoders of
+// the step in weight rows g and g + 8 from the tile (the K-quants with
+// steps written out per type, Q8_0 and F16 with the exact run decoders of
 // qp_runs.cuh), rounds them to fp16 and feeds each run's 32 values to eight
 // MMAs, four per MMA.  The MMA's K order is permuted: K slots 2c,
 // 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3 of lane c's run in MMA i,
@@ -66,8 +66,6 @@ using namespace runs;
 // Bytes per block and 32-value runs per block (F16: a "block" of 32 values)
 // for the types decoded through the generic run decoders.
 template <int TYPE> struct Geom;
-template <> struct Geom<kQ4_K> { static constexpr int BB = 144, RPB = 8; };
-template <> struct Geom<kQ5_K> { static constexpr int BB = 176, RPB = 8; };
 template <> struct Geom<kQ8_0> { static constexpr int BB = 34, RPB = 1; };
 template <> struct Geom<kF16> { static constexpr int BB = 64, RPB = 1; };
 
@@ -101,8 +99,8 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 
 // ----------------------------------------------------- Q2_K and Q6_K steps --
 // A consumer lane (g, c) decodes, in each step of 256 values, runs 2c and
-// 2c + 1 of weight rows g and g + 8.  For the two K-quants that dominate the
-// decode workloads the step is written out per type: a row's fields are read
+// 2c + 1 of weight rows g and g + 8.  For the K-quants the step is written
+// out per type: a row's fields are read
 // from shared memory once for both runs, and each word of quants feeds the
 // MMAs of both runs as soon as it is decoded.  The MMA order is the one
 // described above: MMA k of run rho takes values 4k .. 4k + 3 of the run.
@@ -302,6 +300,78 @@ __device__ __forceinline__ void step_q6k(const uint8_t *b0, const uint8_t *b1, i
     }
 }
 
+// Q4_K / Q5_K (144- / 176-byte superblocks, 16-byte aligned in the stage):
+// run t is sub-block t: the low (t even) or high (t odd) nibbles of
+// qs[32(t >> 1) + l], Q5_K's fifth bit being bit t of qh[l].  The lane's runs
+// 2c and 2c + 1 share the 32 bytes qs[32c ..] (and qh[0 .. 31]).  Scales:
+// the 6-bit (sc, m) of sub-block t from the packed scale bytes, dl = d * sc
+// and nml = -(dmin * m), each rounded once; a value is fma(dl, q, nml),
+// rounded to fp16 (the K-quant page's value formula, as the run decoders).
+__device__ __forceinline__ void k4_run_scales(const uint4 &hd, int t, pair_t &dl2, pair_t &nml2) {
+    const int sh = 8 * (t & 3);
+    const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
+    const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
+    const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
+    const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
+    const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
+    dl2 = pk2(dl, dl);
+    nml2 = pk2(nml, nml);
+}
+
+template <bool Q5>
+struct K4Row {
+    pair_t dla, nmla, dlb, nmlb;   // runs 2c (a) and 2c + 1 (b)
+    uint32_t q[8], h[Q5 ? 8 : 1];
+
+    __device__ __forceinline__ void load(const uint8_t *b, int c) {
+        const uint4 hd = Smem::u128(b);
+        k4_run_scales(hd, 2 * c, dla, nmla);
+        k4_run_scales(hd, 2 * c + 1, dlb, nmlb);
+        const uint8_t *qs = b + (Q5 ? 48 : 16) + 32 * c;
+        const uint4 q0 = Smem::u128(qs), q1 = Smem::u128(qs + 16);
+        q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
+        q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
+        if constexpr (Q5) {
+            const uint4 h0 = Smem::u128(b + 16), h1 = Smem::u128(b + 32);
+            h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
+            h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
+        }
+    }
+    // 4-value quant words of word k for runs a and b
+    __device__ __forceinline__ void quants(int k, int c, uint32_t &ua, uint32_t &ub) const {
+        ua = q[k] & 0x0F0F0F0Fu;
+        ub = (q[k] >> 4) & 0x0F0F0F0Fu;
+        if constexpr (Q5) {
+            ua |= ((h[k] >> (2 * c)) & 0x01010101u) << 4;
+            ub |= ((h[k] >> (2 * c + 1)) & 0x01010101u) << 4;
+        }
+    }
+};
+
+template <bool Q5>
+__device__ __forceinline__ void step_k4(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
+                                        float (&d)[4], float (&e)[4]) {
+    K4Row<Q5> r0, r1;
+    r0.load(b0, c);
+    r1.load(b1, c);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int k = 2 * u + hh;
+            uint32_t ua0, ub0, ua1, ub1;
+            r0.quants(k, c, ua0, ub0);
+            r1.quants(k, c, ua1, ub1);
+            const uint2 p0 = word_affine(ua0, r0.dla, r0.nmla), p1 = word_affine(ua1, r1.dla, r1.nmla);
+            mma_16816(d, p0.x, p1.x, p0.y, p1.y, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
+            const uint2 q0 = word_affine(ub0, r0.dlb, r0.nmlb), q1 = word_affine(ub1, r1.dlb, r1.nmlb);
+            mma_16816(e, q0.x, q1.x, q0.y, q1.y, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
+        }
+    }
+}
+
 constexpr int ROWS = 16;                      // weight rows per block (the MMA's M)
 constexpr int STEP_VALUES = 256;              // values of a row per step (8 runs)
 constexpr int NC = 8;                         // consumer warps per CTA
@@ -489,6 +559,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                         step_q2k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
                     } else if constexpr (TYPE == kQ6_K) {
                         step_q6k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
+                    } else if constexpr (TYPE == kQ4_K || TYPE == kQ5_K) {
+                        step_k4<TYPE == kQ5_K>(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c),
+                                               tok, d, e);
                     } else {
                         const int nruns = (P.in_f + 31) / 32;
                         const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
