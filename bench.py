@@ -403,6 +403,9 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
         nl = len(layer.launches(True))
         evl = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
                for _ in range(steps)]
+        for _ in range(3):                       # untimed warm-up
+            flush_l2()
+            grouped(stream)
         for s_ev in evl:
             flush_l2()
             for k, (qt, idx) in enumerate(layer.launches(True)):
@@ -419,6 +422,12 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
                 "us": round(us, 2), "weight_bytes": wb, "weight_gbs": round(wb / (us / 1e6) / 1e9, 1)}
         res = {}
         for how in ("grouped", "single", "eager"):
+            for _ in range(3):                   # untimed warm-up of this way of launching
+                flush_l2()
+                if how == "eager":
+                    grouped(stream)
+                else:
+                    graphs[how].replay()
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
             for e0, e1 in ev:
                 flush_l2()
@@ -757,15 +766,19 @@ def main_qp(args):
             rows["qwen3_1p7b_q4k_t2048"] = {"ms": round(ms17, 4), "tflops": round(l17.flops() / ms17 / 1e9, 1),
                                             "tok_per_s": round(l17.T / ms17 * 1e3, 1)}
             del l17
+            # The decode GEMV rows run before the seconds-long GEMM rows of
+            # their layer: right after those, the GPU measured slower for a
+            # few dozen microsecond-long steps.
+            rows["decode_gemv_" + args.workload] = bench_gemv(qp, layer, stream, device, peaks)
             l5k = Layer(workloads.WORKLOADS["qwen3_8b_q5k_t8192"], rank, device)
+            rows["decode_gemv_qwen3_8b_q5k"] = bench_gemv(qp, l5k, stream, device, peaks)
             ms5k = time_layer(qp, l5k, stream, max(5, args.steps // 2), 3)
             rows["qwen3_8b_q5k_t8192"] = {"ms": round(ms5k, 4), "tflops": round(l5k.flops() / ms5k / 1e9, 1),
                                           "tok_per_s": round(l5k.T / ms5k * 1e3, 1)}
-            rows["decode_gemv_qwen3_8b_q5k"] = bench_gemv(qp, l5k, stream, device, peaks)
             del l5k
-            rows["decode_gemv_" + args.workload] = bench_gemv(qp, layer, stream, device, peaks)
             wl5 = workloads.WORKLOADS["qwen3_8b_q4k_t31258_chunk4864"]
             l5 = Layer(wl5, rank, device, need_f16=True)
+            rows["decode_gemv_qwen3_8b_q4k"] = bench_gemv(qp, l5, stream, device, peaks)
             ms_f = time_layer(qp, l5, stream, 3, 1, mode="fused", chunk=wl5["chunk"])
             ms_c = time_layer(qp, l5, stream, 3, 1, mode="cached", chunk=wl5["chunk"])
             rows["qwen3_8b_q4k_t31258_chunk4864"] = {
@@ -774,7 +787,6 @@ def main_qp(args):
                 "cached_f16": {"ms": round(ms_c, 3), "tok_per_s": round(l5.T / ms_c * 1e3, 1),
                                "tflops": round(l5.flops() / ms_c / 1e9, 1),
                                "note": "excludes the one-time f16 weight build"}}
-            rows["decode_gemv_qwen3_8b_q4k"] = bench_gemv(qp, l5, stream, device, peaks)
             del l5
             rows["matmul_peaks_8192"] = measure_matmul_peaks(device)
         if not args.no_cpu_baseline:
