@@ -84,7 +84,7 @@ template <> struct QFmt<kQ5_K> { static constexpr int SB_BYTES = 176, BOX = 176;
 template <> struct QFmt<kQ2_K> { static constexpr int SB_BYTES = 84, BOX = 112; };
 template <> struct QFmt<kQ6_K> { static constexpr int SB_BYTES = 210, BOX = 240; };
 template <> struct QFmt<kQ8_0> { static constexpr int SB_BYTES = 272, BOX = 272; };  // 8 blocks
-template <> struct QFmt<0> { static constexpr int SB_BYTES = 0, BOX = 0; };            // fp16 weight
+template <> struct QFmt<0> { static constexpr int BOX = 0; };                           // fp16 weight
 
 // Pipeline depths.  X tiles (TMA), fp16 W tiles (written by the dequant
 // warps in fused mode) and quantized slices (TMA, one superblock = four K
@@ -96,15 +96,17 @@ template <> struct Depth<kQ6_K> { static constexpr int XST = 4, WST = 3, QST = 1
 template <> struct Depth<kQ8_0> { static constexpr int XST = 3, WST = 3, QST = 2; };
 template <> struct Depth<0> { static constexpr int XST = 4, WST = 4, QST = 0; };
 
+// Decode warps per CTA.  In a CTA that issues MMAs they sit only on SM
+// sub-partitions 0, 2 and 3 (warp w runs on sub-partition w % 4):
+// sub-partition 1 keeps its issue slots for the single MMA-issuing thread of
+// warp 1.  Warps 6..15 minus 9 and 13.
+constexpr int kDecodeWarps = 8;
+
 template <int TYPE> struct Cfg {
     static constexpr bool FUSED = TYPE != 0;
     static constexpr int XST = Depth<TYPE>::XST;
     static constexpr int WST = Depth<TYPE>::WST;
     static constexpr int QST = Depth<TYPE>::QST;
-    // Dequant warps sit only on SM sub-partitions 0, 2 and 3 (warp w runs on
-    // sub-partition w % 4): sub-partition 1 keeps its issue slots for the
-    // single MMA-issuing thread of warp 1.  Warps 6..15 minus 9 and 13.
-    static constexpr int DQ_WARPS = FUSED ? 8 : 0;
     static constexpr int THREADS = FUSED ? 16 * 32 : 6 * 32;
     static constexpr int Q_SLOT_BYTES = FUSED ? BM * QFmt<TYPE>::BOX : 0;
     static constexpr int OFF_X = 0;
@@ -570,12 +572,12 @@ __global__ void __launch_bounds__(Cfg<TYPE>::THREADS, 1)
         }
         if constexpr (C::FUSED) {                        // W16 and quantized-slice rings (fused mode only)
             for (int s = 0; s < WS; ++s) {
-                mbar_init(&sh.fullw[s], C::DQ_WARPS);      // each dequant warp
+                mbar_init(&sh.fullw[s], kDecodeWarps);      // each dequant warp
                 mbar_init(&sh.emptyw[s], 1);               // MMA commit
             }
             for (int s = 0; s < C::QST; ++s) {
                 mbar_init(&sh.qfull[s], 1);
-                mbar_init(&sh.qempty[s], C::DQ_WARPS);
+                mbar_init(&sh.qempty[s], kDecodeWarps);
             }
         }
         for (int a = 0; a < 2; ++a) {
@@ -996,7 +998,6 @@ template <int TYPE> struct PairFCfg {
     static constexpr int XST = PairDepth<TYPE>::XST, WST = PairDepth<TYPE>::WST, QST = PairDepth<TYPE>::QST;
     static constexpr int EPI = PairDepth<TYPE>::EPI;
     static constexpr int X_HALF = 128 * BK * 2;                  // 16 KiB: this CTA's 128 tokens
-    static constexpr int DQ_WARPS = 8;
     static constexpr int THREADS = 16 * 32;
     static constexpr int Q_SLOT_BYTES = BM * QFmt<TYPE>::BOX;
     static constexpr int OFF_X = 0;
@@ -1046,12 +1047,12 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             mbar_init(&sh.emptyx[s], 1);           // the leader's multicast commit
         }
         for (int s = 0; s < WS; ++s) {
-            mbar_init(&sh.fullw[s], 2 * C::DQ_WARPS);  // leader: both CTAs' decode warps (the peer's: unused)
+            mbar_init(&sh.fullw[s], 2 * kDecodeWarps);  // leader: both CTAs' decode warps (the peer's: unused)
             mbar_init(&sh.emptyw[s], 1);           // the leader's multicast commit
         }
         for (int s = 0; s < QS; ++s) {
             mbar_init(&sh.qfull[s], 1);
-            mbar_init(&sh.qempty[s], C::DQ_WARPS);
+            mbar_init(&sh.qempty[s], kDecodeWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.accfull[a], 1);
