@@ -1,20 +1,19 @@
 // gemv.cu — the decode-side projection over the same weight blocks:
-//   Y[t, o] = sum_k X[t, k] * W16[o, k]      0 <= t < T <= 8
+//   Y[t, o] = sum_k X[t, k] * W[o, k]      0 <= t < T <= 8
 // for a handful of token rows: the serial path one token at a time ("QK-norm
 // models take the FP16 batched prefill when it fits", §What changes: the
 // serial prefill is one forward per prompt token) and the decode GEMVs that
 // run over the same block types ("Qwen3.5 batched prefill has no f32 dequant
-// for IQ2_XXS, IQ3_S, IQ3_XXS, Q2_K", §Cause).  W16 = the fp16 weights the
-// fused prefill GEMM multiplies (the exact f32 dequant rounded to fp16), and
-// the products are accumulated in f32, so this is the same projection as
-// the prefill GEMM on T <= 8 rows.
+// for IQ2_XXS, IQ3_S, IQ3_XXS, Q2_K", §Cause).  W is the exact f32 dequant
+// for the K-quants (their codes are multiplied as they are and the scales
+// applied in f32, below) and the fp16 weights of the f16 dequant for Q8_0
+// and F16; the sums are f32.
 //
 // Meant to be bound by HBM on W (every weight byte is read once), which puts
-// the integer pipe on a budget of about one to two instructions per weight
-// value: the lanes only decode, and the dot products run on the tensor cores
-// with the warp-level mma.sync m16n8k16, whose cost per value does not depend
-// on T.  The MMA's A operand is 16 weight rows x 16 K values in fp16, B is
-// the K values of the T token rows (columns >= T zero), D = f32.
+// the integer pipe on a budget of one to two instructions per weight value:
+// the lanes only isolate code bits, and the dot products run on the tensor
+// cores with the warp-level mma.sync m16n8k16.  The MMA's A operand is 16
+// weight rows x 16 K values in fp16, B is X (8 columns), D = f32.
 //
 // Two persistent CTAs per SM take 16-row blocks b, b + gridDim.x, ... of the
 // launch.  A producer warp streams each block's rows through a ring of
@@ -25,17 +24,14 @@
 // team w / S is given (the teams take a block's tiles in turn); every
 // consumer warp still waits for and releases every tile.  Measured on
 // the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
-// faster than one with twice the warps and ring.  In a step,
-// lane (g, c) (g = lane / 4, c = lane % 4) decodes runs 2c and 2c + 1 of
-// the step in weight rows g and g + 8 from the tile (the K-quants with
-// steps written out per type, Q8_0 and F16 with the exact run decoders of
-// qp_runs.cuh), rounds them to fp16 and feeds each run's 32 values to eight
-// MMAs, four per MMA.  The MMA's K order is permuted: K slots 2c,
-// 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3 of lane c's run in MMA i,
-// for A and B alike, so the sum over K is unchanged, each lane's A fragment
-// is its own decoded values and its B fragment is 4 consecutive values of
-// token row g of X.  Steps past the row's end contribute zeros.  At a
-// block's end the consumer warps' 16 x 8 partial tiles are summed through
+// faster than one with twice the warps and ring.  A step is 256 values of
+// weight rows g and g + 8 for lane (g, c) (g = lane / 4, c = lane % 4): the
+// K-quants in the sub-block group layout described with their steps below;
+// Q8_0 and F16 with the exact run decoders of qp_runs.cuh (runs 2c, 2c + 1
+// rounded to fp16, B = the token rows, the MMA's K order permuted alike in
+// A and B so that K slots 2c, 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3
+// of lane c's run in MMA i).  Steps past the row's end contribute zeros.  At
+// a block's end the consumer warps' 16 x 8 partial tiles are summed through
 // shared memory in warp order (a named barrier over the consumers only), so
 // results are deterministic.
 //
@@ -97,278 +93,455 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ----------------------------------------------------- Q2_K and Q6_K steps --
-// A consumer lane (g, c) decodes, in each step of 256 values, runs 2c and
-// 2c + 1 of weight rows g and g + 8.  For the K-quants the step is written
-// out per type: a row's fields are read
-// from shared memory once for both runs, and each word of quants feeds the
-// MMAs of both runs as soon as it is decoded.  The MMA order is the one
-// described above: MMA k of run rho takes values 4k .. 4k + 3 of the run.
+// ------------------------------------------- K-quant steps on the raw codes --
+// The K-quant weights are never formed.  An MMA's A operand holds the raw
+// quantized codes of 16 rows: each code u (a small unsigned integer) sits in
+// the low bits of its fp16 field, which is then the subnormal u * 2^-24,
+// exactly.  Within one sub-block of a row the value formulas of the K-quant
+// page ("Q2_K", "Q4_K", "Q5_K", "Q6_K" sections) are affine in u:
+//   w = alpha * (u * 2^-24) + beta,
+//   Q2_K, Q4_K, Q5_K: alpha = d * sc * 2^24, beta = -(dmin * m);
+//   Q6_K:             alpha = d * s * 2^24,  beta = -32 * d * s.
+// So a sub-block's share of a dot product is alpha * D + beta * SX, where
+// D = sum_k X[k] * A[k] comes from the tensor cores and SX = sum_k X[k] from
+// one more MMA whose A is all ones.  alpha * u * 2^-24 and beta are the
+// exact factors of the f32 dequant (d * sc * u and dmin * m need at most 24
+// significant bits), so each weight behind the sums is the exact f32 value:
+// a one-hot X row returns it bit for bit.
+//
+// The scales are applied per (row, sub-block, token) with a group layout: an
+// MMA's 16 K slots belong to NSB consecutive sub-blocks, and its 8 N columns
+// to (token, sub-block) pairs.  K slot pair p (slots 2p, 2p + 1) holds
+// sub-block p % NSB of the group, values i * 16 / NSB + 2 * (p / NSB) + {0, 1}
+// of it in the group's MMA i; column n is token n / NSB restricted to
+// sub-block n % NSB (zero in the other sub-blocks' slots), so column n of D
+// sums one sub-block of one token.  NSB = 8 / T rounded up to a power of
+// two: at T = 1 one MMA spans eight sub-blocks and the scales cost two f32x2
+// fmas per lane per eight MMAs.  Lane (g, c) holds A of rows g, g + 8 in K
+// pairs c and c + 4, B of column g, and D of columns 2c, 2c + 1.
 
-// Q2_K tables of four sub-blocks whose scale bytes are the bytes of sw:
-// t01[s] = entries 0, 1 of sub-block s as a half2, t23[s] = entries 2, 3;
-// entry q = RN_f16(fma(d * sc, q, -(dmin * m))), each f32 operation rounded
-// once (the value formula of the K-quant page, "Q2_K" section), then fp16.
-// A byte-permute selector nibble 2q (2q + 1) then picks entry q's low (high)
-// byte from {t01, t23}.
-template <int P>
-__device__ __forceinline__ void q2k_pair_tables(uint32_t scw, uint32_t mw, pair_t d2, pair_t nd2, uint32_t (&t01)[4],
-                                                uint32_t (&t23)[4]) {
-    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
-    const pair_t sc = fadd2(pk2(bias_float<2 * P>(scw), bias_float<2 * P + 1>(scw)), nbias);   // exact
-    const pair_t m = fadd2(pk2(bias_float<2 * P>(mw), bias_float<2 * P + 1>(mw)), nbias);
-    const pair_t dl = fmul2(d2, sc), nml = fmul2(nd2, m);
-    float x[4], y[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) unpk2(ffma2(dl, pk2(static_cast<float>(q), static_cast<float>(q)), nml), x[q], y[q]);
-    t01[2 * P] = h2_of(x[0], x[1]);
-    t23[2 * P] = h2_of(x[2], x[3]);
-    t01[2 * P + 1] = h2_of(y[0], y[1]);
-    t23[2 * P + 1] = h2_of(y[2], y[3]);
+constexpr uint32_t kOnesH2 = 0x3C003C00u;   // fp16 1.0 twice
+
+// X beyond a lane's column reads as zeros from here (a step's offsets stay
+// below 256 values).
+__device__ __align__(16) uint16_t g_zero_x[256];
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ uint32_t lds16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+__device__ __forceinline__ uint32_t lds8(const uint8_t *p) { return *p; }
+__device__ __forceinline__ uint32_t ldx32(const uint16_t *p) {
+    return __ldg(reinterpret_cast<const unsigned int *>(p));
+}
+__device__ __forceinline__ uint4 ldx128(const uint16_t *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
-__device__ __forceinline__ void q2k_tables4(uint32_t sw, uint32_t dd, uint32_t (&t01)[4], uint32_t (&t23)[4]) {
-    const float d = h2f(dd), dmin = h2f(dd >> 16);
-    const pair_t d2 = pk2(d, d), nd2 = pk2(-dmin, -dmin);   // -(dmin * m) = (-dmin) * m: rounding is sign-symmetric
-    const uint32_t scw = sw & 0x0F0F0F0Fu, mw = (sw >> 4) & 0x0F0F0F0Fu;
-    q2k_pair_tables<0>(scw, mw, d2, nd2, t01, t23);
-    q2k_pair_tables<1>(scw, mw, d2, nd2, t01, t23);
-}
+// Bytes 2h, 2h + 1 of w into the low bytes of two fp16 fields.
+__device__ __forceinline__ uint32_t spread(uint32_t w, int h) { return __byte_perm(w, 0u, h ? 0x4342 : 0x4140); }
+__device__ __forceinline__ uint32_t spread_sel(int h) { return h ? 0x4342u : 0x4140u; }
 
-// Four 2-bit quants (bits 0-1 of each byte of v) -> four fp16 weights of
-// sub-block s: the selectors 2q | (2q + 1) << 4 per value, for the low and
-// the high two bytes of v.
-__device__ __forceinline__ void q2k_pick(uint32_t v, uint32_t t01, uint32_t t23, uint32_t &h01, uint32_t &h23) {
-    h01 = prmt_sel(t01, t23, v * 0x22u + 0x10101010u);
-    h23 = prmt_sel(t01, t23, mad_hi(v, 0x00220000u, 0x1010u));   // (v * 0x22) >> 16, + 0x1010
-}
+// 2^e as a float, for small integer e (exact scaling).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
-// Q2_K (84-byte superblocks, 4-byte aligned in the stage): run t = 2c + rho
-// takes bits 2(t & 3) of qs[32(t >> 2) + l] and scale bytes 2t, 2t + 1; the
-// lane's two runs share the quant words and the scale word of bytes 4c .. 4c + 3.
-__device__ __forceinline__ void step_q2k(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
-                                         float (&d)[4], float (&e)[4]) {
-    uint32_t ta0[4], tb0[4], ta1[4], tb1[4];
-    q2k_tables4(Smem::u32(b0 + 4 * c), Smem::u32(b0 + 80), ta0, tb0);
-    q2k_tables4(Smem::u32(b1 + 4 * c), Smem::u32(b1 + 80), ta1, tb1);
-    const uint8_t *q0 = b0 + 16 + 32 * (c >> 1), *q1 = b1 + 16 + 32 * (c >> 1);
-    const int sh = 4 * (c & 1);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);       // run 2c, values 8u .. 8u + 7
-        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);   // run 2c + 1
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int k = 2 * u + hh, s = k >> 2;
-            const uint32_t w0 = Smem::u32(q0 + 4 * k) >> sh, w1 = Smem::u32(q1 + 4 * k) >> sh;
-            uint32_t a0, a1, a2, a3;
-            q2k_pick(w0 & 0x03030303u, ta0[s], tb0[s], a0, a2);
-            q2k_pick(w1 & 0x03030303u, ta1[s], tb1[s], a1, a3);
-            mma_16816(d, a0, a1, a2, a3, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
-            q2k_pick((w0 >> 2) & 0x03030303u, ta0[s + 2], tb0[s + 2], a0, a2);
-            q2k_pick((w1 >> 2) & 0x03030303u, ta1[s + 2], tb1[s + 2], a1, a3);
-            mma_16816(e, a0, a1, a2, a3, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
-        }
-    }
-}
+template <int NSB>
+struct LaneMap {
+    int c;
+    int j0, j1;    // sub-block (within the group) of K pairs c and c + 4
+    int jg, tg;    // column g: its sub-block and token
+    int jn;        // D columns 2c, 2c + 1: sub-blocks jn, jn + 1 (NSB > 1), or jn for both (NSB = 1)
+    __device__ __forceinline__ LaneMap(int g, int c_)
+        : c(c_), j0(c_ % NSB), j1((c_ + 4) % NSB), jg(g % NSB), tg(g / NSB), jn((2 * c_) % NSB) {}
+};
 
-// Q6_K (210-byte superblocks, 2-byte aligned in the stage): run t = 2c + rho
-// takes the low (c even) or high (c odd) nibbles of ql[64(t >> 2) + 32 rho + l]
-// and bits 2(t & 3) of qh[32(t >> 2) + l], int8 scales 2t, 2t + 1; the two
-// runs share the qh words and the scale bytes 4c .. 4c + 3.
-// MIS: the superblock starts 2 bytes past a 4-byte boundary.  Its fields are
-// then read as the aligned words starting 2 bytes early, so assembled word
-// k holds values 4k - 2 .. 4k + 1 and a value's byte is taken from word k or
-// k + 1 (all reads stay inside the superblock).
-template <bool MIS>
-struct Q6Row {
-    static constexpr int NW = MIS ? 9 : 8;
-    uint32_t u0[NW], u1[NW];   // 6-bit quants of runs 2c, 2c + 1, one per byte
-    pair_t dl[4];              // d * scale of sub-blocks 4c .. 4c + 3, as pairs
-
-    __device__ __forceinline__ void load(const uint8_t *b, int c) {
-        const int o = MIS ? -2 : 0;
-        const uint8_t *ql = b + 64 * (c >> 1) + o, *qh = b + 128 + 32 * (c >> 1) + o;
-        const int hs = 4 * (c & 1);
-#pragma unroll
-        for (int k = 0; k < NW; ++k) {
-            const uint32_t h = Smem::u32(qh + 4 * k) >> hs;
-            u0[k] = ((Smem::u32(ql + 4 * k) >> hs) & 0x0F0F0F0Fu) + ((h & 0x03030303u) << 4);
-            u1[k] = ((Smem::u32(ql + 32 + 4 * k) >> hs) & 0x0F0F0F0Fu) + ((h & 0x0C0C0C0Cu) << 2);
-        }
-        const uint32_t sw = MIS ? (Smem::u16(b + 192 + 4 * c) | (Smem::u16(b + 194 + 4 * c) << 16))
-                                : Smem::u32(b + 192 + 4 * c);
-        const float dd = h2f(Smem::u16(b + 208));
-        const pair_t nb = pk2(-8388736.0f, -8388736.0f);   // -(2^23 + 128): int8 = (byte ^ 0x80) - 128
-        const uint32_t sx = sw ^ 0x80808080u;
-        const pair_t s01 = fadd2(pk2(bias_float<0>(sx), bias_float<1>(sx)), nb);
-        const pair_t s23 = fadd2(pk2(bias_float<2>(sx), bias_float<3>(sx)), nb);
-        float s[4];
-        unpk2(s01, s[0], s[1]);
-        unpk2(s23, s[2], s[3]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float v = __fmul_rn(dd, s[i]);   // exact: 11 x 8 significant bits
-            dl[i] = pk2(v, v);
+// The value B words of the lane in MMA i of a group, from the column-g
+// sub-block chunk at xa (pair c) and xb (pair c + 4) (zeros where the lane's
+// pair is not in column g's sub-block): word i * 8 / NSB + (p / NSB) of it.
+template <int NSB>
+struct XWords {
+    uint4 qa, qb;
+    __device__ __forceinline__ void get(const uint16_t *xa, const uint16_t *xb, int i, int c, uint32_t &b0,
+                                        uint32_t &b1) {
+        if constexpr (NSB == 8) {                       // words i, i
+            if (i % 4 == 0) {
+                qa = ldx128(xa + 2 * i);
+                qb = ldx128(xb + 2 * i);
+            }
+            b0 = word_of(qa, i % 4);
+            b1 = word_of(qb, i % 4);
+        } else if constexpr (NSB == 4) {                // words 2i, 2i + 1 (xa = xb)
+            if (i % 2 == 0) qa = ldx128(xa + 4 * i);
+            b0 = word_of(qa, 2 * (i % 2));
+            b1 = word_of(qa, 2 * (i % 2) + 1);
+        } else if constexpr (NSB == 2) {                // words 4i + c/2, 4i + 2 + c/2 (xa = xb)
+            b0 = ldx32(xa + 8 * i + 2 * (c >> 1));
+            b1 = ldx32(xa + 8 * i + 4 + 2 * (c >> 1));
+        } else {                                        // words 8i + c, 8i + 4 + c (xa = xb)
+            b0 = ldx32(xa + 16 * i + 2 * c);
+            b1 = ldx32(xa + 16 * i + 8 + 2 * c);
         }
     }
 };
 
-// A row read in the 2-byte offset form, brought to the aligned form (word k
-// = values 4k .. 4k + 3), for warps whose lanes' rows start differently.
-__device__ __forceinline__ void q6k_realign(const Q6Row<true> &a, Q6Row<false> &r) {
+// ---- Q2_K (84-byte superblocks: scales[16], qs[64], d, dmin): value v of
+// sub-block s is crumb (s % 8) / 2 of qs[32 (s / 8) + 16 (s % 2) + v], the
+// crumb kept in place in its byte (code u * 4^crumb); scale byte s holds sc
+// (low nibble) and m (high nibble).  Pairs c and c + 4 always read the same
+// 16 qs bytes of a group.
+template <int NSB>
+struct Q2Codes {
+    static constexpr int SBV = 16, NSUB = 16;
+    uint32_t w[NSB == 1 ? 2 : 4];
+    uint32_t m0, m1, sel;
+    __device__ __forceinline__ void load(const uint8_t *sb, int gm, int c) {
+        constexpr uint32_t M = 0x00030003u;
+        if constexpr (NSB == 8) {                       // s = 8gm + c, 8gm + c + 4
+            const uint8_t *q = sb + 16 + 32 * gm + 16 * (c & 1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        r.u0[k] = __funnelshift_r(a.u0[k], a.u0[k + 1], 16);
-        r.u1[k] = __funnelshift_r(a.u1[k], a.u1[k + 1], 16);
-    }
+            for (int k = 0; k < 4; ++k) w[k] = lds32(q + 4 * k);
+            m0 = M << (2 * (c >> 1));
+            m1 = m0 << 4;
+        } else if constexpr (NSB == 4) {                // s = 4gm + c
+            const uint8_t *q = sb + 16 + 32 * (gm >> 1) + 16 * (c & 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r.dl[i] = a.dl[i];
-}
-
-// Values 4k .. 4k + 3 of a run's quant words -> two half2 words.
-template <bool MIS>
-__device__ __forceinline__ void q6k_word(const uint32_t *u, int k, pair_t dl, uint32_t &h01, uint32_t &h23) {
-    const pair_t nb = pk2(-8388640.0f, -8388640.0f);   // -(2^23 + 32)
-    pair_t q01, q23;
-    if (MIS) {
-        q01 = pk2(bias_float<2>(u[k]), bias_float<3>(u[k]));
-        q23 = pk2(bias_float<0>(u[k + 1]), bias_float<1>(u[k + 1]));
-    } else {
-        q01 = pk2(bias_float<0>(u[k]), bias_float<1>(u[k]));
-        q23 = pk2(bias_float<2>(u[k]), bias_float<3>(u[k]));
-    }
-    h01 = f2h2(fmul2(dl, fadd2(q01, nb)));   // d * s * (q - 32): exact product, one rounding to fp16
-    h23 = f2h2(fmul2(dl, fadd2(q23, nb)));
-}
-
-// The MMAs of a step over two rows already read.  mma.sync needs the whole
-// warp: callers reach this with all 32 lanes.
-template <bool MIS>
-__device__ __forceinline__ void q6k_mma(const Q6Row<MIS> &r0, const Q6Row<MIS> &r1, const uint4 *xv, bool tok,
-                                        float (&d)[4], float (&e)[4]) {
+            for (int k = 0; k < 4; ++k) w[k] = lds32(q + 4 * k);
+            m0 = m1 = M << (2 * (2 * (gm & 1) + (c >> 1)));
+        } else if constexpr (NSB == 2) {                // s = 2gm + c % 2
+            const uint8_t *q = sb + 16 + 32 * (gm >> 2) + 16 * (c & 1);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int k = 2 * u + hh, s = k >> 2;
-            uint32_t a0, a1, a2, a3;
-            q6k_word<MIS>(r0.u0, k, r0.dl[s], a0, a2);
-            q6k_word<MIS>(r1.u0, k, r1.dl[s], a1, a3);
-            mma_16816(d, a0, a1, a2, a3, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
-            q6k_word<MIS>(r0.u1, k, r0.dl[s + 2], a0, a2);
-            q6k_word<MIS>(r1.u1, k, r1.dl[s + 2], a1, a3);
-            mma_16816(e, a0, a1, a2, a3, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
+            for (int k = 0; k < 4; ++k) w[k] = lds32(q + 4 * k);
+            m0 = m1 = M << (2 * (gm & 3));
+            sel = spread_sel(c >> 1);
+        } else {                                        // s = gm
+            const uint8_t *q = sb + 16 + 32 * (gm >> 3) + 16 * (gm & 1) + 4 * (c >> 1);
+            w[0] = lds32(q);
+            w[1] = lds32(q + 8);
+            m0 = m1 = M << (2 * ((gm & 7) >> 1));
+            sel = spread_sel(c & 1);
         }
     }
-}
+    __device__ __forceinline__ uint32_t pair(int i, int p) const {
+        if constexpr (NSB == 8) return spread(w[i >> 1], i & 1) & (p ? m1 : m0);
+        else if constexpr (NSB == 4) return spread(w[i], p) & m0;
+        else if constexpr (NSB == 2) return prmt_sel(w[2 * i + p], 0u, sel) & m0;
+        else return prmt_sel(w[p], 0u, sel) & m0;
+    }
+};
 
-// One Q6_K step.  Rows g and g + 8 start alike modulo 4 (8 row pitches
-// apart); with TMA tiles every row of a step starts alike too, so a warp's
-// lanes agree and the warp takes the form of its rows' offset.  Rows staged
-// by one copy each can disagree from lane to lane: then each lane reads its
-// rows in its own form, brings them to the aligned one, and the warp's MMAs
-// run together afterwards.
-__device__ __forceinline__ void step_q6k(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
-                                         float (&d)[4], float (&e)[4]) {
-    const bool mis = (smem_u32(b0) & 2u) != 0u;
-    if (__all_sync(0xffffffffu, mis)) {
-        Q6Row<true> r0, r1;
-        r0.load(b0, c);
-        r1.load(b1, c);
-        q6k_mma<true>(r0, r1, xv, tok, d, e);
-    } else if (!__any_sync(0xffffffffu, mis)) {
-        Q6Row<false> r0, r1;
-        r0.load(b0, c);
-        r1.load(b1, c);
-        q6k_mma<false>(r0, r1, xv, tok, d, e);
+// Q2_K alpha / beta of the lane's D columns in group gm for one row.
+template <int NSB>
+__device__ __forceinline__ void q2_scales(const uint8_t *sb, float d, float ndmin, int gm, const LaneMap<NSB> &L,
+                                          pair_t &al, pair_t &be) {
+    const int s0 = gm * NSB + L.jn;                     // even when NSB > 1
+    const int crumb = (s0 & 7) >> 1;
+    const float dsc = d * pow2f(24 - 2 * crumb);        // exact
+    if constexpr (NSB > 1) {
+        const uint32_t sw = lds16(sb + s0);
+        const uint32_t scw = sw & 0x0F0Fu, mw = (sw >> 4) & 0x0F0Fu;
+        const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+        const pair_t sc = fadd2(pk2(bias_float<0>(scw), bias_float<1>(scw)), nbias);   // exact
+        const pair_t m = fadd2(pk2(bias_float<0>(mw), bias_float<1>(mw)), nbias);
+        al = fmul2(pk2(dsc, dsc), sc);
+        be = fmul2(pk2(ndmin, ndmin), m);
     } else {
-        Q6Row<false> r0, r1;
-        if (mis) {
-            Q6Row<true> a;
-            a.load(b0, c);
-            q6k_realign(a, r0);
-            a.load(b1, c);
-            q6k_realign(a, r1);
-        } else {
-            r0.load(b0, c);
-            r1.load(b1, c);
-        }
-        q6k_mma<false>(r0, r1, xv, tok, d, e);
+        const uint32_t b = lds8(sb + s0);
+        const float a = dsc * u2f_exact(b & 15u), n = ndmin * u2f_exact(b >> 4);
+        al = pk2(a, a);
+        be = pk2(n, n);
     }
 }
 
-// Q4_K / Q5_K (144- / 176-byte superblocks, 16-byte aligned in the stage):
-// run t is sub-block t: the low (t even) or high (t odd) nibbles of
-// qs[32(t >> 1) + l], Q5_K's fifth bit being bit t of qh[l].  The lane's runs
-// 2c and 2c + 1 share the 32 bytes qs[32c ..] (and qh[0 .. 31]).  Scales:
-// the 6-bit (sc, m) of sub-block t from the packed scale bytes, dl = d * sc
-// and nml = -(dmin * m), each rounded once; a value is fma(dl, q, nml),
-// rounded to fp16 (the K-quant page's value formula, as the run decoders).
-__device__ __forceinline__ void k4_run_scales(const uint4 &hd, int t, pair_t &dl2, pair_t &nml2) {
+// ---- Q6_K (210-byte superblocks: ql[128], qh[64], scales[16] int8, d):
+// value v of sub-block s (half n = s / 8, j = (s % 8) / 2, l = 16 (s % 2) + v)
+// is the low (j < 2) or high nibble of ql[64n + 32 (j % 2) + l] plus crumb j
+// of qh[32n + l] as bits 4..5: the 6-bit code u (value d * s * (u - 32)).
+// A superblock starts 2 bytes past a 4-byte boundary when its offset in the
+// stage is; MIS = 0: aligned, 1: 2 bytes past, 2: per lane (shift `sh`).
+// Words are then read from the aligned address 2 bytes early and realigned;
+// every read stays inside the superblock.
+template <int MIS, int N>
+__device__ __forceinline__ void q6_words(const uint8_t *p, uint32_t sh, uint32_t (&w)[N]) {
+    if constexpr (MIS == 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) w[k] = lds32(p + 4 * k);
+    } else {
+        const uint8_t *a = p - (MIS == 1 ? 2 : static_cast<int>(sh >> 3));
+        const uint32_t s = MIS == 1 ? 16u : sh;
+        uint32_t t[N + 1];
+#pragma unroll
+        for (int k = 0; k <= N; ++k) t[k] = lds32(a + 4 * k);
+#pragma unroll
+        for (int k = 0; k < N; ++k) w[k] = __funnelshift_r(t[k], t[k + 1], s);
+    }
+}
+
+// Four 6-bit codes (one per byte) from a ql word (nibble half `hi`) and a qh
+// word (crumb j).
+__device__ __forceinline__ uint32_t q6_code_word(uint32_t wl, uint32_t wh, int hi, int j) {
+    return ((hi ? wl >> 4 : wl) & 0x0F0F0F0Fu) | (((wh >> (2 * j)) << 4) & 0x30303030u);
+}
+
+template <int NSB, int MIS>
+struct Q6Codes {
+    static constexpr int SBV = 16, NSUB = 16;
+    static constexpr int NW = NSB == 1 ? 2 : 4;
+    uint32_t u0[NW], u1[NSB == 8 ? 4 : 1];
+    uint32_t sel;
+    __device__ __forceinline__ void load(const uint8_t *sb, uint32_t sh, int gm, int c) {
+        if constexpr (NSB == 8) {
+            // s = 8gm + c (low nibbles, crumb c/2) and 8gm + c + 4 (high nibbles,
+            // crumb c/2 + 2): the same 16 ql and 16 qh bytes
+            uint32_t wl[4], wh[4];
+            q6_words<MIS, 4>(sb + 64 * gm + 16 * c, sh, wl);
+            q6_words<MIS, 4>(sb + 128 + 32 * gm + 16 * (c & 1), sh, wh);
+            const int j = c >> 1;
+            const uint32_t keep = 0x33333333u << (2 * j);      // crumbs j and j + 2 of every byte
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t hm = wh[k] & keep;
+                u0[k] = (wl[k] & 0x0F0F0F0Fu) | ((hm << (4 - 2 * j)) & 0xF0F0F0F0u);
+                u1[k] = ((wl[k] >> 4) & 0x0F0F0F0Fu) | ((hm >> (2 * j)) & 0xF0F0F0F0u);
+            }
+        } else if constexpr (NSB == 4) {                       // s = 4gm + c
+            uint32_t wl[4], wh[4];
+            q6_words<MIS, 4>(sb + 64 * (gm >> 1) + 16 * c, sh, wl);
+            q6_words<MIS, 4>(sb + 128 + 32 * (gm >> 1) + 16 * (c & 1), sh, wh);
+            const int j = 2 * (gm & 1) + (c >> 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u0[k] = q6_code_word(wl[k], wh[k], gm & 1, j);
+        } else if constexpr (NSB == 2) {                       // s = 2gm + c % 2
+            uint32_t wl[4], wh[4];
+            q6_words<MIS, 4>(sb + 64 * (gm >> 2) + 32 * (gm & 1) + 16 * (c & 1), sh, wl);
+            q6_words<MIS, 4>(sb + 128 + 32 * (gm >> 2) + 16 * (c & 1), sh, wh);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u0[k] = q6_code_word(wl[k], wh[k], (gm & 3) >= 2, gm & 3);
+            sel = spread_sel(c >> 1);
+        } else {                                               // s = gm
+            const int n = gm >> 3, j = (gm & 7) >> 1, l0 = 16 * (gm & 1) + 4 * (c >> 1);
+            const uint8_t *ql = sb + 64 * n + 32 * (j & 1) + l0, *qh = sb + 128 + 32 * n + l0;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint32_t wl[1], wh[1];
+                q6_words<MIS, 1>(ql + 8 * p, sh, wl);
+                q6_words<MIS, 1>(qh + 8 * p, sh, wh);
+                u0[p] = q6_code_word(wl[0], wh[0], j >= 2, j);
+            }
+            sel = spread_sel(c & 1);
+        }
+    }
+    __device__ __forceinline__ uint32_t pair(int i, int p) const {
+        if constexpr (NSB == 8) return spread(p ? u1[i >> 1] : u0[i >> 1], i & 1);
+        else if constexpr (NSB == 4) return spread(u0[i], p);
+        else if constexpr (NSB == 2) return prmt_sel(u0[2 * i + p], 0u, sel);
+        else return prmt_sel(u0[p], 0u, sel);
+    }
+};
+
+template <int NSB>
+__device__ __forceinline__ void q6_scales(const uint8_t *sb, float d24, int gm, const LaneMap<NSB> &L, pair_t &al,
+                                          pair_t &be) {
+    const int s0 = gm * NSB + L.jn;
+    const pair_t m32 = pk2(-1.9073486328125e-06f, -1.9073486328125e-06f);   // -32 * 2^-24
+    if constexpr (NSB > 1) {
+        const uint32_t sx = lds16(sb + 192 + s0) ^ 0x8080u;                // int8 + 128
+        const pair_t nb = pk2(-8388736.0f, -8388736.0f);                  // -(2^23 + 128)
+        const pair_t s = fadd2(pk2(bias_float<0>(sx), bias_float<1>(sx)), nb);   // exact
+        al = fmul2(pk2(d24, d24), s);                                      // d * s * 2^24, exact
+    } else {
+        const float s = static_cast<float>(static_cast<int8_t>(lds8(sb + 192 + s0)));
+        const float a = d24 * s;
+        al = pk2(a, a);
+    }
+    be = fmul2(al, m32);                                                   // -32 * d * s, exact
+}
+
+// ---- Q4_K / Q5_K (144- / 176-byte superblocks, 16-byte aligned in the
+// stage: d, dmin, 12 bytes of packed 6-bit (sc, m), Q5_K's qh[32], qs[128]):
+// value v of sub-block s (32 values) is the low (s even) or high nibble of
+// qs[32 (s / 2) + v], Q5_K's fifth bit being bit s of qh[v].
+template <int TYPE, int NSB>
+struct K4Codes {
+    static constexpr bool Q5 = TYPE == kQ5_K;
+    static constexpr int QS = Q5 ? 48 : 16;
+    static constexpr int SBV = 32, NSUB = 8;
+    const uint8_t *q0, *q1, *qh;   // qs words of pairs c and c + 4 (MMA i reads word i * 8 / NSB + ...)
+    int hi, s0, s1;                // nibble half; sub-blocks of the pairs (Q5_K's qh bit)
+    uint32_t sel;
+    __device__ __forceinline__ void load(const uint8_t *sb, int gm, int c) {
+        qh = sb + 16;
+        if constexpr (NSB == 8) {                       // s = c, c + 4
+            q0 = sb + QS + 32 * (c >> 1);
+            q1 = q0 + 64;
+            hi = c & 1;
+            s0 = c;
+            s1 = c + 4;
+        } else if constexpr (NSB == 4) {                // s = 4gm + c
+            q0 = q1 = sb + QS + 64 * gm + 32 * (c >> 1);
+            hi = c & 1;
+            s0 = s1 = 4 * gm + c;
+        } else if constexpr (NSB == 2) {                // s = 2gm + c % 2
+            q0 = q1 = sb + QS + 32 * gm;
+            hi = c & 1;
+            s0 = s1 = 2 * gm + (c & 1);
+            sel = spread_sel(c >> 1);
+        } else {                                        // s = gm
+            q0 = q1 = sb + QS + 32 * (gm >> 1);
+            hi = gm & 1;
+            s0 = s1 = gm;
+            sel = spread_sel(c & 1);
+        }
+    }
+    // the codes of qs word k (and qh word k) of pair p, one per byte
+    __device__ __forceinline__ uint32_t codes(int k, int p) const {
+        const uint32_t w = lds32((p ? q1 : q0) + 4 * k);
+        uint32_t u = (hi ? w >> 4 : w) & 0x0F0F0F0Fu;
+        if constexpr (Q5) u |= ((lds32(qh + 4 * k) >> (p ? s1 : s0)) & 0x01010101u) << 4;
+        return u;
+    }
+    __device__ __forceinline__ uint32_t pair(int i, int p, int c) const {
+        if constexpr (NSB == 8) return spread(codes(i >> 1, p), i & 1);          // values 2i, 2i + 1
+        else if constexpr (NSB == 4) return spread(codes(i, 0), p);              // 4i + 2p ..
+        else if constexpr (NSB == 2) return prmt_sel(codes(2 * i + p, 0), 0u, sel);   // 8i + 4p + 2(c/2) ..
+        else return prmt_sel(codes(4 * i + (c >> 1) + 2 * p, 0), 0u, sel);       // 16i + 8p + 2c ..
+    }
+};
+
+// The 6-bit (sc, m) of sub-block t from the packed scale bytes (hd.y, hd.z,
+// hd.w = bytes 4..15 of the superblock).
+__device__ __forceinline__ void k4_sm(const uint4 &hd, int t, uint32_t &sc, uint32_t &m) {
     const int sh = 8 * (t & 3);
     const uint32_t ys = hd.y >> sh, zs = hd.z >> sh, ws = hd.w >> sh;
-    const uint32_t sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
-    const uint32_t m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
-    const float dl = __fmul_rn(h2f(hd.x), u2f_exact(sc));
-    const float nml = -__fmul_rn(h2f(hd.x >> 16), u2f_exact(m));
-    dl2 = pk2(dl, dl);
-    nml2 = pk2(nml, nml);
+    sc = t < 4 ? (ys & 63u) : ((ws & 15u) | ((ys >> 6 & 3u) << 4));
+    m = t < 4 ? (zs & 63u) : (((ws >> 4) & 15u) | ((zs >> 6 & 3u) << 4));
 }
 
-template <bool Q5>
-struct K4Row {
-    pair_t dla, nmla, dlb, nmlb;   // runs 2c (a) and 2c + 1 (b)
-    uint32_t q[8], h[Q5 ? 8 : 1];
-
-    __device__ __forceinline__ void load(const uint8_t *b, int c) {
-        const uint4 hd = Smem::u128(b);
-        k4_run_scales(hd, 2 * c, dla, nmla);
-        k4_run_scales(hd, 2 * c + 1, dlb, nmlb);
-        const uint8_t *qs = b + (Q5 ? 48 : 16) + 32 * c;
-        const uint4 q0 = Smem::u128(qs), q1 = Smem::u128(qs + 16);
-        q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
-        q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
-        if constexpr (Q5) {
-            const uint4 h0 = Smem::u128(b + 16), h1 = Smem::u128(b + 32);
-            h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
-            h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
-        }
+template <int NSB>
+__device__ __forceinline__ void k4_scales(const uint4 &hd, float d24, float ndmin, int gm, const LaneMap<NSB> &L,
+                                          pair_t &al, pair_t &be) {
+    const int t0 = gm * NSB + L.jn;
+    uint32_t sc0, m0;
+    k4_sm(hd, t0, sc0, m0);
+    if constexpr (NSB > 1) {
+        uint32_t sc1, m1;
+        k4_sm(hd, t0 + 1, sc1, m1);
+        al = fmul2(pk2(d24, d24), pk2(u2f_exact(sc0), u2f_exact(sc1)));      // d * sc * 2^24, exact
+        be = fmul2(pk2(ndmin, ndmin), pk2(u2f_exact(m0), u2f_exact(m1)));   // -(dmin * m), exact
+    } else {
+        const float a = d24 * u2f_exact(sc0), n = ndmin * u2f_exact(m0);
+        al = pk2(a, a);
+        be = pk2(n, n);
     }
-    // 4-value quant words of word k for runs a and b
-    __device__ __forceinline__ void quants(int k, int c, uint32_t &ua, uint32_t &ub) const {
-        ua = q[k] & 0x0F0F0F0Fu;
-        ub = (q[k] >> 4) & 0x0F0F0F0Fu;
-        if constexpr (Q5) {
-            ua |= ((h[k] >> (2 * c)) & 0x01010101u) << 4;
-            ub |= ((h[k] >> (2 * c + 1)) & 0x01010101u) << 4;
-        }
+}
+
+// Per-row, per-superblock header values.
+template <int TYPE> struct RowHead;
+template <> struct RowHead<kQ2_K> {
+    float d24, ndmin;   // d (scaled per group by the crumb), -dmin
+    __device__ __forceinline__ explicit RowHead(const uint8_t *sb) {
+        const uint32_t dd = lds32(sb + 80);
+        d24 = h2f(dd);
+        ndmin = -h2f(dd >> 16);
     }
 };
+template <> struct RowHead<kQ6_K> {
+    float d24;
+    __device__ __forceinline__ explicit RowHead(const uint8_t *sb) { d24 = h2f(lds16(sb + 208)) * 16777216.0f; }
+};
+template <int TYPE> struct K4Head {
+    uint4 hd;
+    float d24, ndmin;
+    __device__ __forceinline__ explicit K4Head(const uint8_t *sb) {
+        hd = *reinterpret_cast<const uint4 *>(sb);
+        d24 = h2f(hd.x) * 16777216.0f;
+        ndmin = -h2f(hd.x >> 16);
+    }
+};
+template <> struct RowHead<kQ4_K> : K4Head<kQ4_K> {
+    __device__ __forceinline__ explicit RowHead(const uint8_t *sb) : K4Head<kQ4_K>(sb) {}
+};
+template <> struct RowHead<kQ5_K> : K4Head<kQ5_K> {
+    __device__ __forceinline__ explicit RowHead(const uint8_t *sb) : K4Head<kQ5_K>(sb) {}
+};
 
-template <bool Q5>
-__device__ __forceinline__ void step_k4(const uint8_t *b0, const uint8_t *b1, int c, const uint4 *xv, bool tok,
-                                        float (&d)[4], float (&e)[4]) {
-    K4Row<Q5> r0, r1;
-    r0.load(b0, c);
-    r1.load(b1, c);
+// mma.sync without `volatile`: a pure function of its registers, so loads
+// around it may be merged and scheduled freely.
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int TYPE, int NSB, int MIS> struct CodesOf;
+template <int NSB, int MIS> struct CodesOf<kQ2_K, NSB, MIS> { using T = Q2Codes<NSB>; };
+template <int NSB, int MIS> struct CodesOf<kQ6_K, NSB, MIS> { using T = Q6Codes<NSB, MIS>; };
+template <int NSB, int MIS> struct CodesOf<kQ4_K, NSB, MIS> { using T = K4Codes<kQ4_K, NSB>; };
+template <int NSB, int MIS> struct CodesOf<kQ5_K, NSB, MIS> { using T = K4Codes<kQ5_K, NSB>; };
+
+template <int TYPE, int NSB, int MIS>
+__device__ __forceinline__ void load_codes(typename CodesOf<TYPE, NSB, MIS>::T &q, const uint8_t *sb, uint32_t sh,
+                                           int gm, int c) {
+    if constexpr (TYPE == kQ6_K) q.load(sb, sh, gm, c);
+    else q.load(sb, gm, c);
+}
+
+template <int TYPE, int NSB, int MIS>
+__device__ __forceinline__ uint32_t code_pair(const typename CodesOf<TYPE, NSB, MIS>::T &q, int i, int p, int c) {
+    if constexpr (TYPE == kQ4_K || TYPE == kQ5_K) return q.pair(i, p, c);
+    else return q.pair(i, p);
+}
+
+template <int TYPE, int NSB>
+__device__ __forceinline__ void group_scales(const uint8_t *sb, const RowHead<TYPE> &h, int gm,
+                                             const LaneMap<NSB> &L, pair_t &al, pair_t &be) {
+    if constexpr (TYPE == kQ2_K) q2_scales<NSB>(sb, h.d24, h.ndmin, gm, L, al, be);
+    else if constexpr (TYPE == kQ6_K) q6_scales<NSB>(sb, h.d24, gm, L, al, be);
+    else k4_scales<NSB>(h.hd, h.d24, h.ndmin, gm, L, al, be);
+}
+
+// One step (one superblock of rows g and g + 8, at r0 and r1 in the stage)
+// of a K-quant: for each group of NSB sub-blocks, the SX MMA(s), the value
+// MMAs, and acc += alpha * D + beta * SX for the lane's two D columns of each
+// row.  xa, xb, xg: the step's X values of the lane's value-B pairs and of
+// its column, or the zero page.
+template <int TYPE, int NSB, int MIS>
+__device__ __forceinline__ void step_codes(const uint8_t *r0, const uint8_t *r1, uint32_t sh, const LaneMap<NSB> &L,
+                                           const uint16_t *xa, const uint16_t *xb, const uint16_t *xg,
+                                           pair_t (&acc)[2]) {
+    using Q = typename CodesOf<TYPE, NSB, MIS>::T;
+    constexpr int SBV = Q::SBV, GROUPS = Q::NSUB / NSB, MMAS = NSB * SBV / 16;
+    const RowHead<TYPE> h0(r0), h1(r1);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint4 xa = tok ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 xb = tok ? __ldg(xv + 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+    for (int gm = 0; gm < GROUPS; ++gm) {
+        const int xo = SBV * (gm * NSB + L.jg);        // column g's sub-block in the step's X
+        // two accumulators for the value MMAs (alternating), so that their
+        // dependency chain is half as long
+        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f}, E[4] = {0.0f, 0.0f, 0.0f, 0.0f}, S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int k = 2 * u + hh;
-            uint32_t ua0, ub0, ua1, ub1;
-            r0.quants(k, c, ua0, ub0);
-            r1.quants(k, c, ua1, ub1);
-            const uint2 p0 = word_affine(ua0, r0.dla, r0.nmla), p1 = word_affine(ua1, r1.dla, r1.nmla);
-            mma_16816(d, p0.x, p1.x, p0.y, p1.y, hh ? xa.z : xa.x, hh ? xa.w : xa.y);
-            const uint2 q0 = word_affine(ub0, r0.dlb, r0.nmlb), q1 = word_affine(ub1, r1.dlb, r1.nmlb);
-            mma_16816(e, q0.x, q1.x, q0.y, q1.y, hh ? xb.z : xb.x, hh ? xb.w : xb.y);
+        for (int hh = 0; hh < SBV / 16; ++hh)
+            mma_acc(S, kOnesH2, kOnesH2, kOnesH2, kOnesH2, ldx32(xg + xo + 16 * hh + 2 * L.c),
+                    ldx32(xg + xo + 16 * hh + 8 + 2 * L.c));
+        Q q0, q1;
+        load_codes<TYPE, NSB, MIS>(q0, r0, sh, gm, L.c);
+        load_codes<TYPE, NSB, MIS>(q1, r1, sh, gm, L.c);
+        XWords<NSB> xw;
+#pragma unroll
+        for (int i = 0; i < MMAS; ++i) {
+            uint32_t b0, b1;
+            xw.get(xa + xo, xb + xo, i, L.c, b0, b1);
+            mma_acc(i % 2 ? E : D, code_pair<TYPE, NSB, MIS>(q0, i, 0, L.c), code_pair<TYPE, NSB, MIS>(q1, i, 0, L.c),
+                    code_pair<TYPE, NSB, MIS>(q0, i, 1, L.c), code_pair<TYPE, NSB, MIS>(q1, i, 1, L.c), b0, b1);
         }
+        if constexpr (MMAS > 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) D[k] += E[k];
+        }
+        pair_t al0, be0, al1, be1;
+        group_scales<TYPE, NSB>(r0, h0, gm, L, al0, be0);
+        group_scales<TYPE, NSB>(r1, h1, gm, L, al1, be1);
+        acc[0] = ffma2(al0, pk2(D[0], D[1]), ffma2(be0, pk2(S[0], S[1]), acc[0]));
+        acc[1] = ffma2(al1, pk2(D[2], D[3]), ffma2(be1, pk2(S[2], S[3]), acc[1]));
     }
 }
 
@@ -385,7 +558,7 @@ constexpr int GEMV_THREADS = (NC + 1) * 32;   // + the producer warp
 template <int TYPE> struct Stage;
 template <> struct Stage<kQ4_K> { static constexpr int STEP = 144, S = 8, PITCH = 1168, NST = 5; };
 template <> struct Stage<kQ5_K> { static constexpr int STEP = 176, S = 8, PITCH = 1424, NST = 4; };
-template <> struct Stage<kQ2_K> { static constexpr int STEP = 84, S = 8, PITCH = 688, NST = 8; };
+template <> struct Stage<kQ2_K> { static constexpr int STEP = 84, S = 16, PITCH = 1360, NST = 4; };
 template <> struct Stage<kQ6_K> { static constexpr int STEP = 210, S = 8, PITCH = 1712, NST = 3; };
 template <> struct Stage<kQ8_0> { static constexpr int STEP = 272, S = 4, PITCH = 1104, NST = 5; };
 template <> struct Stage<kF16> { static constexpr int STEP = 512, S = 2, PITCH = 1040, NST = 5; };
@@ -427,15 +600,23 @@ __device__ __forceinline__ BlockLoc block_loc(const GemvParams &gp, int b) {
     return {k, (b - (k ? gp.g[k - 1].blk_end : 0)) * ROWS, nsteps, (nsteps + Stage<TYPE>::S - 1) / Stage<TYPE>::S};
 }
 
-template <int TYPE>
+template <int TYPE> constexpr bool kIsKQuant = TYPE == kQ2_K || TYPE == kQ4_K || TYPE == kQ5_K || TYPE == kQ6_K;
+
+// NSB: sub-blocks per K-quant MMA (8 / T rounded up to a power of two); 1
+// for Q8_0 and F16, whose columns are the token rows.
+template <int TYPE, int NSB>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_constant__ GemvParams gp) {
     using G = Geom<TYPE>;
     using S = Stage<TYPE>;
     using Raw = typename RawOf<TYPE>::T;
     constexpr int TILE = tile_bytes<TYPE>();
-    constexpr int TEAMS = NC / S::S;                      // tiles in work at once
+    // S < NC: teams of S warps take whole tiles in turn; S >= NC: every warp
+    // takes S / NC steps of every tile
+    constexpr int TEAMS = S::S >= NC ? 1 : NC / S::S;     // tiles in work at once
+    constexpr int SPW = S::S >= NC ? S::S / NC : 1;       // steps per warp and tile
+    static_assert(S::S >= NC ? S::S % NC == 0 : NC % S::S == 0, "steps per tile");
     extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ float part[NC][ROWS][8];                   // each consumer warp's 16 weight rows x 8 tokens
+    __shared__ float part[2][NC][ROWS][8];                // each consumer warp's 16 weight rows x 8 columns, 2 buffers
     __shared__ __align__(8) uint64_t full[S::NST], empty[S::NST];
     __shared__ uint32_t stop_word, drain_failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -452,12 +633,15 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         mbar_fence_init();
     }
     __syncthreads();
-    grid_dependency_wait();                               // the previous grid's memory operations are done
     grid_launch_dependents();                             // the next grid may launch; it still waits for this one
     const int nblk = gp.g[gp.n - 1].blk_end;
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer --
+        // Block-quantized weights are streamed before the previous grid has
+        // finished (no kernel of this library writes them), so the ring fills
+        // while it drains; F16 weights may be such a kernel's output.
+        if constexpr (TYPE == kF16) grid_dependency_wait();
         // The CTA's tiles in order: block after block, each block's tiles
         // 0 .. ntiles - 1; tile n goes to slot n % NST.
         int n = 0;
@@ -522,13 +706,19 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------------------ consumers --
+        grid_dependency_wait();                           // X, Y: the previous grid's memory operations are done
         const int g = lane >> 2, c = lane & 3;
-        const int team = warp / S::S, sl = warp % S::S;   // this warp's team and step within a tile
+        const int team = S::S >= NC ? 0 : warp / S::S;    // this warp's team
+        const int sl = S::S >= NC ? warp : warp % S::S;   // ... and first step within a tile
         const int T = gp.T;
-        const bool tok = g < T;                           // this lane's B column is a token row
+        const bool tok = g < T;                           // Q8_0, F16: this lane's B column is a token row
+        const LaneMap<NSB> lm(g, c);                      // K-quants: the group layout
+        const bool pa = lm.j0 == lm.jg && lm.tg < T, pb = lm.j1 == lm.jg && lm.tg < T, pg = lm.tg < T;
         float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        pair_t acc[2] = {pk2(0.0f, 0.0f), pk2(0.0f, 0.0f)};
         bool live = true;
         int n0 = 0;                                       // the block's first tile in the CTA's sequence
+        int nb = 0;                                       // blocks done (partial-tile buffer nb % 2)
         for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
             const BlockLoc L = block_loc<TYPE>(gp, b);
             const GemvGroup &P = gp.g[L.grp];
@@ -540,6 +730,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                                         : static_cast<int>((reinterpret_cast<uintptr_t>(P.W) +
                                                             static_cast<uint64_t>(L.m0 + g + 8) * P.row_bytes) & 15);
             const uint16_t *xrow = P.X + static_cast<int64_t>(tok ? g : 0) * P.in_f;
+            const uint16_t *xcol = P.X + static_cast<int64_t>(pg ? lm.tg : 0) * P.in_f;
             for (int j = 0; j < L.ntiles; ++j) {
                 // Every consumer warp waits for every tile and releases it, also
                 // the tiles another team reads: a warp that skipped ring rounds
@@ -549,51 +740,66 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                 live = live && wait_phase_warp(&full[s], static_cast<uint32_t>((n / S::NST) & 1), gp.limit_ns, stop,
                                                gp.err, kErrTimeoutGemv);
                 if (!live) continue;
-                const int q = j * S::S + sl;              // this warp's step of the row
-                if (j % TEAMS == team && q < L.nsteps) {
-                    const int off = j * S::S * S::STEP;
-                    const uint8_t *slot = ring + s * TILE;
-                    const uint8_t *src0 = slot + g * S::PITCH + ((base0 + off) & 15) + sl * S::STEP;
-                    const uint8_t *src1 = slot + (g + 8) * S::PITCH + ((base1 + off) & 15) + sl * S::STEP;
-                    if constexpr (TYPE == kQ2_K) {
-                        step_q2k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
-                    } else if constexpr (TYPE == kQ6_K) {
-                        step_q6k(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c), tok, d, e);
-                    } else if constexpr (TYPE == kQ4_K || TYPE == kQ5_K) {
-                        step_k4<TYPE == kQ5_K>(src0, src1, c, reinterpret_cast<const uint4 *>(xrow + 256 * q + 64 * c),
-                                               tok, d, e);
-                    } else {
-                        const int nruns = (P.in_f + 31) / 32;
-                        const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
+                // this warp's steps of the tile: sl, sl + NC, ...
 #pragma unroll
-                        for (int rho = 0; rho < 2; ++rho) {
-                            const int t = 2 * c + rho;        // this lane's run of the step
-                            const int jr = 8 * q + t;         // ... and of the row
-                            const bool valid = jr < nruns;
-                            uint32_t h0[16], h1[16];
-                            if (valid && row0) {
-                                Raw raw;
-                                raw.template load<Smem>(src0 + (t / G::RPB) * G::BB, t % G::RPB);
-                                run_f16<TYPE>(raw, t % G::RPB, h0);
+                for (int us = 0; us < SPW; ++us) {
+                    const int sq = sl + us * NC;          // step of the tile
+                    const int q = j * S::S + sq;          // ... and of the row
+                    if (j % TEAMS == team && q < L.nsteps) {
+                        const int off = j * S::S * S::STEP;
+                        const uint8_t *slot = ring + s * TILE;
+                        const uint8_t *src0 = slot + g * S::PITCH + ((base0 + off) & 15) + sq * S::STEP;
+                        const uint8_t *src1 = slot + (g + 8) * S::PITCH + ((base1 + off) & 15) + sq * S::STEP;
+                        if constexpr (kIsKQuant<TYPE>) {
+                            const uint16_t *xs = xcol + 256 * q;
+                            const uint16_t *xa = pa ? xs : g_zero_x, *xb = pb ? xs : g_zero_x;
+                            const uint16_t *xg = pg ? xs : g_zero_x;
+                            if constexpr (TYPE == kQ6_K) {
+                                // rows g and g + 8 start alike modulo 4 (8 row pitches apart);
+                                // with TMA tiles every row of the step does
+                                const uint32_t sh = (smem_u32(src0) & 2u) ? 16u : 0u;
+                                if (__all_sync(0xffffffffu, sh != 0u))
+                                    step_codes<TYPE, NSB, 1>(src0, src1, sh, lm, xa, xb, xg, acc);
+                                else if (!__any_sync(0xffffffffu, sh != 0u))
+                                    step_codes<TYPE, NSB, 0>(src0, src1, sh, lm, xa, xb, xg, acc);
+                                else
+                                    step_codes<TYPE, NSB, 2>(src0, src1, sh, lm, xa, xb, xg, acc);
                             } else {
-#pragma unroll
-                                for (int p = 0; p < 16; ++p) h0[p] = 0u;
+                                step_codes<TYPE, NSB, 0>(src0, src1, 0u, lm, xa, xb, xg, acc);
                             }
-                            if (valid && row1) {
-                                Raw raw;
-                                raw.template load<Smem>(src1 + (t / G::RPB) * G::BB, t % G::RPB);
-                                run_f16<TYPE>(raw, t % G::RPB, h1);
-                            } else {
+                        } else {
+                            const int nruns = (P.in_f + 31) / 32;
+                            const bool row0 = L.m0 + g < P.out_f, row1 = L.m0 + g + 8 < P.out_f;
 #pragma unroll
-                                for (int p = 0; p < 16; ++p) h1[p] = 0u;
-                            }
-                            const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * jr);
-                            float (&acc)[4] = rho ? e : d;
+                            for (int rho = 0; rho < 2; ++rho) {
+                                const int t = 2 * c + rho;        // this lane's run of the step
+                                const int jr = 8 * q + t;         // ... and of the row
+                                const bool valid = jr < nruns;
+                                uint32_t h0[16], h1[16];
+                                if (valid && row0) {
+                                    Raw raw;
+                                    raw.template load<Smem>(src0 + (t / G::RPB) * G::BB, t % G::RPB);
+                                    run_f16<TYPE>(raw, t % G::RPB, h0);
+                                } else {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {     // 8 values of X per 16-byte load: two MMAs
-                                const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
-                                mma_16816(acc, h0[4 * u], h1[4 * u], h0[4 * u + 1], h1[4 * u + 1], x.x, x.y);
-                                mma_16816(acc, h0[4 * u + 2], h1[4 * u + 2], h0[4 * u + 3], h1[4 * u + 3], x.z, x.w);
+                                    for (int p = 0; p < 16; ++p) h0[p] = 0u;
+                                }
+                                if (valid && row1) {
+                                    Raw raw;
+                                    raw.template load<Smem>(src1 + (t / G::RPB) * G::BB, t % G::RPB);
+                                    run_f16<TYPE>(raw, t % G::RPB, h1);
+                                } else {
+#pragma unroll
+                                    for (int p = 0; p < 16; ++p) h1[p] = 0u;
+                                }
+                                const uint4 *xv = reinterpret_cast<const uint4 *>(xrow + 32 * jr);
+                                float (&dr)[4] = rho ? e : d;
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {     // 8 values of X per 16-byte load: two MMAs
+                                    const uint4 x = tok && valid ? __ldg(xv + u) : make_uint4(0u, 0u, 0u, 0u);
+                                    mma_16816(dr, h0[4 * u], h1[4 * u], h0[4 * u + 1], h1[4 * u + 1], x.x, x.y);
+                                    mma_16816(dr, h0[4 * u + 2], h1[4 * u + 2], h0[4 * u + 3], h1[4 * u + 3], x.z, x.w);
+                                }
                             }
                         }
                     }
@@ -602,22 +808,53 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
             n0 += L.ntiles;
-            // block end: D rows g, g + 8 (weight rows), columns 2c, 2c + 1 (tokens)
-            part[warp][g][2 * c] = d[0] + e[0];
-            part[warp][g][2 * c + 1] = d[1] + e[1];
-            part[warp][g + 8][2 * c] = d[2] + e[2];
-            part[warp][g + 8][2 * c + 1] = d[3] + e[3];
+            // block end: D rows g, g + 8 (weight rows), columns 2c, 2c + 1 (token
+            // n / NSB, sub-block n % NSB)
+            float v[4];
+            if constexpr (kIsKQuant<TYPE>) {
+                unpk2(acc[0], v[0], v[1]);
+                unpk2(acc[1], v[2], v[3]);
+                acc[0] = acc[1] = pk2(0.0f, 0.0f);
+            } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) d[k] = e[k] = 0.0f;
-            named_barrier_sync(1, NC * 32);
-            for (int o = threadIdx.x; o < ROWS * 8; o += NC * 32) {
-                const int tt = o / ROWS, r = o % ROWS;    // consecutive threads: consecutive rows of Y
-                float v = 0.0f;
+                for (int k = 0; k < 4; ++k) {
+                    v[k] = d[k] + e[k];
+                    d[k] = e[k] = 0.0f;
+                }
+            }
+            // The sub-block columns of a token are summed in the warp (fixed
+            // shuffle order), the warps' tiles through shared memory in warp
+            // order.  The tiles are double buffered: a warp writes the next
+            // block's tile into the other buffer, and it reaches the block
+            // after that only past the next block's barrier, which this
+            // block's readers reach after their reads; so one barrier a block.
+            float (&pw)[ROWS][8] = part[nb & 1][warp];
+            if constexpr (NSB == 1) {
+                pw[g][2 * c] = v[0];
+                pw[g][2 * c + 1] = v[1];
+                pw[g + 8][2 * c] = v[2];
+                pw[g + 8][2 * c + 1] = v[3];
+            } else {
+                float y0 = v[0] + v[1], y1 = v[2] + v[3];     // token 2c / NSB, rows g and g + 8
 #pragma unroll
-                for (int w = 0; w < NC; ++w) v += part[w][r][tt];
-                if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = v;
+                for (int m = 1; m < NSB / 2; m <<= 1) {      // the lanes c of one token
+                    y0 += __shfl_xor_sync(0xffffffffu, y0, m);
+                    y1 += __shfl_xor_sync(0xffffffffu, y1, m);
+                }
+                if ((c & (NSB / 2 - 1)) == 0) {
+                    pw[g][2 * c / NSB] = y0;
+                    pw[g + 8][2 * c / NSB] = y1;
+                }
             }
             named_barrier_sync(1, NC * 32);
+            for (int o = threadIdx.x; o < ROWS * (8 / NSB); o += NC * 32) {
+                const int tt = o / ROWS, r = o % ROWS;    // consecutive threads: consecutive rows of Y
+                float y = 0.0f;
+#pragma unroll
+                for (int w = 0; w < NC; ++w) y += part[nb & 1][w][r][tt];
+                if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = y;
+            }
+            ++nb;
         }
     }
     __syncthreads();
@@ -645,9 +882,9 @@ bool encode_w(void *encode_fn, const void *W, int64_t row_bytes, int64_t out_f, 
 // ring runs on from one block into its next, across the projections of the
 // launch.  Launched with programmatic stream serialization (the kernel waits
 // for the previous grid before it reads or writes).
-template <int TYPE>
-cudaError_t launch_typed(const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env) {
-    auto kern = gemv_kernel<TYPE>;
+template <int TYPE, int NSB>
+cudaError_t launch_nsb(const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env) {
+    auto kern = gemv_kernel<TYPE, NSB>;
     constexpr int smem = gemv_smem<TYPE>();
     static std::atomic<int> smem_set[kMaxDevices];        // the opt-in holds per device
     if (!smem_set[env.device].load()) {
@@ -686,6 +923,19 @@ cudaError_t launch_typed(const GemvArgs *a, int n, cudaStream_t stream, const La
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, gp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// The K-quants take NSB = 8 / T rounded up to a power of two (8 / NSB token
+// columns per MMA); Q8_0 and F16 one column per token.
+template <int TYPE>
+cudaError_t launch_typed(const GemvArgs *a, int n, cudaStream_t stream, const LaunchEnv &env) {
+    if constexpr (kIsKQuant<TYPE>) {
+        const int64_t T = a[0].T;
+        if (T == 1) return launch_nsb<TYPE, 8>(a, n, stream, env);
+        if (T == 2) return launch_nsb<TYPE, 4>(a, n, stream, env);
+        if (T <= 4) return launch_nsb<TYPE, 2>(a, n, stream, env);
+    }
+    return launch_nsb<TYPE, 1>(a, n, stream, env);
 }
 
 }  // namespace

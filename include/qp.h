@@ -203,12 +203,19 @@ qp_status qp_prefill_chunked(int type, const void *W, const uint16_t *W16, int64
  * Decode-side projection over the same weights (PR #4624 §What changes: the
  * serial prefill is one forward per prompt token; issue #4952 §Cause: the
  * decode GEMVs run over the same block types):
- *   Y[t, o] = sum_k X[t, k] * W16[o, k]      0 <= t < T <= QP_GEMV_MAX_T
- * with W16 = the fp16 weights qp_dequant_f16 gives (the weights
- * qp_prefill_gemm multiplies), exact products and f32 accumulation on the
- * tensor cores, W read once.  Deterministic run to run; within the GEMM
- * tolerance of the fp64 reference (not bitwise equal to qp_prefill_gemm,
- * whose f32 sums run in another order).
+ *   Y[t, o] = sum_k X[t, k] * Wd[o, k]      0 <= t < T <= QP_GEMV_MAX_T
+ * with Wd = the f32 weights qp_dequant_f32 gives for the K-quants (Q2_K,
+ * Q4_K, Q5_K, Q6_K: the quantized codes are multiplied exactly on the
+ * tensor cores and each sub-block's scale and min applied in f32) and the
+ * fp16 weights qp_dequant_f16 gives for Q8_0 and F16; f32 accumulation, W
+ * read once.  A one-hot X row returns a column of Wd bit for bit.
+ * Deterministic run to run; within the GEMM tolerance of the fp64
+ * reference (not bitwise equal to qp_prefill_gemm, which multiplies the
+ * fp16 weights and sums in another order).  The launch may start before an
+ * earlier kernel on the stream has finished when that kernel allows it (this
+ * library's kernels do); block-quantized W is then read right away, so it
+ * must not be the output of such a kernel (F16 weights, which
+ * qp_dequant_f16 may just have written, are read only after it).
  *   W   device, out_f * qp_row_bytes(type, in_f) bytes, 16-byte aligned
  *   X   device, [T x in_f] fp16 row-major, 16-byte aligned
  *   Y   device, [T x out_f] f32 row-major, 4-byte aligned

@@ -1,8 +1,9 @@
 """GPU parity of qp_decode_gemv (the decode-side projection over the same
 weight blocks, T = 1..8 token rows) against the CPU oracle's fp64
 reference: the GEMM tolerance of the workload definition, exact one-hot
-rows (the GEMV multiplies the fp16 weights of qp_dequant_f16, as the prefill
-GEMM does), determinism."""
+rows (the GEMV multiplies the exact f32 weights of qp_dequant_f32 for the
+K-quants, and the fp16 weights of qp_dequant_f16 for Q8_0 and F16),
+determinism, and every token-column layout of the K-quant kernels."""
 import numpy as np
 import pytest
 
@@ -50,12 +51,22 @@ def test_decode_gemv_vs_oracle(cuda_device, qtype, out_f, in_f, T):
     assert_gemm_within_tolerance(Y, Yref, A, "gemv %d %dx%d T=%d" % (qtype, out_f, in_f, T))
 
 
+KQUANTS = [qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K]
+
+
 @pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
-def test_decode_gemv_one_hot_rows_give_the_f16_weights(cuda_device, qtype):
+def test_decode_gemv_one_hot_rows_give_the_weights(cuda_device, qtype):
+    """A one-hot X row returns a column of the weights bit for bit: the f32
+    dequant for the K-quants (their codes are multiplied as exact fp16
+    subnormals and the sub-block scales applied in f32), the fp16 dequant
+    for Q8_0 and F16."""
     out_f, in_f = 96, 2048
     w = synth.blocks(qtype, out_f, in_f, seed=13, tensor=qtype)
-    W = oracle.dequant_f16(qtype, w, out_f, in_f).view(np.float16).astype(np.float32)
-    for ks in ([0, 31, 32, 255, 256, 1000, 2047, 1024], [7], [2046, 1]):
+    if qtype in KQUANTS:
+        W = oracle.dequant_f32(qtype, w, out_f, in_f)
+    else:
+        W = oracle.dequant_f16(qtype, w, out_f, in_f).view(np.float16).astype(np.float32)
+    for ks in ([0, 31, 32, 255, 256, 1000, 2047, 1024], [7], [2046, 1], [15, 16, 17], [300, 511, 512, 513, 1535]):
         X = np.zeros((len(ks), in_f), np.float16)
         for t, k in enumerate(ks):
             X[t, k] = 1.0
@@ -65,6 +76,21 @@ def test_decode_gemv_one_hot_rows_give_the_f16_weights(cuda_device, qtype):
             # under a negative scale) comes out +0, as IEEE addition gives
             want = W[:, k] + np.float32(0.0)
             assert np.array_equal(Y[t].view(np.uint32), want.view(np.uint32)), (qtype, k)
+
+
+@pytest.mark.parametrize("qtype", KQUANTS)
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("out_f,in_f", [(48, 1024), (40, 1280)])
+def test_decode_gemv_every_token_layout(cuda_device, qtype, T, out_f, in_f):
+    """The K-quant kernels take 8 / T sub-blocks per MMA (T rounded up to a
+    power of two): each layout, with TMA-staged rows and, at in_f = 1280,
+    Q2_K and Q6_K rows whose pitch is no multiple of 16 bytes (staged row by
+    row; Q6_K rows then start 2 bytes past a word every other row)."""
+    w = synth.blocks(qtype, out_f, in_f, seed=40 + T, tensor=qtype)
+    X = synth.normal_f16((T, in_f), seed=50 + T, tensor=3)
+    Y = gemv(qtype, dev(w), out_f, in_f, dev(X), T).cpu().numpy()
+    Yref, A = oracle.gemm_f64(X, oracle.dequant_f32(qtype, w, out_f, in_f))
+    assert_gemm_within_tolerance(Y, Yref, A, "gemv %d %dx%d T=%d" % (qtype, out_f, in_f, T))
 
 
 def test_decode_gemv_is_deterministic(cuda_device):
