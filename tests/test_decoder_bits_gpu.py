@@ -10,8 +10,10 @@ weight is a finite fp16 number.
   of the fp16 weight, so every fp16 weight the decoders produce is compared
   with the oracle's, exactly; and random X against the fp64 oracle at the
   workload tolerance.  Both tilings.
-- GEMV: one-hot rows over every column of the weight (eight per launch),
-  exact, and random X against the oracle.
+- GEMV: one-hot rows over every column of the weight (1, 2, 4 or 8 per
+  launch: each token-column layout of the K-quant kernels), exact (the f32
+  weights for the K-quants, the fp16 weights for Q8_0), and random X
+  against the oracle.
 """
 import numpy as np
 import pytest
@@ -79,15 +81,21 @@ def test_gemm_random_fields_vs_oracle(cuda_device, tiling, qtype):
     assert_gemm_within_tolerance(Y.cpu().numpy(), Yref, A, "random fields %s" % ID[qtype])
 
 
+@pytest.mark.parametrize("T", [8, 4, 2, 1])
 @pytest.mark.parametrize("in_f", [2048, 1280], ids=["tma_tiles", "row_copies"])
 @pytest.mark.parametrize("qtype", QUANT_TYPES, ids=lambda q: ID[q])
-def test_gemv_one_hot_over_every_column(cuda_device, qtype, in_f):
+def test_gemv_one_hot_over_every_column(cuda_device, qtype, in_f, T):
     """Every weight of every row, exactly.  With 1280 values a Q2_K or Q6_K
     row is not a whole number of 16-byte words, so the rows are staged by one
-    copy each and (Q6_K) every other row starts 2 bytes past a word."""
+    copy each and (Q6_K) every other row starts 2 bytes past a word.  A -0
+    weight comes out +0 (it is added to +0 sums)."""
     t = torch()
-    out_f, T = 72, 8
+    out_f = 72
     w, W16 = weights(qtype, out_f, in_f, seed=43)
+    if qtype == qp.Q8_0:
+        want = W16.astype(np.float32) + np.float32(0.0)
+    else:
+        want = oracle.dequant_f32(qtype, w, out_f, in_f) + np.float32(0.0)
     Wd = dev(w)
     n = in_f // T
     X = np.zeros((n, T, in_f), np.float16)
@@ -100,7 +108,7 @@ def test_gemv_one_hot_over_every_column(cuda_device, qtype, in_f):
         qp.qp_decode_gemv(qtype, Wd, out_f, in_f, Xd[j], T, Y[j])
     qp.qp_check()
     got = Y.cpu().numpy().reshape(in_f, out_f)
-    assert np.array_equal(got, W16.astype(np.float32).T)
+    assert np.array_equal(got.view(np.uint32), np.ascontiguousarray(want.T).view(np.uint32))
 
 
 @pytest.mark.parametrize("qtype", QUANT_TYPES, ids=lambda q: ID[q])
