@@ -118,3 +118,38 @@ def test_grouped_decode_gemv_equals_single_calls_bitwise(cuda_device, qtype):
     qp.qp_check()
     for k, (a, b) in enumerate(zip(singles, ys)):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32)), shapes[k]
+
+
+def test_decode_gemv_reads_operands_written_just_before(cuda_device):
+    """A GEMV may start while the previous kernel on the stream (one of this
+    library's, which let the next launch begin early) still runs.  F16
+    weights that qp_dequant_f16 writes right before it are read only after
+    that kernel, and so is X: here X is itself the output of a dequant
+    launched just before a K-quant GEMV.  Repeated with fresh values, so
+    stale data would show."""
+    import torch
+    out_f, in_f, T = 512, 4096, 1
+    for rep in range(3):
+        w = synth.blocks(qp.Q4_K, out_f, in_f, seed=60 + rep, tensor=1)
+        Wd = dev(w)
+        W16 = torch.full((out_f, in_f), float("nan"), dtype=torch.float16, device="cuda")
+        X = dev(synth.normal_f16((T, in_f), seed=61 + rep, tensor=2))
+        Y1 = torch.full((T, out_f), float("nan"), dtype=torch.float32, device="cuda")
+        qp.qp_dequant_f16(qp.Q4_K, Wd, out_f, in_f, W16)
+        qp.qp_decode_gemv(qp.F16, W16, out_f, in_f, X, T, Y1)
+        # X of the next GEMV: a 1 x 512 Q4_K tensor dequantized right before it
+        xq = synth.blocks(qp.Q4_K, T, out_f, seed=62 + rep, tensor=3)
+        X2 = torch.full((T, out_f), float("nan"), dtype=torch.float16, device="cuda")
+        w2 = synth.blocks(qp.Q2_K, 256, out_f, seed=63 + rep, tensor=4)
+        W2d = dev(w2)
+        Y2 = torch.full((T, 256), float("nan"), dtype=torch.float32, device="cuda")
+        qp.qp_dequant_f16(qp.Q4_K, dev(xq), T, out_f, X2)
+        qp.qp_decode_gemv(qp.Q2_K, W2d, 256, out_f, X2, T, Y2)
+        qp.qp_check()
+        Wf = oracle.dequant_f16(qp.Q4_K, w, out_f, in_f).view(np.float16).astype(np.float32)
+        Yref, A = oracle.gemm_f64(X.cpu().numpy(), Wf)
+        assert_gemm_within_tolerance(Y1.cpu().numpy(), Yref, A, "F16 GEMV after the dequant of its weights")
+        X2ref = oracle.dequant_f16(qp.Q4_K, xq, T, out_f).view(np.float16)
+        assert np.array_equal(X2.cpu().numpy().view(np.uint16), X2ref.view(np.uint16))
+        Y2ref, A2 = oracle.gemm_f64(X2ref, oracle.dequant_f32(qp.Q2_K, w2, 256, out_f))
+        assert_gemm_within_tolerance(Y2.cpu().numpy(), Y2ref, A2, "Q2_K GEMV after the dequant of its X")
