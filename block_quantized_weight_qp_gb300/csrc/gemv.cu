@@ -587,14 +587,14 @@ struct GemvParams {
 };
 
 // Block b of the launch: its projection, first weight row, steps per row
-// and tiles.
+// and tiles.  A CTA's blocks only increase, so the projection search starts
+// at the previous block's (k).
 struct BlockLoc {
     int grp, m0, nsteps, ntiles;
 };
 
 template <int TYPE>
-__device__ __forceinline__ BlockLoc block_loc(const GemvParams &gp, int b) {
-    int k = 0;
+__device__ __forceinline__ BlockLoc block_loc(const GemvParams &gp, int b, int &k) {
     while (k < gp.n - 1 && b >= gp.g[k].blk_end) ++k;
     const int nsteps = (gp.g[k].in_f + STEP_VALUES - 1) / STEP_VALUES;
     return {k, (b - (k ? gp.g[k - 1].blk_end : 0)) * ROWS, nsteps, (nsteps + Stage<TYPE>::S - 1) / Stage<TYPE>::S};
@@ -639,18 +639,23 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
     if (warp == NC) {
         // ------------------------------------------------------------ producer --
         // Block-quantized weights are streamed before the previous grid has
-        // finished (no kernel of this library writes them), so the ring fills
-        // while it drains; F16 weights may be such a kernel's output.
+        // finished (no kernel of this library writes them): the first NST
+        // tiles, whose slots are free, fill the ring while it drains.  The
+        // producer waits for that grid before its first wait on a slot, which
+        // needs consumers past their own dependency wait, so the time limit
+        // never runs while the previous grid does.  F16 weights may be such a
+        // kernel's output: their producer waits first.
         if constexpr (TYPE == kF16) grid_dependency_wait();
         // The CTA's tiles in order: block after block, each block's tiles
         // 0 .. ntiles - 1; tile n goes to slot n % NST.
-        int n = 0;
+        int n = 0, kp = 0;
         bool ok = true;
         for (int b = blockIdx.x; ok && b < nblk; b += gridDim.x) {
-            const BlockLoc L = block_loc<TYPE>(gp, b);
+            const BlockLoc L = block_loc<TYPE>(gp, b, kp);
             const GemvGroup &P = gp.g[L.grp];
             for (int j = 0; j < L.ntiles; ++j, ++n) {
                 const int s = n % S::NST;
+                if (TYPE != kF16 && n == S::NST) grid_dependency_wait();
                 if (!wait_phase_warp(&empty[s], ((n / S::NST) & 1) ^ 1u, gp.limit_ns, stop, gp.err,
                                      kErrTimeoutGemv)) {
                     ok = false;
@@ -719,8 +724,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         bool live = true;
         int n0 = 0;                                       // the block's first tile in the CTA's sequence
         int nb = 0;                                       // blocks done (partial-tile buffer nb % 2)
+        int kp = 0;                                       // the current block's projection
         for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
-            const BlockLoc L = block_loc<TYPE>(gp, b);
+            const BlockLoc L = block_loc<TYPE>(gp, b, kp);
             const GemvGroup &P = gp.g[L.grp];
             // rows g, g + 8: the row's start modulo 16 (0 when staged by TMA)
             const int base0 = P.use_tma ? 0
