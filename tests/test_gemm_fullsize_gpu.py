@@ -147,3 +147,32 @@ def test_chunk_check_rows_cover_every_boundary():
         assert c - 1 in rows and c in rows
     assert 31257 in rows and 0 in rows and 16 in rows
     assert np.all(np.diff(rows) > 0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["qwen3_8b_q2k_q6k_t8192", "qwen3_8b_q5k_t8192"])
+@pytest.mark.parametrize("T", [1, 8])
+def test_full_size_decode_gemv_every_output_vs_oracle(cuda_device, name, T):
+    """The decode GEMV over a whole 8B-shaped layer's weights, issued as the
+    benchmark issues it (one grouped launch per run of one block type, here
+    for T = 1 and 8 token rows): every element of all seven outputs against
+    the fp64 oracle at the workload tolerance."""
+    t = torch()
+    wl = workloads.WORKLOADS[name]
+    dims = workloads.input_dims(wl)
+    X = {k: synth.normal_f16((T, dims[k]), seed=wl["seed"], tensor=3000 + i) for i, k in enumerate(dims)}
+    Xd = {k: dev(v) for k, v in X.items()}
+    W = [synth.blocks(qt, out_f, in_f, seed=wl["seed"], tensor=i)
+         for i, (_, out_f, in_f, _, qt) in enumerate(wl["projections"])]
+    Wd = [dev(w) for w in W]
+    Y = [t.full((T, out_f), float("nan"), dtype=t.float32, device="cuda")
+         for (_, out_f, _, _, _) in wl["projections"]]
+    for qt, idx in workloads.type_runs(wl["projections"]):
+        descs = [(Wd[i], wl["projections"][i][1], wl["projections"][i][2], Xd[wl["projections"][i][3]], Y[i])
+                 for i in idx]
+        qp.qp_decode_gemv_group(qt, descs, T)
+    qp.qp_check()
+    rows = np.arange(T, dtype=np.int64)
+    for i, (pname, out_f, in_f, src, qt) in enumerate(wl["projections"]):
+        W32 = oracle.dequant_f32(qt, W[i], out_f, in_f)
+        check_rows(Y[i], X[src], W32, rows, "gemv %s/%s T=%d" % (name, pname, T))
