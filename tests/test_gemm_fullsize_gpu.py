@@ -150,7 +150,7 @@ def test_chunk_check_rows_cover_every_boundary():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["qwen3_8b_q2k_q6k_t8192", "qwen3_8b_q5k_t8192"])
+@pytest.mark.parametrize("name", ["qwen3_8b_q2k_q6k_t8192", "qwen3_8b_q4k_t31258_chunk4864", "qwen3_8b_q5k_t8192"])
 @pytest.mark.parametrize("T", [1, 8])
 def test_full_size_decode_gemv_every_output_vs_oracle(cuda_device, name, T):
     """The decode GEMV over a whole 8B-shaped layer's weights, issued as the
