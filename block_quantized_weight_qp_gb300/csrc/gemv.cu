@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
     constexpr int SPW = S::S >= NC ? S::S / NC : 1;       // steps per warp and tile
     static_assert(S::S >= NC ? S::S % NC == 0 : NC % S::S == 0, "steps per tile");
     extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ float part[2][NC][ROWS][8];                // each consumer warp's 16 weight rows x 8 columns, 2 buffers
+    __shared__ float part[2][NC][ROWS][8 / NSB];          // each consumer warp's 16 weight rows x tokens, 2 buffers
     __shared__ __align__(8) uint64_t full[S::NST], empty[S::NST];
     __shared__ uint32_t stop_word, drain_failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -834,7 +834,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
             // block's tile into the other buffer, and it reaches the block
             // after that only past the next block's barrier, which this
             // block's readers reach after their reads; so one barrier a block.
-            float (&pw)[ROWS][8] = part[nb & 1][warp];
+            float (&pw)[ROWS][8 / NSB] = part[nb & 1][warp];
             if constexpr (NSB == 1) {
                 pw[g][2 * c] = v[0];
                 pw[g][2 * c + 1] = v[1];
