@@ -20,9 +20,10 @@
 // shared-memory tiles with 2-D TMA copies: a tile is the 16 rows x S steps
 // (S x 256 values) of one K range, as the 16-byte aligned cover of that range
 // in every row (up to 2 KB per row, so that the copies are long).  Eight
-// consumer warps split the tiles: warp w takes step w % S of every tile its
-// team w / S is given (the teams take a block's tiles in turn); every
-// consumer warp still waits for and releases every tile.  Measured on
+// consumer warps split the tiles: with S < 8 (Q8_0, F16), warp w takes step
+// w % S of every tile its team w / S is given (the teams take a block's tiles
+// in turn); with S >= 8, warp w takes steps w, w + 8, ... of every tile.
+// Every consumer warp waits for and releases every tile.  Measured on
 // the 8B-shaped layer's weights at T = 1, two such CTAs per SM stream 13%
 // faster than one with twice the warps and ring.  A step is 256 values of
 // weight rows g and g + 8 for lane (g, c) (g = lane / 4, c = lane % 4): the
