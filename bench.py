@@ -350,8 +350,8 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
     Q2_K layer the six Q2_K projections, then the Q6_K down projection),
     captured in a CUDA graph as a decode loop would run it.  Also timed: the
     same launches made eagerly, and the seven projections launched one at a
-    time (graph).  The weights (88 MB for the Q2_K layer, 155-189 MB for the
-    Q4_K and Q5_K ones) fit in L2 or nearly, so before every timed step a 256 MB
+    time (graph).  The weights (88 MB for the Q2_K layer, 108.5 and 132.6 MB for
+    the Q4_K and Q5_K ones) fit in L2 or nearly, so before every timed step a 256 MB
     buffer is written (outside the timed region: events bracket the GEMV
     launches of each step only).  GB/s counts the weight bytes plus the X and
     Y bytes of a step.
