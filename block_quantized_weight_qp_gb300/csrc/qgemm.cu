@@ -16,7 +16,8 @@
 //          two CTAs on two SMs computes a 256-row x 256-token tile with the
 //          paired MMA (tcgen05 cta_group::2, M = 256); each CTA stages (or
 //          decodes) its own 128 weight rows and 128 of the tokens, so each
-//          SM's shared memory carries half the token operand.
+//          SM's shared memory carries half the token operand.  The fused
+//          pair kernel's stages hold two 64-value K panels each.
 //   one CTA (prefill_gemm_kernel): 128-row x 256-token tiles, M = 128.
 // Both run each output through the same K steps and give bitwise equal Y.
 // Roles (one-CTA kernel; the pair kernels keep the same warp layout, with
@@ -457,7 +458,10 @@ template <int WO> struct Dec<kQ8_0, WO> {
 #else
 #define QP_SLICE_INLINE __forceinline__
 #endif
-template <int TYPE, int WO, int S>
+// PPS: K panels (64-value K steps) per W16 stage: 1 (single-CTA kernel), or
+// 2 (pair kernel: a stage is two 16 KiB panels, one barrier round per
+// 128 values of K).
+template <int TYPE, int WO, int S, int PPS = 1>
 __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *row, uint32_t hs16, int p,
                                               uint32_t ws_addr, const ChunkAddr &ca, uint64_t *qempty, int lane,
                                               int &stage, uint32_t &phase, uint64_t limit_ns, uint32_t *err) {
@@ -467,11 +471,27 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty);
     }
-    // The atoms go in pairs: both stages are written, then one proxy fence
-    // makes the pair's stores visible to the tensor cores before either
-    // stage's arrive (one fence per atom measured 1.2% slower on the Q6_K
-    // down projection).  The second stage's wait needs no arrive of the first:
-    // the ring is at least two stages deep.
+    // The atoms go in pairs: both K panels are written, then one proxy fence
+    // makes the pair's stores visible to the tensor cores before the arrive
+    // (one fence per atom measured 1.2% slower on the Q6_K down projection).
+    // With one panel per stage the pair spans two stages, and the second
+    // stage's wait needs no arrive of the first: the ring is at least two
+    // stages deep.  With two panels per stage the pair is one stage.
+#define QP_DEQUANT_STAGE2(A)                                                                                   \
+    {                                                                                                          \
+        if (!wait_phase_warp(&sh.emptyw[stage], phase ^ 1u, limit_ns, sh.stop, err, kErrTimeoutDequant)) \
+            return false;                                                                                      \
+        const uint32_t st = ws_addr + static_cast<uint32_t>(stage * 2 * W_STAGE_BYTES);                        \
+        dec.template atom<A>(row, hs16, p, st, ca);                                                            \
+        dec.template atom<A + 1>(row, hs16, p, st + W_STAGE_BYTES, ca);                                        \
+        fence_proxy_async_smem();                                                                              \
+        __syncwarp();                                                                                          \
+        if (lane == 0) {                                                                                       \
+            if (sh.fullw_remote) mbar_arrive_remote(sh.fullw_remote + static_cast<uint32_t>(stage * 8));       \
+            else mbar_arrive(&sh.fullw[stage]);                                                                \
+        }                                                                                                      \
+        advance(stage, phase, S);                                                                              \
+    }
 #define QP_DEQUANT_PAIR(A)                                                                                     \
     {                                                                                                          \
         const int s0 = stage;                                                                                  \
@@ -495,15 +515,21 @@ __device__ QP_SLICE_INLINE bool dequant_slice(const Shared &sh, const uint8_t *r
         }                                                                                                      \
         advance(stage, phase, S);                                                                              \
     }
-    static_assert(S >= 2, "a pair of atoms needs two W stages");
-    QP_DEQUANT_PAIR(0)
-    QP_DEQUANT_PAIR(2)
+    if constexpr (PPS == 2) {
+        QP_DEQUANT_STAGE2(0)
+        QP_DEQUANT_STAGE2(2)
+    } else {
+        static_assert(PPS == 1 && S >= 2, "a pair of atoms needs two W stages");
+        QP_DEQUANT_PAIR(0)
+        QP_DEQUANT_PAIR(2)
+    }
 #undef QP_DEQUANT_PAIR
+#undef QP_DEQUANT_STAGE2
     return true;
 }
 
 // (first, stride): this CTA's tile sequence.
-template <int TYPE, int WST, int QST>
+template <int TYPE, int WST, int QST, int PPS = 1>
 __device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams &gp, int first, int stride,
                                              const uint8_t *qslots, uint32_t ws_addr, int r, int p, int lane,
                                              uint64_t limit_ns, uint32_t *err) {
@@ -521,13 +547,13 @@ __device__ __forceinline__ void dequant_role(const Shared &sh, const GroupParams
             bool ok;
             if constexpr (TYPE == kQ2_K || TYPE == kQ6_K) {
                 switch (rem >> 2) {
-                case 0: ok = dequant_slice<TYPE, 0, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                case 1: ok = dequant_slice<TYPE, 1, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                case 2: ok = dequant_slice<TYPE, 2, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
-                default: ok = dequant_slice<TYPE, 3, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 0: ok = dequant_slice<TYPE, 0, WST, PPS>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 1: ok = dequant_slice<TYPE, 1, WST, PPS>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                case 2: ok = dequant_slice<TYPE, 2, WST, PPS>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
+                default: ok = dequant_slice<TYPE, 3, WST, PPS>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err); break;
                 }
             } else {
-                ok = dequant_slice<TYPE, 0, WST>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err);
+                ok = dequant_slice<TYPE, 0, WST, PPS>(sh, row, hs16, p, ws_addr, ca, &sh.qempty[qs], lane, stage, phase, limit_ns, err);
             }
             if (!ok) return;
             if constexpr (!Dec<TYPE, 0>::REGS) {
@@ -987,22 +1013,27 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
 // accfull in both CTAs.  (A forwarding thread in the peer that waited on the
 // peer's own barrier and passed one arrival on measured 2% slower on the
 // Q2_K launch.)
-// Ring depths and epilogue staging buffers per warp.  The token ring (16 KiB
-// stages) is the one that pays for depth (measured on the Q2_K / Q6_K layer:
-// 4 -> 6 -> 8 stages, +5% then +0.5%); more fp16 W stages or a second slice
-// slot did not help.
-template <int TYPE> struct PairDepth { static constexpr int XST = 6, WST = 4, QST = 1, EPI = 2; };
-template <> struct PairDepth<kQ8_0> { static constexpr int XST = 4, WST = 4, QST = 2, EPI = 1; };
+// A stage holds two 64-value K panels of both operands (X: 2 x 16 KiB of
+// this CTA's tokens; W16: 2 x 16 KiB), so the MMA thread and the decode warps
+// meet once per 128 values of K: measured on the 8B-shaped layer against
+// one-panel stages of the same bytes (6 X, 4 W16): Q2_K launch +1.8%, Q6_K
+// launch +5.1%.  Ring depths in stages and epilogue staging buffers per warp.
+// The token ring is the one that pays for depth (measured with one-panel
+// stages on the Q2_K / Q6_K layer: 4 -> 6 -> 8 stages, +5% then +0.5%); more
+// fp16 W stages or a second slice slot did not help.
+template <int TYPE> struct PairDepth { static constexpr int XST = 3, WST = 2, QST = 1, EPI = 2; };
+template <> struct PairDepth<kQ8_0> { static constexpr int XST = 2, WST = 2, QST = 2, EPI = 1; };
 
 template <int TYPE> struct PairFCfg {
     static constexpr int XST = PairDepth<TYPE>::XST, WST = PairDepth<TYPE>::WST, QST = PairDepth<TYPE>::QST;
     static constexpr int EPI = PairDepth<TYPE>::EPI;
-    static constexpr int X_HALF = 128 * BK * 2;                  // 16 KiB: this CTA's 128 tokens
+    static constexpr int X_HALF = 128 * BK * 2;                  // 16 KiB: this CTA's 128 tokens, one panel
+    static constexpr int X_ST = 2 * X_HALF, W_ST = 2 * W_STAGE_BYTES;   // a stage: two K panels
     static constexpr int THREADS = 16 * 32;
     static constexpr int Q_SLOT_BYTES = BM * QFmt<TYPE>::BOX;
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_W = OFF_X + XST * X_HALF;
-    static constexpr int OFF_Q = OFF_W + WST * W_STAGE_BYTES;
+    static constexpr int OFF_W = OFF_X + XST * X_ST;
+    static constexpr int OFF_Q = OFF_W + WST * W_ST;
     static constexpr int OFF_EPI = OFF_Q + QST * Q_SLOT_BYTES;   // 4 epilogue warps x EPI x 4 KiB
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI * 4096;
     // fullx, emptyx, fullw, emptyw, qfull, qempty, accfull[2], accempty[2], done
@@ -1085,7 +1116,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
     if (alloc_ok && warp == 0) {
         // --------------------------------------------------------- producer --
         if (lane == 0) {
-            int stage = 0, qs = 0, loads = 0, qloads = 0;
+            int stage = 0, qs = 0, loads = 0, qloads = 0, skip_arm = -1;   // loads: token stages armed
             uint32_t phase = 0, qphase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const TileLoc L = locate(gp, tile);
@@ -1102,14 +1133,20 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                     ++qloads;
                     advance(qs, qphase, QS);
 #pragma unroll 1
-                    for (int a = 0; a < SB / BK; ++a) {
+                    for (int a = 0; a < SB / BK; a += 2) {   // a stage: K panels a, a + 1
                         if (!wait_phase(&sh.emptyx[stage], phase ^ 1u, limit_ns, sh.stop, err,
                                         kErrTimeoutProducer))
                             goto producer_done;
-                        if (rank == 0) mbar_arrive_expect_tx(&sh.fullx[stage], 2 * C::X_HALF);
-                        if (loads != inject_stall)
-                            tma_load_2d_pair(xs + stage * C::X_HALF, tmX, mapa_shared(smem_u32(&sh.fullx[stage]), 0u),
-                                             kb * SB + a * BK, n0);
+                        if (rank == 0) mbar_arrive_expect_tx(&sh.fullx[stage], 4 * C::X_HALF);
+                        // the test hook counts loads in panels; the stage holding
+                        // the named panel gets no copies at all
+                        if (inject_stall == 2 * loads || inject_stall == 2 * loads + 1) {
+                            skip_arm = loads;
+                        } else {
+                            const uint32_t fx = mapa_shared(smem_u32(&sh.fullx[stage]), 0u);
+                            tma_load_2d_pair(xs + stage * C::X_ST, tmX, fx, kb * SB + a * BK, n0);
+                            tma_load_2d_pair(xs + stage * C::X_ST + C::X_HALF, tmX, fx, kb * SB + (a + 1) * BK, n0);
+                        }
                         ++loads;
                         advance(stage, phase, XS);
                     }
@@ -1119,7 +1156,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             // Each CTA's slice copies complete on its own barriers; the token
             // halves of both CTAs on the leader's.
             bool drained = drain_ring(sh.qfull, QS, qloads, -1, limit_ns);
-            if (rank == 0) drained = drain_ring(sh.fullx, XS, loads, inject_stall, limit_ns) && drained;
+            if (rank == 0) drained = drain_ring(sh.fullx, XS, loads, skip_arm, limit_ns) && drained;
             if (!drained) {
                 *sh.drain_failed = 1u;
                 atomicOr(err, kErrTimeoutProducer);
@@ -1132,7 +1169,7 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
             int stage = 0, wstage = 0, acc = 0;
             uint32_t phase = 0, wphase = 0, acc_phase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
-                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
+                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK) / 2;   // stages of two K panels
                 if (!wait_phase(&sh.accempty[acc], acc_phase ^ 1u, limit_ns, sh.stop, err,
                                       kErrTimeoutMma))
                     goto mma_done;
@@ -1143,11 +1180,14 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
                         !wait_phase(&sh.fullw[wstage], wphase, limit_ns, sh.stop, err, kErrTimeoutMma))
                         goto mma_done;
                     tc_fence_after();
-                    const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wstage * W_STAGE_BYTES));
-                    const uint64_t bdesc = desc_sw128_kmajor(smem_u32(xs + stage * C::X_HALF));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | kk) != 0);
+                    for (int pp = 0; pp < 2; ++pp) {            // the K panels in order
+                        const uint64_t adesc = desc_sw128_kmajor(smem_u32(ws + wstage * C::W_ST + pp * W_STAGE_BYTES));
+                        const uint64_t bdesc = desc_sw128_kmajor(smem_u32(xs + stage * C::X_ST + pp * C::X_HALF));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | pp | kk) != 0);
+                    }
                     mma_commit_pair_multicast(&sh.emptyx[stage], 0x3);
                     mma_commit_pair_multicast(&sh.emptyw[wstage], 0x3);
                     advance(stage, phase, XS);
@@ -1206,8 +1246,8 @@ __global__ void __launch_bounds__(PairFCfg<TYPE>::THREADS, 1)
         }
         if (u >= 0) {
             const int r = (u & 3) * 32 + lane;                 // this CTA's weight row
-            dequant_role<TYPE, WS, QS>(sh, gp, first, stride, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns,
-                                         err);
+            dequant_role<TYPE, WS, QS, 2>(sh, gp, first, stride, qslots, smem_u32(ws), r, u >> 2, lane, limit_ns,
+                                            err);
         }
     }
 
