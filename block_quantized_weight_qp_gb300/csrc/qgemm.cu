@@ -833,10 +833,14 @@ __device__ __forceinline__ void drain_acc(uint32_t taddr, const CUtensorMap *tmY
     }
 }
 
+// A stage holds two 64-value K panels, each this CTA's A half and B half, so
+// the MMA thread and the producer meet once per 128 values of K (as in the
+// fused pair kernel).
 template <int ACC> struct PairCfg {
-    static constexpr int ST = 6, EPI = 2;
+    static constexpr int ST = 3, EPI = 2;
     static constexpr int HALF_BYTES = 128 * BK * 2;              // 16 KiB
-    static constexpr int STAGE_BYTES = 2 * HALF_BYTES;           // A half + B half
+    static constexpr int PANEL_BYTES = 2 * HALF_BYTES;           // A half + B half of one K panel
+    static constexpr int STAGE_BYTES = 2 * PANEL_BYTES;          // two K panels
     static constexpr int OFF_EPI = ST * STAGE_BYTES;             // 4 epilogue warps x EPI x 4 KiB
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI * 4096;
     static constexpr int NBAR = 2 * ST + 5;                      // full, empty, accfull[2], accempty[2], done
@@ -899,29 +903,37 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
     if (alloc_ok && warp == 0) {
         // --------------------------------------------------------- producer --
         if (lane == 0) {
-            int stage = 0, loads = 0;
+            int stage = 0, loads = 0, skip_arm = -1;   // loads: stages armed
             uint32_t phase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
                 const TileLoc L = locate(gp, tile);
                 const int m0 = 2 * L.m0 + 128 * static_cast<int>(rank), n0 = L.n0 + 128 * static_cast<int>(rank);
                 const CUtensorMap *tmX = &gp.tmX[L.g], *tmW = &gp.tmW[L.g];
-                for (int k = 0; k < gp.nk[L.g] * (SB / BK); ++k) {
+                for (int k = 0; k < gp.nk[L.g] * (SB / BK); k += 2) {   // K panels k, k + 1
                     if (!wait_phase(&empty[stage], phase ^ 1u, limit_ns, stop, err, kErrTimeoutProducer))
                         goto producer_done;
                     const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0u);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P::STAGE_BYTES);
                     uint8_t *st = stages + stage * P::STAGE_BYTES;
-                    if (loads++ != inject_stall) {   // test hook: leave one stage's copies unissued
-                        tma_load_2d_pair(st, tmW, bar, k * BK, m0);
-                        tma_load_2d_pair(st + P::HALF_BYTES, tmX, bar, k * BK, n0);
+                    // test hook: loads counted in panels; the stage holding the
+                    // named panel gets no copies at all
+                    if (inject_stall == 2 * loads || inject_stall == 2 * loads + 1) {
+                        skip_arm = loads;
+                    } else {
+#pragma unroll
+                        for (int pp = 0; pp < 2; ++pp) {
+                            tma_load_2d_pair(st + pp * P::PANEL_BYTES, tmW, bar, (k + pp) * BK, m0);
+                            tma_load_2d_pair(st + pp * P::PANEL_BYTES + P::HALF_BYTES, tmX, bar, (k + pp) * BK, n0);
+                        }
                     }
+                    ++loads;
                     advance(stage, phase, P::ST);
                 }
             }
         producer_done:
             // The leader's stage barriers count both CTAs' bytes: once every
             // phase it armed has completed, every copy of both has landed.
-            if (rank == 0 && !drain_ring(full, P::ST, loads, inject_stall, limit_ns)) {
+            if (rank == 0 && !drain_ring(full, P::ST, loads, skip_arm, limit_ns)) {
                 *drain_failed = 1u;
                 atomicOr(err, kErrTimeoutProducer);
             }
@@ -933,7 +945,7 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             for (int tile = first; tile < gp.num_tiles; tile += stride) {
-                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK);
+                const int nks = gp.nk[locate(gp, tile).g] * (SB / BK) / 2;   // stages of two K panels
                 if (!wait_phase(&accempty[acc], acc_phase ^ 1u, limit_ns, stop, err, kErrTimeoutMma))
                     goto mma_done;
                 tc_fence_after();
@@ -941,12 +953,15 @@ __global__ void __launch_bounds__(PairCfg<ACC>::THREADS, 1)
                 for (int k = 0; k < nks; ++k) {
                     if (!wait_phase(&full[stage], phase, limit_ns, stop, err, kErrTimeoutMma)) goto mma_done;
                     tc_fence_after();
-                    uint8_t *st = stages + stage * P::STAGE_BYTES;
-                    const uint64_t adesc = desc_sw128_kmajor(smem_u32(st));
-                    const uint64_t bdesc = desc_sw128_kmajor(smem_u32(st + P::HALF_BYTES));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | kk) != 0);
+                    for (int pp = 0; pp < 2; ++pp) {            // the K panels in order
+                        uint8_t *st = stages + stage * P::STAGE_BYTES + pp * P::PANEL_BYTES;
+                        const uint64_t adesc = desc_sw128_kmajor(smem_u32(st));
+                        const uint64_t bdesc = desc_sw128_kmajor(smem_u32(st + P::HALF_BYTES));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_f16_ss_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC_PAIR, (k | pp | kk) != 0);
+                    }
                     mma_commit_pair_multicast(&empty[stage], 0x3);
                     advance(stage, phase, P::ST);
                 }
