@@ -646,6 +646,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         // needs consumers past their own dependency wait, so the time limit
         // never runs while the previous grid does.  F16 weights may be such a
         // kernel's output: their producer waits first.
+        // The first NST tiles go out one at a time, each once the one before
+        // it has landed (a wait on copies only, so it too ends while the
+        // previous grid runs): every CTA's first tile then reaches the SM
+        // without the rest of all CTAs' prefill in the DRAM queues beside it,
+        // and the consumers start sooner.  Past the prefill, tiles go out as
+        // slots free up, several in flight.
         if constexpr (TYPE == kF16) grid_dependency_wait();
         // The CTA's tiles in order: block after block, each block's tiles
         // 0 .. ntiles - 1; tile n goes to slot n % NST.
@@ -657,6 +663,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
             for (int j = 0; j < L.ntiles; ++j, ++n) {
                 const int s = n % S::NST;
                 if (TYPE != kF16 && n == S::NST) grid_dependency_wait();
+                if (n > 0 && n < S::NST &&
+                    !wait_phase_warp(&full[n - 1], 0u, gp.limit_ns, stop, gp.err, kErrTimeoutGemv)) {
+                    ok = false;
+                    break;
+                }
                 if (!wait_phase_warp(&empty[s], ((n / S::NST) & 1) ^ 1u, gp.limit_ns, stop, gp.err,
                                      kErrTimeoutGemv)) {
                     ok = false;
