@@ -617,7 +617,19 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
     constexpr int SPW = S::S >= NC ? S::S / NC : 1;       // steps per warp and tile
     static_assert(S::S >= NC ? S::S % NC == 0 : NC % S::S == 0, "steps per tile");
     extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ float part[2][NC][ROWS][8 / NSB];          // each consumer warp's 16 weight rows x tokens, 2 buffers
+    // Block end.  K-quants with NSB >= 2: no barrier; each warp publishes its
+    // partial tile and counts itself in, and the warp that completes a
+    // block's count sums the eight tiles.  NBUF = NST + 1 buffers: a warp
+    // reaches block B only once every warp has released the first tile of
+    // block B - NBUF + 1 (B's first tile reuses the slot of a tile NST
+    // earlier, and every block has at least one tile), that is, once every
+    // warp, the summing one included, is done with block B - NBUF.  Else
+    // (Q8_0, F16, and K-quants at NSB = 1, whose tiles would not fit beside
+    // the ring): one named barrier per block over two buffers.
+    constexpr bool LAST_SUMS = kIsKQuant<TYPE> && NSB >= 2;
+    constexpr int NBUF = LAST_SUMS ? S::NST + 1 : 2;
+    __shared__ float part[NBUF][NC][ROWS][8 / NSB];       // each consumer warp's 16 weight rows x tokens
+    __shared__ uint32_t arrivals[NBUF];                   // warps counted in, over every use of the buffer
     __shared__ __align__(8) uint64_t full[S::NST], empty[S::NST];
     __shared__ uint32_t stop_word, drain_failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -629,6 +641,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         }
         stop_word = 0u;
         drain_failed = 0u;
+        for (int k = 0; k < NBUF; ++k) arrivals[k] = 0u;
         for (int k = 0; k < gp.n; ++k)
             if (gp.g[k].use_tma) prefetch_tensormap(&gp.tmW[k]);
         mbar_fence_init();
@@ -846,7 +859,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
             // block's tile into the other buffer, and it reaches the block
             // after that only past the next block's barrier, which this
             // block's readers reach after their reads; so one barrier a block.
-            float (&pw)[ROWS][8 / NSB] = part[nb & 1][warp];
+            const int buf = nb % NBUF;
+            float (&pw)[ROWS][8 / NSB] = part[buf][warp];
             if constexpr (NSB == 1) {
                 pw[g][2 * c] = v[0];
                 pw[g][2 * c + 1] = v[1];
@@ -864,13 +878,34 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                     pw[g + 8][2 * c / NSB] = y1;
                 }
             }
-            named_barrier_sync(1, NC * 32);
-            for (int o = threadIdx.x; o < ROWS * (8 / NSB); o += NC * 32) {
-                const int tt = o / ROWS, r = o % ROWS;    // consecutive threads: consecutive rows of Y
-                float y = 0.0f;
+            if constexpr (LAST_SUMS) {
+                __syncwarp();                             // the warp's tile stores precede lane 0's release
+                uint32_t before = 0u;
+                if (lane == 0) {
+                    __threadfence_block();
+                    before = atomicAdd(&arrivals[buf], 1u);
+                    __threadfence_block();
+                }
+                before = __shfl_sync(0xffffffffu, before, 0);
+                __syncwarp();                             // lane 0's acquire precedes the warp's reads
+                if (before == static_cast<uint32_t>(NC * (nb / NBUF + 1) - 1)) {
+                    for (int o = lane; o < ROWS * (8 / NSB); o += 32) {
+                        const int tt = o / ROWS, r = o % ROWS;
+                        float y = 0.0f;
 #pragma unroll
-                for (int w = 0; w < NC; ++w) y += part[nb & 1][w][r][tt];
-                if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = y;
+                        for (int w = 0; w < NC; ++w) y += part[buf][w][r][tt];
+                        if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = y;
+                    }
+                }
+            } else {
+                named_barrier_sync(1, NC * 32);
+                for (int o = threadIdx.x; o < ROWS * (8 / NSB); o += NC * 32) {
+                    const int tt = o / ROWS, r = o % ROWS;    // consecutive threads: consecutive rows of Y
+                    float y = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < NC; ++w) y += part[buf][w][r][tt];
+                    if (tt < T && L.m0 + r < P.out_f) P.Y[static_cast<int64_t>(tt) * P.out_f + L.m0 + r] = y;
+                }
             }
             ++nb;
         }
