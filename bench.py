@@ -356,6 +356,12 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
     launches of each step only).  GB/s counts the weight bytes plus the X and
     Y bytes of a step.
 
+    Also timed, as a decode loop runs layer after layer: STACK copies of the
+    layer (each its own copy of the weights, so four layers hold 353 MB for
+    the Q2_K one, more than L2) launched back to back in one graph; reported
+    per layer.  There each launch's ring prefill overlaps the previous
+    launch's tail, which a single layer timed alone cannot show.
+
     L2 flush: the 256 MB write evicts the weights, and the following read of
     another 256 MB buffer leaves the L2 holding only clean lines, as it does
     when a decode step streams a layer's weights after the previous layer's
@@ -420,8 +426,26 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
             us = statistics.mean(e[k][0].elapsed_time(e[k][1]) for e in evl) * 1e3
             per_launch["%s:%s" % (synth.NAMES[qt], ",".join(wl["projections"][i][0] for i in idx))] = {
                 "us": round(us, 2), "weight_bytes": wb, "weight_gbs": round(wb / (us / 1e6) / 1e9, 1)}
+        # STACK layers back to back, each with its own copy of the weights and Y
+        STACK = 4
+        Wst = [layer.W] + [[w.clone() for w in layer.W] for _ in range(STACK - 1)]
+        Yst = [Y] + [[torch.empty_like(y) for y in Y] for _ in range(STACK - 1)]
+
+        def stacked(st):
+            for li in range(STACK):
+                for qt, idx in layer.launches(True):
+                    descs = [(Wst[li][i], wl["projections"][i][1], wl["projections"][i][2],
+                              X[wl["projections"][i][3]], Yst[li][i]) for i in idx]
+                    qp.qp_decode_gemv_group(qt, descs, T, st)
+        stacked(stream)
+        torch.cuda.synchronize()
+        graphs["stacked"] = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graphs["stacked"], stream=cap):
+                stacked(cap)
+        torch.cuda.synchronize()
         res = {}
-        for how in ("grouped", "single", "eager"):
+        for how in ("grouped", "single", "eager", "stacked"):
             for _ in range(3):                   # untimed warm-up of this way of launching
                 flush_l2()
                 if how == "eager":
@@ -440,14 +464,19 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
             torch.cuda.synchronize()
             res[how] = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
         qp.qp_check(stream)
-        del graphs
+        del graphs, Wst, Yst
         ms = res["grouped"]
         nbytes = wbytes + sum(x.numel() * 2 for x in X.values()) + sum(y.numel() * 4 for y in Y)
         gbs = nbytes / (ms / 1e3) / 1e9
+        ms_l = res["stacked"] / STACK
+        gbs_l = nbytes / (ms_l / 1e3) / 1e9
         out["T%d" % T] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1),
                           "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 1),
                           "tok_per_s": round(T / (ms / 1e3), 1), "eager_ms": round(res["eager"], 4),
-                          "one_launch_per_projection_ms": round(res["single"], 4), "per_launch_eager": per_launch}
+                          "one_launch_per_projection_ms": round(res["single"], 4), "per_launch_eager": per_launch,
+                          "layers_back_to_back": {"layers": STACK, "ms_per_layer": round(ms_l, 4),
+                                                  "gbs": round(gbs_l, 1),
+                                                  "pct_hbm": round(100.0 * gbs_l / peaks["hbm_gbs"], 1)}}
     del flush, flush_rd
     return out
 
