@@ -103,13 +103,15 @@ def test_decode_gemv_is_deterministic(cuda_device):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+@pytest.mark.parametrize("T", [1, 5])
 @pytest.mark.parametrize("qtype", [qp.Q8_0, qp.Q2_K, qp.Q4_K, qp.Q5_K, qp.Q6_K, qp.F16])
-def test_grouped_decode_gemv_equals_single_calls_bitwise(cuda_device, qtype):
+def test_grouped_decode_gemv_equals_single_calls_bitwise(cuda_device, qtype, T):
     """One launch over several projections (own X, own Y each, the long-K
-    one included) gives every Y bitwise as its own call does."""
+    one and a one-superblock one included) gives every Y bitwise as its own
+    call does.  T = 1: the K-quant blocks end without a barrier (the warp
+    that completes a block's count sums it); T = 5: with one."""
     import torch
-    shapes = [(37, 1024), (256, 4096), (8, 2048), (1029, 1024), (64, 12288)]
-    T = 5
+    shapes = [(37, 1024), (256, 4096), (8, 2048), (1029, 1024), (64, 12288), (4000, 256)]
     ws = [dev(synth.blocks(qtype, o, i, seed=20 + k, tensor=qtype)) for k, (o, i) in enumerate(shapes)]
     xs = [dev(synth.normal_f16((T, i), seed=30 + k, tensor=1)) for k, (o, i) in enumerate(shapes)]
     singles = [gemv(qtype, w, o, i, x, T) for w, (o, i), x in zip(ws, shapes, xs)]
@@ -118,6 +120,23 @@ def test_grouped_decode_gemv_equals_single_calls_bitwise(cuda_device, qtype):
     qp.qp_check()
     for k, (a, b) in enumerate(zip(singles, ys)):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32)), shapes[k]
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("qtype", KQUANTS)
+def test_decode_gemv_many_one_step_blocks_vs_oracle(cuda_device, qtype, T):
+    """Rows of one superblock, 16,000 of them: each 16-row block is a single
+    one-step tile, so seven of a CTA's eight consumer warps have no step in
+    it and run ahead to the ring's depth, and every CTA ends many blocks
+    in a row.  Their partial tiles are summed by whichever warp completes a
+    block's count, from buffers reused every NST + 1 blocks."""
+    out_f, in_f = 16000, 256
+    w = synth.blocks(qtype, out_f, in_f, seed=41 + T, tensor=qtype)
+    X = synth.normal_f16((T, in_f), seed=41 + T, tensor=7)
+    Y = gemv(qtype, dev(w), out_f, in_f, dev(X), T).cpu().numpy()
+    W = oracle.dequant_f32(qtype, w, out_f, in_f)
+    Yref, A = oracle.gemm_f64(X, W)
+    assert_gemm_within_tolerance(Y, Yref, A, "gemv %d %dx%d T=%d" % (qtype, out_f, in_f, T))
 
 
 def test_decode_gemv_reads_operands_written_just_before(cuda_device):
