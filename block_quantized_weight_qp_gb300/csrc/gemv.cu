@@ -33,8 +33,9 @@
 // A and B so that K slots 2c, 2c + 1, 2c + 8, 2c + 9 hold values 4i .. 4i + 3
 // of lane c's run in MMA i).  Steps past the row's end contribute zeros.  At
 // a block's end the consumer warps' 16 x 8 partial tiles are summed through
-// shared memory in warp order (a named barrier over the consumers only), so
-// results are deterministic.
+// shared memory in warp order, so results are deterministic: for the
+// K-quants at T <= 4 by the warp that completes the block's arrival count
+// (no barrier), otherwise behind a named barrier over the consumers only.
 //
 // Weights whose row pitch is not a multiple of 16 bytes (which a TMA tensor
 // cannot describe) are staged instead by 16 bulk copies a tile, one per row.
