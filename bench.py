@@ -44,9 +44,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the dominant kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum), from one ncu capture of the kernel source whose hash
 # is recorded; reported only while the source is unchanged.
-NCU_TRAFFIC = {"source_sha": "506945d5a072212e", "bytes_per_launch": 1546648832,
-               "what": "fused Q2_K launch over q,k,v,o,gate,up on CTA pairs, T=8192 (read 457.78 MB + write "
-                       "1088.87 MB); algorithmic 1321.9 MB (W 46.8 + X 134.2 + Y 1140.9): X_h is read again by "
+NCU_TRAFFIC = {"source_sha": "8a84ee6a42054f95", "bytes_per_launch": 1559492864,
+               "what": "fused Q2_K launch over q,k,v,o,gate,up on CTA pairs, T=8192 (read 469.54 MB + write "
+                       "1089.96 MB); algorithmic 1321.9 MB (W 46.8 + X 134.2 + Y 1140.9): X_h is read again by "
                        "each projection that shares it, and part of Y is still in L2 at kernel end"}
 KERNEL_SOURCES = ["block_quantized_weight_qp_gb300/csrc/qgemm.cu",
                   "block_quantized_weight_qp_gb300/csrc/qp_ptx.cuh",
