@@ -89,7 +89,7 @@ qp_status device_info(DeviceInfo **out) {
 }
 
 qp::LaunchEnv env_of(const DeviceInfo *d) {
-    return qp::LaunchEnv{d->dev, d->num_sms, d->err, g_wait_limit_ns.load(), g_encode};
+    return qp::LaunchEnv{d->dev, d->num_sms, d->err, g_wait_limit_ns.load(), g_encode, -1};
 }
 
 int64_t qk_of(int t) { return t == qp::kF16 ? 1 : (t == qp::kQ8_0 ? 32 : 256); }
@@ -323,7 +323,9 @@ qp_status run_gemv(int type, const qp_gemm_desc *descs, int n, int64_t T, void *
     for (int i = 0; i < n; ++i)
         a[i] = qp::GemvArgs{descs[i].W, qp_row_bytes(type, descs[i].in_f), descs[i].out_f, descs[i].in_f, T,
                             descs[i].X, descs[i].Y};
-    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), env_of(d)) != cudaSuccess) {
+    qp::LaunchEnv env = env_of(d);
+    env.inject_stall = g_inject_stall.exchange(-1);
+    if (qp::launch_decode_gemv(type, a, n, static_cast<cudaStream_t>(stream), env) != cudaSuccess) {
         cudaGetLastError();
         return QP_ERR_CUDA;
     }

@@ -586,6 +586,7 @@ struct GemvParams {
     int n, T;
     uint32_t *err;
     uint64_t limit_ns;
+    int inject_stall;              // test hook: each CTA's producer arms ring tile n but leaves its copy out
 };
 
 // Block b of the launch: its projection, first weight row, steps per row
@@ -689,11 +690,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                 }
                 uint8_t *const slot = ring + s * TILE;
                 const int64_t off = static_cast<int64_t>(j) * S::S * S::STEP;   // the tile's first byte in a row
+                const bool drop = n == gp.inject_stall;   // test hook: the tile's copy left out
                 if (P.use_tma) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&full[s], TILE);
-                        tma_load_2d(slot, &gp.tmW[L.grp], &full[s], static_cast<int32_t>((off & ~int64_t(15)) >> 3),
-                                    L.m0);
+                        if (!drop)
+                            tma_load_2d(slot, &gp.tmW[L.grp], &full[s],
+                                        static_cast<int32_t>((off & ~int64_t(15)) >> 3), L.m0);
                     }
                 } else if (lane < ROWS) {
                     // row m0 + lane: the 16-byte aligned cover of its S steps
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
                     const uint32_t total = __reduce_add_sync(0x0000ffffu, bytes);
                     __syncwarp(0x0000ffffu);              // the plain stores above precede the arrive
                     if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
-                    if (bytes) bulk_load(dst, a0, bytes, &full[s]);
+                    if (bytes && !drop) bulk_load(dst, a0, bytes, &full[s]);
                 }
                 __syncwarp();
             }
@@ -728,8 +731,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const __grid_cons
         if (lane == 0) {
             bool drained = true;
             for (int m = n - S::NST < 0 ? 0 : n - S::NST; m < n; ++m)
-                drained = wait_drain(&full[m % S::NST], static_cast<uint32_t>((m / S::NST) & 1), gp.limit_ns) &&
-                          drained;
+                if (m != gp.inject_stall)                 // a dropped tile has no copy to wait for
+                    drained = wait_drain(&full[m % S::NST], static_cast<uint32_t>((m / S::NST) & 1), gp.limit_ns) &&
+                              drained;
             if (!drained) {
                 drain_failed = 1u;
                 atomicOr(gp.err, kErrTimeoutGemv);
@@ -964,6 +968,7 @@ cudaError_t launch_nsb(const GemvArgs *a, int n, cudaStream_t stream, const Laun
     gp.T = static_cast<int>(a[0].T);
     gp.err = env.err;
     gp.limit_ns = env.wait_limit_ns;
+    gp.inject_stall = env.inject_stall;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

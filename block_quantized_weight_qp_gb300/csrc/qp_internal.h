@@ -37,6 +37,7 @@ struct LaunchEnv {
     uint32_t *err;         // device error word
     uint64_t wait_limit_ns;
     void *encode_fn;       // cuTensorMapEncodeTiled
+    int inject_stall;      // test hook (decode GEMV): >= 0 makes each CTA's producer drop that ring tile's copy
 };
 
 cudaError_t launch_dequant_f32(int type, const void *blocks, int64_t rows, int64_t cols, float *out,

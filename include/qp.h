@@ -299,12 +299,14 @@ qp_status qp_check(void *stream);
 void qp_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Test hook for the bounded-wait path.  The next GEMM launch made by this
- * process arms the barrier of its `load_index`-th pipeline stage but never
- * issues the copy that would complete it, so the consumers' wait on that
- * stage runs out after the wait limit: the launch records QP_ERR_TIMEOUT
- * (read by qp_check), stops, frees its tensor memory and returns; its output
- * is incomplete.  Applies to one launch only; -1 disarms.  Host only.
+ * Test hook for the bounded-wait path.  The next GEMM or decode GEMV launch
+ * made by this process arms the barrier of its `load_index`-th pipeline stage
+ * (GEMM: the load_index-th 64-value K panel a CTA loads; GEMV: the
+ * load_index-th weight tile of each CTA's ring) but never issues the copy
+ * that would complete it, so the consumers' wait on that stage runs out
+ * after the wait limit: the launch records QP_ERR_TIMEOUT (read by
+ * qp_check), stops, frees its tensor memory and returns; its output is
+ * incomplete.  Applies to one launch only; -1 disarms.  Host only.
  */
 void qp_debug_inject_stall(int load_index);
 

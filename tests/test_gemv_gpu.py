@@ -139,6 +139,38 @@ def test_decode_gemv_many_one_step_blocks_vs_oracle(cuda_device, qtype, T):
     assert_gemm_within_tolerance(Y, Yref, A, "gemv %d %dx%d T=%d" % (qtype, out_f, in_f, T))
 
 
+@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("stall", [1, 6], ids=["prefill_tile", "ring_tile"])
+def test_decode_gemv_bounded_wait_reports_timeout_and_recovers(cuda_device, T, stall):
+    """A ring tile whose copy is never issued (each CTA's tile `stall`: one
+    of the first tiles, which go out one at a time, or one past them): the
+    consumers' wait runs out after the limit, the launch records the timeout
+    and returns, every warp still ending every block (T = 1: the arrival
+    count; T = 5: the named barrier); the next call runs normally in the
+    same context and gives the clean result bit for bit.  34,816 Q2_K rows
+    (2,176 blocks of one tile each) give each of up to 304 CTAs at least
+    seven tiles."""
+    import torch
+    qtype, out_f, in_f = qp.Q2_K, 34816, 4096
+    Wd = dev(synth.blocks(qtype, out_f, in_f, seed=51, tensor=1))
+    Xd = dev(synth.normal_f16((T, in_f), seed=51, tensor=2))
+    Yok = gemv(qtype, Wd, out_f, in_f, Xd, T)
+    qp.qp_set_wait_limit_ns(50_000_000)     # 50 ms
+    try:
+        Y = torch.full((T, out_f), float("nan"), dtype=torch.float32, device="cuda")
+        qp.qp_debug_inject_stall(stall)
+        qp.qp_decode_gemv(qtype, Wd, out_f, in_f, Xd, T, Y)
+        with pytest.raises(qp.QPError) as e:
+            qp.qp_check()
+        assert e.value.status == qp.QP_ERR_TIMEOUT
+        qp.qp_check()                        # the word was cleared
+        Y2 = gemv(qtype, Wd, out_f, in_f, Xd, T)
+        assert torch.equal(Y2.view(torch.int32), Yok.view(torch.int32))
+    finally:
+        qp.qp_set_wait_limit_ns(0)
+        qp.qp_debug_inject_stall(-1)
+
+
 def test_decode_gemv_reads_operands_written_just_before(cuda_device):
     """A GEMV may start while the previous kernel on the stream (one of this
     library's, which let the next launch begin early) still runs.  F16
