@@ -344,7 +344,7 @@ def bench_dequant(qp, stream, device, launches=64, only=None):
     return out
 
 
-def bench_gemv(qp, layer, stream, device, peaks, steps=20):
+def bench_gemv(qp, layer, stream, device, peaks, steps=20, ts=(1, 8)):
     """The decode GEMV over the layer's seven weights for T = 1 and 8 token
     rows, as one grouped launch per block type (qp_decode_gemv_group; for the
     Q2_K layer the six Q2_K projections, then the Q6_K down projection),
@@ -377,7 +377,7 @@ def bench_gemv(qp, layer, stream, device, peaks, steps=20):
         flush_rd.sum()
     wbytes = sum(w.numel() for w in layer.W)
     out = {}
-    for T in (1, 8):
+    for T in ts:
         dims = workloads.input_dims(wl)
         X = {k: torch.from_numpy(synth.normal_f16((T, d), seed=wl["seed"], tensor=3000 + i)).to(device)
              for i, (k, d) in enumerate(dims.items())}
@@ -598,7 +598,8 @@ def main_gemv_only(args):
     peaks, _ = load_peaks()
     stream = torch.cuda.current_stream(device)
     layer = Layer(workloads.WORKLOADS[args.workload], 0, device)
-    print(json.dumps({"decode_gemv": bench_gemv(qp, layer, stream, device, peaks, steps=args.steps)}))
+    ts = (args.gemv_t,) if args.gemv_t else (1, 8)
+    print(json.dumps({"decode_gemv": bench_gemv(qp, layer, stream, device, peaks, steps=args.steps, ts=ts)}))
 
 
 def main_qp(args):
@@ -918,6 +919,8 @@ def parse_args(argv=None):
                    help="cached: the same step over f16 weights made once by qp_dequant_f16")
     p.add_argument("--dequant-only", action="store_true", help="only the standalone dequant rows")
     p.add_argument("--gemv-only", action="store_true", help="only the decode GEMV row")
+    p.add_argument("--gemv-t", type=int, default=0, choices=range(0, 9),
+                   help="with --gemv-only: time this token count only (default: 1 and 8)")
     p.add_argument("--dequant-cases", default=None, help="e.g. Q4_K_f16,Q2_K_f32 (with --dequant-only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-rows", type=int, default=8)

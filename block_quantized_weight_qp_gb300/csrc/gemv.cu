@@ -115,7 +115,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // MMA's 16 K slots belong to NSB consecutive sub-blocks, and its 8 N columns
 // to (token, sub-block) pairs.  K slot pair p (slots 2p, 2p + 1) holds
 // sub-block p % NSB of the group, values i * 16 / NSB + 2 * (p / NSB) + {0, 1}
-// of it in the group's MMA i; column n is token n / NSB restricted to
+// of it in the group's MMA i (NSB = 1 and 2: pairs c and c + 4 hold values
+// 16i / NSB + 4 (c / (2 / NSB)) + {0, 1} and {2, 3} of their sub-block, so that
+// a lane's four X values are one 8-byte load); column n is token n / NSB
+// restricted to
 // sub-block n % NSB (zero in the other sub-blocks' slots), so column n of D
 // sums one sub-block of one token.  NSB = 8 / T rounded up to a power of
 // two: at T = 1 one MMA spans eight sub-blocks and the scales cost two f32x2
@@ -131,9 +134,7 @@ __device__ __align__(16) uint16_t g_zero_x[256];
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
 __device__ __forceinline__ uint32_t lds8(const uint8_t *p) { return *p; }
-__device__ __forceinline__ uint32_t ldx32(const uint16_t *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
-}
+__device__ __forceinline__ uint2 ldx64(const uint16_t *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); }
 __device__ __forceinline__ uint4 ldx128(const uint16_t *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
     return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
@@ -141,7 +142,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
 
 // Bytes 2h, 2h + 1 of w into the low bytes of two fp16 fields.
 __device__ __forceinline__ uint32_t spread(uint32_t w, int h) { return __byte_perm(w, 0u, h ? 0x4342 : 0x4140); }
-__device__ __forceinline__ uint32_t spread_sel(int h) { return h ? 0x4342u : 0x4140u; }
 
 // 2^e as a float, for small integer e (exact scaling).
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
@@ -175,12 +175,14 @@ struct XWords {
             if (i % 2 == 0) qa = ldx128(xa + 4 * i);
             b0 = word_of(qa, 2 * (i % 2));
             b1 = word_of(qa, 2 * (i % 2) + 1);
-        } else if constexpr (NSB == 2) {                // words 4i + c/2, 4i + 2 + c/2 (xa = xb)
-            b0 = ldx32(xa + 8 * i + 2 * (c >> 1));
-            b1 = ldx32(xa + 8 * i + 4 + 2 * (c >> 1));
-        } else {                                        // words 8i + c, 8i + 4 + c (xa = xb)
-            b0 = ldx32(xa + 16 * i + 2 * c);
-            b1 = ldx32(xa + 16 * i + 8 + 2 * c);
+        } else if constexpr (NSB == 2) {                // values 8i + 4(c/2) .. + 3 (xa = xb)
+            const uint2 v = ldx64(xa + 8 * i + 4 * (c >> 1));
+            b0 = v.x;
+            b1 = v.y;
+        } else {                                        // values 16i + 4c .. 16i + 4c + 3 (xa = xb)
+            const uint2 v = ldx64(xa + 16 * i + 4 * c);
+            b0 = v.x;
+            b1 = v.y;
         }
     }
 };
@@ -193,8 +195,8 @@ struct XWords {
 template <int NSB>
 struct Q2Codes {
     static constexpr int SBV = 16, NSUB = 16;
-    uint32_t w[NSB == 1 ? 2 : 4];
-    uint32_t m0, m1, sel;
+    uint32_t w[NSB == 1 ? 1 : (NSB == 2 ? 2 : 4)];
+    uint32_t m0, m1;
     __device__ __forceinline__ void load(const uint8_t *sb, int gm, int c) {
         constexpr uint32_t M = 0x00030003u;
         if constexpr (NSB == 8) {                       // s = 8gm + c, 8gm + c + 4
@@ -208,25 +210,21 @@ struct Q2Codes {
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = lds32(q + 4 * k);
             m0 = m1 = M << (2 * (2 * (gm & 1) + (c >> 1)));
-        } else if constexpr (NSB == 2) {                // s = 2gm + c % 2
-            const uint8_t *q = sb + 16 + 32 * (gm >> 2) + 16 * (c & 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) w[k] = lds32(q + 4 * k);
-            m0 = m1 = M << (2 * (gm & 3));
-            sel = spread_sel(c >> 1);
-        } else {                                        // s = gm
-            const uint8_t *q = sb + 16 + 32 * (gm >> 3) + 16 * (gm & 1) + 4 * (c >> 1);
+        } else if constexpr (NSB == 2) {                // s = 2gm + c % 2, values 8i + 4(c/2) .. + 3
+            const uint8_t *q = sb + 16 + 32 * (gm >> 2) + 16 * (c & 1) + 4 * (c >> 1);
             w[0] = lds32(q);
             w[1] = lds32(q + 8);
+            m0 = m1 = M << (2 * (gm & 3));
+        } else {                                        // s = gm, values 4c .. 4c + 3
+            w[0] = lds32(sb + 16 + 32 * (gm >> 3) + 16 * (gm & 1) + 4 * c);
             m0 = m1 = M << (2 * ((gm & 7) >> 1));
-            sel = spread_sel(c & 1);
         }
     }
     __device__ __forceinline__ uint32_t pair(int i, int p) const {
         if constexpr (NSB == 8) return spread(w[i >> 1], i & 1) & (p ? m1 : m0);
         else if constexpr (NSB == 4) return spread(w[i], p) & m0;
-        else if constexpr (NSB == 2) return prmt_sel(w[2 * i + p], 0u, sel) & m0;
-        else return prmt_sel(w[p], 0u, sel) & m0;
+        else if constexpr (NSB == 2) return spread(w[i], p) & m0;
+        else return spread(w[0], p) & m0;
     }
 };
 
@@ -286,9 +284,8 @@ __device__ __forceinline__ uint32_t q6_code_word(uint32_t wl, uint32_t wh, int h
 template <int NSB, int MIS>
 struct Q6Codes {
     static constexpr int SBV = 16, NSUB = 16;
-    static constexpr int NW = NSB == 1 ? 2 : 4;
+    static constexpr int NW = NSB == 1 ? 1 : (NSB == 2 ? 2 : 4);
     uint32_t u0[NW], u1[NSB == 8 ? 4 : 1];
-    uint32_t sel;
     __device__ __forceinline__ void load(const uint8_t *sb, uint32_t sh, int gm, int c) {
         if constexpr (NSB == 8) {
             // s = 8gm + c (low nibbles, crumb c/2) and 8gm + c + 4 (high nibbles,
@@ -311,31 +308,28 @@ struct Q6Codes {
             const int j = 2 * (gm & 1) + (c >> 1);
 #pragma unroll
             for (int k = 0; k < 4; ++k) u0[k] = q6_code_word(wl[k], wh[k], gm & 1, j);
-        } else if constexpr (NSB == 2) {                       // s = 2gm + c % 2
-            uint32_t wl[4], wh[4];
-            q6_words<MIS, 4>(sb + 64 * (gm >> 2) + 32 * (gm & 1) + 16 * (c & 1), sh, wl);
-            q6_words<MIS, 4>(sb + 128 + 32 * (gm >> 2) + 16 * (c & 1), sh, wh);
+        } else if constexpr (NSB == 2) {                       // s = 2gm + c % 2, values 8i + 4(c/2) .. + 3
+            const int l0 = 16 * (c & 1) + 4 * (c >> 1);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) u0[k] = q6_code_word(wl[k], wh[k], (gm & 3) >= 2, gm & 3);
-            sel = spread_sel(c >> 1);
-        } else {                                               // s = gm
-            const int n = gm >> 3, j = (gm & 7) >> 1, l0 = 16 * (gm & 1) + 4 * (c >> 1);
-            const uint8_t *ql = sb + 64 * n + 32 * (j & 1) + l0, *qh = sb + 128 + 32 * n + l0;
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
+            for (int i = 0; i < 2; ++i) {
                 uint32_t wl[1], wh[1];
-                q6_words<MIS, 1>(ql + 8 * p, sh, wl);
-                q6_words<MIS, 1>(qh + 8 * p, sh, wh);
-                u0[p] = q6_code_word(wl[0], wh[0], j >= 2, j);
+                q6_words<MIS, 1>(sb + 64 * (gm >> 2) + 32 * (gm & 1) + l0 + 8 * i, sh, wl);
+                q6_words<MIS, 1>(sb + 128 + 32 * (gm >> 2) + l0 + 8 * i, sh, wh);
+                u0[i] = q6_code_word(wl[0], wh[0], (gm & 3) >= 2, gm & 3);
             }
-            sel = spread_sel(c & 1);
+        } else {                                               // s = gm, values 4c .. 4c + 3
+            const int n = gm >> 3, j = (gm & 7) >> 1, l0 = 16 * (gm & 1) + 4 * c;
+            uint32_t wl[1], wh[1];
+            q6_words<MIS, 1>(sb + 64 * n + 32 * (j & 1) + l0, sh, wl);
+            q6_words<MIS, 1>(sb + 128 + 32 * n + l0, sh, wh);
+            u0[0] = q6_code_word(wl[0], wh[0], j >= 2, j);
         }
     }
     __device__ __forceinline__ uint32_t pair(int i, int p) const {
         if constexpr (NSB == 8) return spread(p ? u1[i >> 1] : u0[i >> 1], i & 1);
         else if constexpr (NSB == 4) return spread(u0[i], p);
-        else if constexpr (NSB == 2) return prmt_sel(u0[2 * i + p], 0u, sel);
-        else return prmt_sel(u0[p], 0u, sel);
+        else if constexpr (NSB == 2) return spread(u0[i], p);
+        else return spread(u0[0], p);
     }
 };
 
@@ -368,7 +362,6 @@ struct K4Codes {
     static constexpr int SBV = 32, NSUB = 8;
     const uint8_t *q0, *q1, *qh;   // qs words of pairs c and c + 4 (MMA i reads word i * 8 / NSB + ...)
     int hi, s0, s1;                // nibble half; sub-blocks of the pairs (Q5_K's qh bit)
-    uint32_t sel;
     __device__ __forceinline__ void load(const uint8_t *sb, int gm, int c) {
         qh = sb + 16;
         if constexpr (NSB == 8) {                       // s = c, c + 4
@@ -385,12 +378,10 @@ struct K4Codes {
             q0 = q1 = sb + QS + 32 * gm;
             hi = c & 1;
             s0 = s1 = 2 * gm + (c & 1);
-            sel = spread_sel(c >> 1);
         } else {                                        // s = gm
             q0 = q1 = sb + QS + 32 * (gm >> 1);
             hi = gm & 1;
             s0 = s1 = gm;
-            sel = spread_sel(c & 1);
         }
     }
     // the codes of qs word k (and qh word k) of pair p, one per byte
@@ -403,8 +394,8 @@ struct K4Codes {
     __device__ __forceinline__ uint32_t pair(int i, int p, int c) const {
         if constexpr (NSB == 8) return spread(codes(i >> 1, p), i & 1);          // values 2i, 2i + 1
         else if constexpr (NSB == 4) return spread(codes(i, 0), p);              // 4i + 2p ..
-        else if constexpr (NSB == 2) return prmt_sel(codes(2 * i + p, 0), 0u, sel);   // 8i + 4p + 2(c/2) ..
-        else return prmt_sel(codes(4 * i + (c >> 1) + 2 * p, 0), 0u, sel);       // 16i + 8p + 2c ..
+        else if constexpr (NSB == 2) return spread(codes(2 * i + (c >> 1), 0), p);   // 8i + 4(c/2) + 2p ..
+        else return spread(codes(4 * i + c, 0), p);                             // 16i + 4c + 2p ..
     }
 };
 
@@ -521,9 +512,13 @@ __device__ __forceinline__ void step_codes(const uint8_t *r0, const uint8_t *r1,
         // dependency chain is half as long
         float D[4] = {0.0f, 0.0f, 0.0f, 0.0f}, E[4] = {0.0f, 0.0f, 0.0f, 0.0f}, S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int hh = 0; hh < SBV / 16; ++hh)
-            mma_acc(S, kOnesH2, kOnesH2, kOnesH2, kOnesH2, ldx32(xg + xo + 16 * hh + 2 * L.c),
-                    ldx32(xg + xo + 16 * hh + 8 + 2 * L.c));
+        for (int hh = 0; hh < SBV / 16; ++hh) {
+            // A is all ones, so any K order that covers the sub-block's 16
+            // values once does: lane c takes values 4c .. 4c + 3 in one load
+            // (at NSB = 1 the same load as its value MMA's)
+            const uint2 v = ldx64(xg + xo + 16 * hh + 4 * L.c);
+            mma_acc(S, kOnesH2, kOnesH2, kOnesH2, kOnesH2, v.x, v.y);
+        }
         Q q0, q1;
         load_codes<TYPE, NSB, MIS>(q0, r0, sh, gm, L.c);
         load_codes<TYPE, NSB, MIS>(q1, r1, sh, gm, L.c);
