@@ -158,7 +158,9 @@ struct LaneMap {
 
 // The value B words of the lane in MMA i of a group, from the column-g
 // sub-block chunk at xa (pair c) and xb (pair c + 4) (zeros where the lane's
-// pair is not in column g's sub-block): word i * 8 / NSB + (p / NSB) of it.
+// pair is not in column g's sub-block): for NSB >= 4 word i * 8 / NSB +
+// (p / NSB) of it, for NSB <= 2 the four values from 16i / NSB +
+// 4 (c / (2 / NSB)) in one load.
 template <int NSB>
 struct XWords {
     uint4 qa, qb;
