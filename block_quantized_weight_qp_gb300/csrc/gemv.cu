@@ -495,6 +495,46 @@ __device__ __forceinline__ void group_scales(const uint8_t *sb, const RowHead<TY
     else k4_scales<NSB>(h.hd, h.d24, h.ndmin, gm, L, al, be);
 }
 
+// NSB = 1: the factors of rows g and g + 8 (the same sub-block gm) computed
+// together in f32 pairs, the same exact operations as group_scales per row;
+// each row's alpha and beta then fill both of its D columns (the tokens).
+template <int TYPE>
+__device__ __forceinline__ void row_pair_scales(const uint8_t *r0, const uint8_t *r1, const RowHead<TYPE> &h0,
+                                                const RowHead<TYPE> &h1, int gm, pair_t &al0, pair_t &be0,
+                                                pair_t &al1, pair_t &be1) {
+    const pair_t nbias = pk2(-8388608.0f, -8388608.0f);
+    pair_t a, n;
+    if constexpr (TYPE == kQ2_K) {
+        const float p2 = pow2f(24 - 2 * ((gm & 7) >> 1));                  // the crumb's 4^-crumb
+        const uint32_t w = lds8(r0 + gm) | (lds8(r1 + gm) << 8);           // the rows' scale bytes
+        const uint32_t scw = w & 0x0F0Fu, mw = (w >> 4) & 0x0F0Fu;
+        const pair_t sc = fadd2(pk2(bias_float<0>(scw), bias_float<1>(scw)), nbias);   // exact
+        const pair_t m = fadd2(pk2(bias_float<0>(mw), bias_float<1>(mw)), nbias);
+        a = fmul2(pk2(h0.d24 * p2, h1.d24 * p2), sc);                      // exact
+        n = fmul2(pk2(h0.ndmin, h1.ndmin), m);                             // -(dmin * m), exact
+    } else if constexpr (TYPE == kQ6_K) {
+        const uint32_t sx = (lds8(r0 + 192 + gm) | (lds8(r1 + 192 + gm) << 8)) ^ 0x8080u;   // int8 + 128
+        const pair_t sv = fadd2(pk2(bias_float<0>(sx), bias_float<1>(sx)), pk2(-8388736.0f, -8388736.0f));
+        a = fmul2(pk2(h0.d24, h1.d24), sv);                                // d * s * 2^24, exact
+        n = fmul2(a, pk2(-1.9073486328125e-06f, -1.9073486328125e-06f)); // -32 * d * s, exact
+    } else {
+        uint32_t sc0, m0, sc1, m1;
+        k4_sm(h0.hd, gm, sc0, m0);
+        k4_sm(h1.hd, gm, sc1, m1);
+        const pair_t sc = fadd2(pk2(__uint_as_float(0x4B000000u | sc0), __uint_as_float(0x4B000000u | sc1)), nbias);
+        const pair_t m = fadd2(pk2(__uint_as_float(0x4B000000u | m0), __uint_as_float(0x4B000000u | m1)), nbias);
+        a = fmul2(pk2(h0.d24, h1.d24), sc);                                // d * sc * 2^24, exact
+        n = fmul2(pk2(h0.ndmin, h1.ndmin), m);                             // -(dmin * m), exact
+    }
+    float a0, a1, n0, n1;
+    unpk2(a, a0, a1);
+    unpk2(n, n0, n1);
+    al0 = pk2(a0, a0);
+    be0 = pk2(n0, n0);
+    al1 = pk2(a1, a1);
+    be1 = pk2(n1, n1);
+}
+
 // One step (one superblock of rows g and g + 8, at r0 and r1 in the stage)
 // of a K-quant: for each group of NSB sub-blocks, the SX MMA(s), the value
 // MMAs, and acc += alpha * D + beta * SX for the lane's two D columns of each
@@ -537,8 +577,12 @@ __device__ __forceinline__ void step_codes(const uint8_t *r0, const uint8_t *r1,
             for (int k = 0; k < 4; ++k) D[k] += E[k];
         }
         pair_t al0, be0, al1, be1;
-        group_scales<TYPE, NSB>(r0, h0, gm, L, al0, be0);
-        group_scales<TYPE, NSB>(r1, h1, gm, L, al1, be1);
+        if constexpr (NSB == 1) {
+            row_pair_scales<TYPE>(r0, r1, h0, h1, gm, al0, be0, al1, be1);
+        } else {
+            group_scales<TYPE, NSB>(r0, h0, gm, L, al0, be0);
+            group_scales<TYPE, NSB>(r1, h1, gm, L, al1, be1);
+        }
         acc[0] = ffma2(al0, pk2(D[0], D[1]), ffma2(be0, pk2(S[0], S[1]), acc[0]));
         acc[1] = ffma2(al1, pk2(D[2], D[3]), ffma2(be1, pk2(S[2], S[3]), acc[1]));
     }
